@@ -1,0 +1,43 @@
+"""CPU oracle for the ONNX matrix-product family (TEST INFRASTRUCTURE ONLY).
+
+This package is the slow, obviously-correct reference that the CUDA library is
+checked against.  It is written from the operator pages alone and shares no
+code with the CUDA path: nothing under ``quantized_gemm_gb300/`` may import it,
+and it imports nothing from there.  Only ``tests/``, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.
+
+Arithmetic conventions (readings of the pages, listed with reasons in the
+design notes):
+
+* Floating point: every input is widened exactly to float64 and the
+  contraction is done in float64; results are returned unrounded (float64).
+* Integers: contractions are exact modulo 2**64 (uint64 arithmetic) and then
+  reduced modulo 2**n of the operator's type T, i.e. numpy's wrap-around.
+* QLinearMatMul: the int32 accumulator is the exact integer sum reduced
+  modulo 2**32; the requantisation is a fixed sequence of IEEE float32
+  operations (see ``qlinear_matmul``).
+
+Each module cites the page and section it follows:
+
+* ``matmul``          -- MatMul (onnx-light, ai.onnx since version 13)
+* ``gemm``            -- Gemm (onnx-light, ai.onnx since version 13)
+* ``qlinear_matmul``  -- QLinearMatMul - version 10 (onnx-light)
+* ``grouped_matmul``  -- GroupedMatMul - 29 (onnx.ai)
+
+Parity status: every function here is pinned by tests in
+``tests/test_oracle_pins.py`` (printed worked examples, brute force on tiny
+inputs, closed forms and identities); none is "parity unpinned" except the
+integer-Gemm corner with non-integral alpha/beta, which this oracle rejects.
+"""
+
+from .matmul import matmul, matmul_output_shape, matmul_abs_scale
+from .gemm import gemm, gemm_output_shape, gemm_abs_scale
+from .qlinear_matmul import qlinear_matmul, requantize
+from .grouped_matmul import grouped_matmul, grouped_abs_scale
+
+__all__ = [
+    "matmul", "matmul_output_shape", "matmul_abs_scale",
+    "gemm", "gemm_output_shape", "gemm_abs_scale",
+    "qlinear_matmul", "requantize",
+    "grouped_matmul", "grouped_abs_scale",
+]
