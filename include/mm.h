@@ -1,0 +1,180 @@
+/*
+ * mm.h -- C ABI of the GB300 (sm_103a) library for the ONNX matrix-product
+ * operator family: MatMul, Gemm, QLinearMatMul and GroupedMatMul.
+ *
+ * Every entry point takes plain pointers and sizes; no C++ or framework type
+ * crosses this boundary.  All computation runs in this library's own CUDA
+ * kernels on the caller's stream; there is no CPU fallback.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ * Tensors.  An mm_tensor names caller-owned DEVICE memory (`data`), an element
+ *   type, a rank (0..MM_MAX_DIMS), a shape and per-dimension strides counted in
+ *   ELEMENTS (not bytes).  Input strides may be any non-negative values,
+ *   including 0 (a broadcast view).  Output tensors (Y, y, output) must be
+ *   dense row-major (strides equal to the suffix products of the shape) and
+ *   must not overlap any input.
+ * Shapes.  Outputs are preallocated by the caller with exactly the shape and
+ *   type the operator infers (the *_output_shape helpers compute it); any other
+ *   shape returns MM_ERR_SHAPE and any other type MM_ERR_DTYPE.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Calls are asynchronous: the return value reports host-side
+ *   validation and launch errors only.  Device-side conditions (an out-of-range
+ *   group index, a pipeline wait that timed out) are recorded in a per-device
+ *   status word read with mm_get_device_status().
+ * Memory.  The library never allocates device memory.  Operators whose fast
+ *   path needs scratch space (QLinearMatMul, GroupedMatMul) take a
+ *   caller-provided workspace whose size is given by the matching
+ *   *_workspace_size function; the workspace must be 256-byte aligned.
+ * Threads.  Entry points may be called from several host threads; calls that
+ *   share a workspace must be ordered on one stream.
+ */
+#ifndef QGEMM_GB300_MM_H
+#define QGEMM_GB300_MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MM_MAX_DIMS 8
+
+typedef enum mm_status {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,  /* NULL pointer, rank out of range, negative size or stride, bad attribute */
+  MM_ERR_SHAPE = 2,        /* shapes violate the operator's rules, or the output has the wrong shape/layout */
+  MM_ERR_DTYPE = 3,        /* an element type outside the operator's type constraints */
+  MM_ERR_UNSUPPORTED = 4,  /* a case the pages leave undefined, or a forced path that cannot run it */
+  MM_ERR_WORKSPACE = 5,    /* workspace NULL, too small or not 256-byte aligned */
+  MM_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed */
+  MM_ERR_TIMEOUT = 7,      /* device side: a pipeline wait exceeded its limit and the kernel gave up */
+  MM_ERR_INDEX_RANGE = 8   /* device side: a GroupedMatMul index outside [0, G) was seen */
+} mm_status;
+
+typedef enum mm_dtype {
+  MM_BF16 = 0, MM_F16 = 1, MM_F32 = 2, MM_F64 = 3,
+  MM_I32 = 4, MM_I64 = 5, MM_U32 = 6, MM_U64 = 7,
+  MM_I8 = 8, MM_U8 = 9
+} mm_dtype;
+
+typedef struct mm_tensor {
+  void* data;                      /* device pointer, caller-owned */
+  int32_t dtype;                   /* an mm_dtype value */
+  int32_t ndim;                    /* 0 .. MM_MAX_DIMS */
+  int64_t shape[MM_MAX_DIMS];
+  int64_t strides[MM_MAX_DIMS];    /* in elements */
+} mm_tensor;
+
+/* Which kernel family runs a call (see mm_set_path_policy / mm_last_path). */
+typedef enum mm_path {
+  MM_PATH_AUTO = 0,    /* policy only: let the planner choose */
+  MM_PATH_SIMT = 1,    /* CUDA-core kernels (every type, every stride pattern) */
+  MM_PATH_TENSOR = 2,  /* tcgen05 tensor-core kernels (bf16/f16 and 8-bit quantized operands) */
+  MM_PATH_NONE = 3     /* result only: no kernel was needed (an empty output) */
+} mm_path;
+
+/* Human-readable name of a status code; never NULL. */
+const char* mm_status_string(mm_status status);
+
+/* Library version string, e.g. "0.1.0". */
+const char* mm_version(void);
+
+/* Process-wide planner policy (MM_PATH_AUTO by default).  MM_PATH_SIMT forces
+ * the CUDA-core kernels; MM_PATH_TENSOR forces the tensor-core kernels and
+ * makes calls they cannot run return MM_ERR_UNSUPPORTED.  Meant for tests and
+ * measurements.  Returns MM_ERR_INVALID_ARG for an unknown value. */
+mm_status mm_set_path_policy(int32_t policy);
+
+/* The mm_path taken by the most recent successful compute call made on the
+ * calling host thread (MM_PATH_NONE before any). */
+int32_t mm_last_path(void);
+
+/* ---------------------------------------------------------------- MatMul
+ * MatMul (onnx-light operator page, ai.onnx MatMul since version 13; summary
+ * and Examples): Y = A @ B with numpy.matmul semantics.  A 1-D A is promoted to
+ * [1, K] and a 1-D B to [K, 1], the promoted dimension being removed from Y;
+ * leading (batch) dimensions are right-aligned and broadcast (each pair equal
+ * or containing a 1).  T is one of bf16, f16, f32, f64, i32, i64, u32, u64 and
+ * is shared by A, B and Y.
+ * Arithmetic: bf16/f16 and f32 accumulate in fp32 (f32 uses FFMA, never TF32),
+ * f64 in fp64, then one round-to-nearest-even conversion to T; integer types
+ * wrap modulo 2^n.  K = 0 gives zeros. */
+mm_status mm_matmul_output_shape(const mm_tensor* A, const mm_tensor* B,
+                                 int32_t* out_ndim, int64_t* out_shape /* [MM_MAX_DIMS] */);
+mm_status mm_matmul(const mm_tensor* A, const mm_tensor* B, const mm_tensor* Y, void* stream);
+
+/* ---------------------------------------------------------------- Gemm
+ * Gemm (onnx-light operator page, ai.onnx Gemm since version 13; definition
+ * and Inputs/Outputs): Y = alpha * A' * B' + beta * C, A' = A^T if transA != 0
+ * else A (A is (M,K) or (K,M)), B' = B^T if transB != 0 else B (B is (K,N) or
+ * (N,K)), Y is (M,N).  C is optional (NULL = absent = scalar 0) and
+ * unidirectionally broadcastable to (M,N): rank <= 2, right-aligned, each
+ * dimension equal to the target or 1.  ONNX defaults are alpha = beta = 1,
+ * transA = transB = 0.  Float T: y = alpha*acc + beta*c evaluated in fp32
+ * (fp64 for f64), rounded once to T.  Integer T: alpha and beta must be
+ * integral (else MM_ERR_UNSUPPORTED) and Y is exact modulo 2^n. */
+mm_status mm_gemm_output_shape(const mm_tensor* A, const mm_tensor* B, int64_t transA, int64_t transB,
+                               int32_t* out_ndim, int64_t* out_shape /* [MM_MAX_DIMS] */);
+mm_status mm_gemm(const mm_tensor* A, const mm_tensor* B, const mm_tensor* C /* NULL = absent */,
+                  float alpha, float beta, int64_t transA, int64_t transB,
+                  const mm_tensor* Y, void* stream);
+
+/* ---------------------------------------------------------------- QLinearMatMul
+ * QLinearMatMul - version 10 (onnx-light operator page source; summary,
+ * Inputs, Type Constraints): numpy.matmul of 8-bit operands with
+ *   acc = sum_k (a - a_zero_point) * (b - b_zero_point)   exact, wrapped to int32,
+ *   y   = saturate(round_half_even(x / y_scale) + y_zero_point),
+ * where x is evaluated in IEEE fp32 as  s = a_scale*b_scale; v = float(acc)*s;
+ * q = v / y_scale  (each a correctly rounded fp32 operation, in this order) and
+ * saturate clamps to [-128,127] (int8) or [0,255] (uint8).  Results are
+ * bit-exact with that definition.
+ * Types: a/a_zero_point share T1, b/b_zero_point share T2, y/y_zero_point share
+ * T3, each MM_I8 or MM_U8; scales are MM_F32 (MM_F16 is also accepted and is
+ * widened exactly to fp32).
+ * Parameter shapes: a scale and its zero point have the same shape.  One
+ * element = per tensor.  Per row of a: [M] (2-D a) or a.shape[:-1] + [1].
+ * Per column of b: [N] (2-D b) or b.shape[:-2] + [1, N].  y_scale and
+ * y_zero_point are per tensor.  Scales and zero points are device tensors.
+ * The output shape is mm_matmul_output_shape(a, b).
+ * Workspace: mm_qlinear_matmul_workspace_size() bytes (0 when the planner uses
+ * the CUDA-core kernel, which needs none). */
+mm_status mm_qlinear_matmul_workspace_size(const mm_tensor* a, const mm_tensor* b, size_t* bytes);
+mm_status mm_qlinear_matmul(const mm_tensor* a, const mm_tensor* a_scale, const mm_tensor* a_zero_point,
+                            const mm_tensor* b, const mm_tensor* b_scale, const mm_tensor* b_zero_point,
+                            const mm_tensor* y_scale, const mm_tensor* y_zero_point,
+                            const mm_tensor* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- GroupedMatMul
+ * GroupedMatMul - 29 (onnx.ai operator page; Summary, Inputs, Outputs, Type
+ * Constraints): input [M,K], weights [G,K,N], group_indices [M,S] (MM_I32 or
+ * MM_I64), optional bias [G,N] (NULL = absent), output [M,S,N]:
+ *   output[m,i,:] = input[m,:] @ weights[g,:,:] (+ bias[g,:]),  g = group_indices[m,i].
+ * T is bf16, f16, f32 or f64.  The selected weights are never materialised:
+ * rows are routed to their group on the device and each group's rows are
+ * multiplied by weights[g] in place.  Accumulation as for MatMul; the bias is
+ * added to the accumulator before the single rounding to T.
+ * Indices outside [0, G) are invalid input (undefined on the page).  Here the
+ * kernels never read out of bounds for them: the affected output rows are
+ * written as zeros and MM_ERR_INDEX_RANGE is recorded in the device status.
+ * Workspace: mm_grouped_matmul_workspace_size() bytes. */
+mm_status mm_grouped_matmul_workspace_size(const mm_tensor* input, const mm_tensor* weights,
+                                           const mm_tensor* group_indices, size_t* bytes);
+mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights,
+                            const mm_tensor* group_indices, const mm_tensor* bias /* NULL = absent */,
+                            const mm_tensor* output, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------- device status
+ * Synchronises `stream`, then returns and clears the device-side status of the
+ * current device: MM_OK, MM_ERR_INDEX_RANGE or MM_ERR_TIMEOUT (the first set,
+ * in that order of precedence: TIMEOUT over INDEX_RANGE), or MM_ERR_CUDA if the
+ * synchronisation itself failed. */
+mm_status mm_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_GB300_MM_H */

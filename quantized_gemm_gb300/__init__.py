@@ -1,0 +1,207 @@
+"""Python binding of the GB300 ONNX matrix-product library (include/mm.h).
+
+Argument marshalling only: every function below turns torch tensors into the
+C ABI's ``mm_tensor`` descriptors (device pointer, type, shape, element
+strides), allocates the output (and, where the fast path needs one, the
+workspace) with torch's allocator, and calls the library's entry point of the
+same name on the current CUDA stream.  All arithmetic runs in the library's
+CUDA kernels; there is no fallback of any kind, and importing a function whose
+shared library was not built raises immediately.
+"""
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MMError", "mm_matmul", "mm_gemm", "mm_qlinear_matmul", "mm_grouped_matmul",
+    "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_version", "library_path",
+    "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
+]
+
+MM_MAX_DIMS = 8
+MM_PATH_AUTO, MM_PATH_SIMT, MM_PATH_TENSOR, MM_PATH_NONE = 0, 1, 2, 3
+_STATUS = ["MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_SHAPE", "MM_ERR_DTYPE", "MM_ERR_UNSUPPORTED",
+           "MM_ERR_WORKSPACE", "MM_ERR_CUDA", "MM_ERR_TIMEOUT", "MM_ERR_INDEX_RANGE"]
+
+_DTYPES = {
+    torch.bfloat16: 0, torch.float16: 1, torch.float32: 2, torch.float64: 3,
+    torch.int32: 4, torch.int64: 5, torch.uint32: 6, torch.uint64: 7,
+    torch.int8: 8, torch.uint8: 9,
+}
+
+
+def library_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqgemm_gb300.so")
+
+
+class MMTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * MM_MAX_DIMS), ("strides", ctypes.c_int64 * MM_MAX_DIMS)]
+
+
+class MMError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        self.name = _STATUS[status] if 0 <= status < len(_STATUS) else "unknown"
+        super().__init__("%s: %s" % (where, _lib().mm_status_string(status).decode()))
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError("the CUDA library %s is not built; run __graft_entry__.build() "
+                               "(or python -m quantized_gemm_gb300.build)" % path)
+        lib = ctypes.CDLL(path)
+        P, I32, I64, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        T = ctypes.POINTER(MMTensor)
+        sigs = {
+            "mm_status_string": ([I32], ctypes.c_char_p),
+            "mm_version": ([], ctypes.c_char_p),
+            "mm_set_path_policy": ([I32], I32),
+            "mm_last_path": ([], I32),
+            "mm_matmul_output_shape": ([T, T, ctypes.POINTER(I32), ctypes.POINTER(I64)], I32),
+            "mm_matmul": ([T, T, T, P], I32),
+            "mm_gemm_output_shape": ([T, T, I64, I64, ctypes.POINTER(I32), ctypes.POINTER(I64)], I32),
+            "mm_gemm": ([T, T, T, F, F, I64, I64, T, P], I32),
+            "mm_qlinear_matmul_workspace_size": ([T, T, ctypes.POINTER(SZ)], I32),
+            "mm_qlinear_matmul": ([T, T, T, T, T, T, T, T, T, P, SZ, P], I32),
+            "mm_grouped_matmul_workspace_size": ([T, T, T, ctypes.POINTER(SZ)], I32),
+            "mm_grouped_matmul": ([T, T, T, T, T, P, SZ, P], I32),
+            "mm_get_device_status": ([P], I32),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def _desc(t):
+    """mm_tensor describing torch tensor ``t`` (None -> NULL)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    if t.dim() > MM_MAX_DIMS:
+        raise ValueError("at most %d dimensions" % MM_MAX_DIMS)
+    d = MMTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.strides[i] = st
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream(t, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise MMError(status, where)
+
+
+def _out_shape(fn, *args):
+    nd = ctypes.c_int32()
+    shape = (ctypes.c_int64 * MM_MAX_DIMS)()
+    _check(fn(*args, ctypes.byref(nd), shape), fn.__name__)
+    return tuple(shape[i] for i in range(nd.value))
+
+
+def _workspace(nbytes, device):
+    if nbytes == 0:
+        return None, 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, nbytes
+
+
+def mm_version():
+    return _lib().mm_version().decode()
+
+
+def mm_set_path_policy(policy):
+    _check(_lib().mm_set_path_policy(policy), "mm_set_path_policy")
+
+
+def mm_last_path():
+    return _lib().mm_last_path()
+
+
+def mm_matmul(A, B, out=None, stream=None):
+    """Y = A @ B with numpy.matmul semantics (MatMul, opset 13)."""
+    lib = _lib()
+    dA, dB = _desc(A), _desc(B)
+    shape = _out_shape(lib.mm_matmul_output_shape, _ref(dA), _ref(dB))
+    Y = torch.empty(shape, dtype=A.dtype, device=A.device) if out is None else out
+    _check(lib.mm_matmul(_ref(dA), _ref(dB), _ref(_desc(Y)), _stream(A, stream)), "mm_matmul")
+    return Y
+
+
+def mm_gemm(A, B, C=None, alpha=1.0, beta=1.0, transA=0, transB=0, out=None, stream=None):
+    """Y = alpha * A' @ B' + beta * C (Gemm, opset 13)."""
+    lib = _lib()
+    dA, dB = _desc(A), _desc(B)
+    shape = _out_shape(lib.mm_gemm_output_shape, _ref(dA), _ref(dB), int(transA), int(transB))
+    Y = torch.empty(shape, dtype=A.dtype, device=A.device) if out is None else out
+    _check(lib.mm_gemm(_ref(dA), _ref(dB), _ref(_desc(C)), float(alpha), float(beta), int(transA), int(transB),
+                       _ref(_desc(Y)), _stream(A, stream)), "mm_gemm")
+    return Y
+
+
+def mm_qlinear_matmul(a, a_scale, a_zero_point, b, b_scale, b_zero_point, y_scale, y_zero_point,
+                      out=None, stream=None):
+    """Quantized matmul of int8/uint8 tensors (QLinearMatMul, opset 10); y has y_zero_point's type."""
+    lib = _lib()
+    da, db = _desc(a), _desc(b)
+    shape = _out_shape(lib.mm_matmul_output_shape, _ref(da), _ref(db))
+    y = torch.empty(shape, dtype=y_zero_point.dtype, device=a.device) if out is None else out
+    nbytes = ctypes.c_size_t()
+    _check(lib.mm_qlinear_matmul_workspace_size(_ref(da), _ref(db), ctypes.byref(nbytes)),
+           "mm_qlinear_matmul_workspace_size")
+    ws, wsb = _workspace(nbytes.value, a.device)
+    _check(lib.mm_qlinear_matmul(_ref(da), _ref(_desc(a_scale)), _ref(_desc(a_zero_point)), _ref(db),
+                                 _ref(_desc(b_scale)), _ref(_desc(b_zero_point)), _ref(_desc(y_scale)),
+                                 _ref(_desc(y_zero_point)), _ref(_desc(y)),
+                                 None if ws is None else ws.data_ptr(), wsb, _stream(a, stream)),
+           "mm_qlinear_matmul")
+    return y
+
+
+def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream=None):
+    """output[m, i] = input[m] @ weights[group_indices[m, i]] (+ bias[g]) (GroupedMatMul, opset 29)."""
+    lib = _lib()
+    dx, dw, dg = _desc(input), _desc(weights), _desc(group_indices)
+    M, S, N = input.shape[0], group_indices.shape[1], weights.shape[2]
+    y = torch.empty((M, S, N), dtype=input.dtype, device=input.device) if out is None else out
+    nbytes = ctypes.c_size_t()
+    _check(lib.mm_grouped_matmul_workspace_size(_ref(dx), _ref(dw), _ref(dg), ctypes.byref(nbytes)),
+           "mm_grouped_matmul_workspace_size")
+    ws, wsb = _workspace(nbytes.value, input.device)
+    _check(lib.mm_grouped_matmul(_ref(dx), _ref(dw), _ref(dg), _ref(_desc(bias)), _ref(_desc(y)),
+                                 None if ws is None else ws.data_ptr(), wsb, _stream(input, stream)),
+           "mm_grouped_matmul")
+    return y
+
+
+def mm_get_device_status(stream=None, device=None):
+    """Synchronise the stream; return (and clear) the device-side status name, e.g. 'MM_OK'."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    s = _lib().mm_get_device_status(ctypes.c_void_p(stream.cuda_stream))
+    return _STATUS[s]

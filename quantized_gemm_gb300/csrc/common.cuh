@@ -1,0 +1,68 @@
+// Internal types shared by the host planner and the CUDA kernels.
+//
+// An operand of any operator is described as a batch of 2-D matrices: a
+// broadcast batch shape (BatchMap, row-major, shared by all operands of one
+// call) plus, per operand, one element stride per batch dimension (0 where the
+// operand is broadcast) and the element strides of its two matrix dimensions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "mm.h"
+
+namespace qg {
+
+constexpr int kMaxBatchDims = MM_MAX_DIMS - 2;
+
+struct BatchMap {
+  int nb;                          // number of batch dimensions
+  int64_t shape[kMaxBatchDims];    // broadcast batch shape
+  int64_t count;                   // product of shape (1 when nb == 0)
+};
+
+struct MatView {                   // X[b, r, c] = ptr[boff(b) + r*rs + c*cs]
+  const void* ptr;
+  int64_t bstride[kMaxBatchDims];
+  int64_t rs, cs;
+};
+
+struct VecView {                   // per-row / per-column parameter: ptr[boff(b) + i*vs]
+  const void* ptr;
+  int64_t bstride[kMaxBatchDims];
+  int64_t vs;
+};
+
+// Device status word bits (see mm_get_device_status).
+enum : unsigned { kStatusIndexRange = 1u, kStatusTimeout = 2u };
+
+// Element offset of flattened batch index b for an operand with strides bstride.
+__host__ __device__ __forceinline__ int64_t batch_offset(const BatchMap& bm, const int64_t* bstride,
+                                                         int64_t b) {
+  int64_t off = 0;
+  for (int d = bm.nb - 1; d >= 0; --d) {
+    const int64_t n = bm.shape[d];
+    off += (b % n) * bstride[d];
+    b /= n;
+  }
+  return off;
+}
+
+// QLinearMatMul requantisation of one int32 accumulator: each step is one
+// correctly rounded IEEE fp32 operation, in the order
+//   s = a_scale*b_scale; v = float(acc)*s; q = v/y_scale; r = rint(q) (ties to even);
+//   t = r + y_zero_point; saturate with fmin/fmax to [qmin, qmax].
+// (QLinearMatMul - version 10: quantization formula and rounding sentence.)
+__device__ __forceinline__ float requant_f32(int32_t acc, float sa, float sb, float ys, float yzp,
+                                             float qmin, float qmax) {
+  const float s = __fmul_rn(sa, sb);
+  const float v = __fmul_rn(__int2float_rn(acc), s);
+  const float q = __fdiv_rn(v, ys);
+  const float r = rintf(q);
+  const float t = __fadd_rn(r, yzp);
+  return fminf(fmaxf(t, qmin), qmax);
+}
+
+}  // namespace qg

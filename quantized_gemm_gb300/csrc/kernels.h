@@ -1,0 +1,53 @@
+// Launchers implemented by the kernel translation units and called by the
+// C-ABI layer (api.cu).  Every launcher enqueues work on `stream` and returns
+// MM_OK or MM_ERR_CUDA; arguments have been validated by the caller.
+#pragma once
+
+#include "common.cuh"
+
+namespace qg {
+
+// MatMul and Gemm: Y[b] = alpha * A[b] @ B[b] + beta * C (C broadcast view).
+struct GemmArgs {
+  int dtype;                 // mm_dtype shared by A, B, C, Y
+  int64_t M, N, K;
+  BatchMap bm;
+  MatView a;                 // rows M, cols K
+  MatView b;                 // rows K, cols N
+  MatView c;                 // rows M, cols N (strides 0 where broadcast); ptr null = absent
+  MatView y;                 // rows M, cols N, dense
+  float alpha, beta;         // float types
+  double alpha_d, beta_d;    // f64
+  uint64_t alpha_i, beta_i;  // integer types: two's complement of the integral values
+};
+
+// QLinearMatMul.
+struct QLinearArgs {
+  int64_t M, N, K;
+  BatchMap bm;
+  MatView a, b, y;           // a: rows M cols K; b: rows K cols N; y dense
+  VecView sa, za;            // indexed by row m (vs = 0 for per-tensor)
+  VecView sb, zb;            // indexed by column n
+  const void* ys;            // y_scale (one element)
+  const void* yz;            // y_zero_point (one element)
+  int a_signed, b_signed, y_signed;
+  int sa_f16, sb_f16, ys_f16;
+};
+
+// GroupedMatMul.
+struct GroupedArgs {
+  int dtype;                 // T
+  int ind64;                 // Tind is int64
+  int64_t M, K, N, G, S;
+  const void* x;   int64_t x_rs, x_cs;
+  const void* w;   int64_t w_gs, w_ks, w_ns;
+  const void* gi;  int64_t gi_ms, gi_ss;
+  const void* bias; int64_t bias_gs, bias_ns;   // bias null = absent
+  void* out;                 // dense [M, S, N]
+};
+
+mm_status launch_simt_gemm(const GemmArgs& args, cudaStream_t stream);
+mm_status launch_simt_qlinear(const QLinearArgs& args, cudaStream_t stream);
+mm_status launch_simt_grouped(const GroupedArgs& args, unsigned* status, cudaStream_t stream);
+
+}  // namespace qg

@@ -1,0 +1,338 @@
+// CUDA-core kernels: every element type and every stride pattern.
+//
+// These run the types that have no tensor-core path on GB300 (f32 via FFMA --
+// never TF32 --, f64, and the 32/64-bit integer types, which wrap modulo 2^n),
+// and any bf16/f16 or 8-bit call whose layout the tensor-core kernels do not
+// take.  A block computes a 64 x 64 output tile with 256 threads (4 x 4
+// outputs each, strided by 16 so shared-memory reads are conflict-free and
+// global stores are coalesced along the row); K is staged through shared
+// memory 16 at a time with plain strided loads.
+#include "kernels.h"
+
+namespace qg {
+namespace {
+
+constexpr int kTile = 64;
+constexpr int kTk = 16;
+constexpr int kThreads = 256;
+
+template <typename T> struct Arith;
+template <> struct Arith<__nv_bfloat16> {
+  using acc = float;
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ __nv_bfloat16 store(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct Arith<__half> {
+  using acc = float;
+  static __device__ __forceinline__ float load(const __half* p) { return __half2float(*p); }
+  static __device__ __forceinline__ __half store(float v) { return __float2half_rn(v); }
+};
+template <> struct Arith<float> {
+  using acc = float;
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ float store(float v) { return v; }
+};
+template <> struct Arith<double> {
+  using acc = double;
+  static __device__ __forceinline__ double load(const double* p) { return *p; }
+  static __device__ __forceinline__ double store(double v) { return v; }
+};
+// Integers accumulate in the unsigned type of the same width: wrap-around
+// modulo 2^n is then well defined and equals numpy's result.
+template <> struct Arith<int32_t> {
+  using acc = uint32_t;
+  static __device__ __forceinline__ uint32_t load(const int32_t* p) { return (uint32_t)*p; }
+  static __device__ __forceinline__ int32_t store(uint32_t v) { return (int32_t)v; }
+};
+template <> struct Arith<uint32_t> {
+  using acc = uint32_t;
+  static __device__ __forceinline__ uint32_t load(const uint32_t* p) { return *p; }
+  static __device__ __forceinline__ uint32_t store(uint32_t v) { return v; }
+};
+template <> struct Arith<int64_t> {
+  using acc = uint64_t;
+  static __device__ __forceinline__ uint64_t load(const int64_t* p) { return (uint64_t)*p; }
+  static __device__ __forceinline__ int64_t store(uint64_t v) { return (int64_t)v; }
+};
+template <> struct Arith<uint64_t> {
+  using acc = uint64_t;
+  static __device__ __forceinline__ uint64_t load(const uint64_t* p) { return *p; }
+  static __device__ __forceinline__ uint64_t store(uint64_t v) { return v; }
+};
+
+template <typename A> __device__ __forceinline__ A mac(A acc, A x, A y) { return acc + x * y; }
+template <> __device__ __forceinline__ float mac<float>(float acc, float x, float y) { return __fmaf_rn(x, y, acc); }
+template <> __device__ __forceinline__ double mac<double>(double acc, double x, double y) { return __fma_rn(x, y, acc); }
+
+// y = alpha*acc + beta*c in the accumulator type.
+template <typename T> struct Epi {
+  using acc = typename Arith<T>::acc;
+  static __device__ __forceinline__ acc apply(const GemmArgs& p, acc v, const T* c) {
+    acc r = (acc)p.alpha * v;
+    if (c) r = __fmaf_rn(p.beta, Arith<T>::load(c), r);
+    return r;
+  }
+};
+template <> struct Epi<double> {
+  static __device__ __forceinline__ double apply(const GemmArgs& p, double v, const double* c) {
+    double r = p.alpha_d * v;
+    if (c) r = __fma_rn(p.beta_d, *c, r);
+    return r;
+  }
+};
+template <typename T, typename U> struct EpiInt {
+  static __device__ __forceinline__ U apply(const GemmArgs& p, U v, const T* c) {
+    U r = (U)p.alpha_i * v;
+    if (c) r += (U)p.beta_i * Arith<T>::load(c);
+    return r;
+  }
+};
+template <> struct Epi<int32_t> : EpiInt<int32_t, uint32_t> {};
+template <> struct Epi<uint32_t> : EpiInt<uint32_t, uint32_t> {};
+template <> struct Epi<int64_t> : EpiInt<int64_t, uint64_t> {};
+template <> struct Epi<uint64_t> : EpiInt<uint64_t, uint64_t> {};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmArgs p) {
+  using Acc = typename Arith<T>::acc;
+  __shared__ Acc As[kTk][kTile + 1];
+  __shared__ Acc Bs[kTk][kTile + 1];
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  const int64_t n0 = (int64_t)blockIdx.x * kTile;
+  const int64_t mtiles = (p.M + kTile - 1) / kTile;
+  const T* A = static_cast<const T*>(p.a.ptr);
+  const T* B = static_cast<const T*>(p.b.ptr);
+  const T* C = static_cast<const T*>(p.c.ptr);
+  T* Y = static_cast<T*>(const_cast<void*>(p.y.ptr));
+
+  for (int64_t bt = blockIdx.z; bt < p.bm.count; bt += gridDim.z) {
+    const T* Ab = A + batch_offset(p.bm, p.a.bstride, bt);
+    const T* Bb = B + batch_offset(p.bm, p.b.bstride, bt);
+    const T* Cb = C ? C + batch_offset(p.bm, p.c.bstride, bt) : nullptr;
+    T* Yb = Y + batch_offset(p.bm, p.y.bstride, bt);
+    for (int64_t mt = blockIdx.y; mt < mtiles; mt += gridDim.y) {
+      const int64_t m0 = mt * kTile;
+      Acc acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = Acc(0);
+
+      for (int64_t k0 = 0; k0 < p.K; k0 += kTk) {
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int e = tid + e4 * kThreads;
+          const int ar = e / kTk, ak = e % kTk;        // A tile: 64 rows x 16 k
+          const int64_t gm = m0 + ar, gk = k0 + ak;
+          As[ak][ar] = (gm < p.M && gk < p.K) ? Arith<T>::load(Ab + gm * p.a.rs + gk * p.a.cs) : Acc(0);
+          const int bk = e / kTile, bn = e % kTile;    // B tile: 16 k x 64 cols
+          const int64_t hk = k0 + bk, hn = n0 + bn;
+          Bs[bk][bn] = (hk < p.K && hn < p.N) ? Arith<T>::load(Bb + hk * p.b.rs + hn * p.b.cs) : Acc(0);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kTk; ++kk) {
+          Acc av[4], bv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) av[i] = As[kk][ty + 16 * i];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = mac<Acc>(acc[i][j], av[i], bv[j]);
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t gm = m0 + ty + 16 * i;
+        if (gm >= p.M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t gn = n0 + tx + 16 * j;
+          if (gn >= p.N) continue;
+          const T* c = Cb ? Cb + gm * p.c.rs + gn * p.c.cs : nullptr;
+          Yb[gm * p.y.rs + gn * p.y.cs] = Arith<T>::store(Epi<T>::apply(p, acc[i][j], c));
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ QLinear
+
+__device__ __forceinline__ int load_q(const void* base, int64_t off, int is_signed) {
+  const uint8_t u = static_cast<const uint8_t*>(base)[off];
+  return is_signed ? (int)(int8_t)u : (int)u;
+}
+__device__ __forceinline__ float load_scale(const void* base, int64_t off, int is_f16) {
+  return is_f16 ? __half2float(static_cast<const __half*>(base)[off]) : static_cast<const float*>(base)[off];
+}
+
+__global__ void __launch_bounds__(kThreads) simt_qlinear_kernel(const QLinearArgs p) {
+  __shared__ int As[kTk][kTile + 1];
+  __shared__ int Bs[kTk][kTile + 1];
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  const int64_t n0 = (int64_t)blockIdx.x * kTile;
+  const int64_t mtiles = (p.M + kTile - 1) / kTile;
+  const float qmin = p.y_signed ? -128.f : 0.f, qmax = p.y_signed ? 127.f : 255.f;
+  const float ys = load_scale(p.ys, 0, p.ys_f16);
+  const float yz = (float)load_q(p.yz, 0, p.y_signed);
+  uint8_t* Y = static_cast<uint8_t*>(const_cast<void*>(p.y.ptr));
+
+  for (int64_t bt = blockIdx.z; bt < p.bm.count; bt += gridDim.z) {
+    const int64_t aoff = batch_offset(p.bm, p.a.bstride, bt);
+    const int64_t boff = batch_offset(p.bm, p.b.bstride, bt);
+    const int64_t yoff = batch_offset(p.bm, p.y.bstride, bt);
+    const int64_t saoff = batch_offset(p.bm, p.sa.bstride, bt), zaoff = batch_offset(p.bm, p.za.bstride, bt);
+    const int64_t sboff = batch_offset(p.bm, p.sb.bstride, bt), zboff = batch_offset(p.bm, p.zb.bstride, bt);
+    for (int64_t mt = blockIdx.y; mt < mtiles; mt += gridDim.y) {
+      const int64_t m0 = mt * kTile;
+      uint32_t acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0u;
+      for (int64_t k0 = 0; k0 < p.K; k0 += kTk) {
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int e = tid + e4 * kThreads;
+          const int ar = e / kTk, ak = e % kTk;
+          const int64_t gm = m0 + ar, gk = k0 + ak;
+          As[ak][ar] = (gm < p.M && gk < p.K)
+                           ? load_q(p.a.ptr, aoff + gm * p.a.rs + gk * p.a.cs, p.a_signed) -
+                                 load_q(p.za.ptr, zaoff + gm * p.za.vs, p.a_signed)
+                           : 0;
+          const int bk = e / kTile, bn = e % kTile;
+          const int64_t hk = k0 + bk, hn = n0 + bn;
+          Bs[bk][bn] = (hk < p.K && hn < p.N)
+                           ? load_q(p.b.ptr, boff + hk * p.b.rs + hn * p.b.cs, p.b_signed) -
+                                 load_q(p.zb.ptr, zboff + hn * p.zb.vs, p.b_signed)
+                           : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kTk; ++kk) {
+          uint32_t av[4], bv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) av[i] = (uint32_t)As[kk][ty + 16 * i];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bv[j] = (uint32_t)Bs[kk][tx + 16 * j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] += av[i] * bv[j];   // wraps modulo 2^32
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t gm = m0 + ty + 16 * i;
+        if (gm >= p.M) continue;
+        const float sa = load_scale(p.sa.ptr, saoff + gm * p.sa.vs, p.sa_f16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t gn = n0 + tx + 16 * j;
+          if (gn >= p.N) continue;
+          const float sb = load_scale(p.sb.ptr, sboff + gn * p.sb.vs, p.sb_f16);
+          const float t = requant_f32((int32_t)acc[i][j], sa, sb, ys, yz, qmin, qmax);
+          Y[yoff + gm * p.y.rs + gn * p.y.cs] = (uint8_t)(int)t;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ GroupedMatMul
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArgs p, unsigned* status) {
+  using Acc = typename Arith<T>::acc;
+  constexpr int kChunk = 1024;
+  __shared__ Acc xs[kChunk];
+  const T* X = static_cast<const T*>(p.x);
+  const T* W = static_cast<const T*>(p.w);
+  const T* Bias = static_cast<const T*>(p.bias);
+  T* Out = static_cast<T*>(p.out);
+  const int64_t rows = p.M * p.S;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const int64_t m = r / p.S, i = r % p.S;
+    const int64_t goff = m * p.gi_ms + i * p.gi_ss;
+    const int64_t g = p.ind64 ? static_cast<const int64_t*>(p.gi)[goff]
+                              : (int64_t) static_cast<const int32_t*>(p.gi)[goff];
+    const int64_t n = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (g < 0 || g >= p.G) {   // invalid input: never read weights[g]; zero row, flag it
+      if (n < p.N) Out[r * p.N + n] = Arith<T>::store(Acc(0));
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, kStatusIndexRange);
+      continue;
+    }
+    Acc acc = Acc(0);
+    for (int64_t k0 = 0; k0 < p.K; k0 += kChunk) {
+      const int kc = (int)((p.K - k0) < kChunk ? (p.K - k0) : kChunk);
+      __syncthreads();
+      for (int k = threadIdx.x; k < kc; k += kThreads) xs[k] = Arith<T>::load(X + m * p.x_rs + (k0 + k) * p.x_cs);
+      __syncthreads();
+      if (n < p.N) {
+        const T* wcol = W + g * p.w_gs + n * p.w_ns + k0 * p.w_ks;
+        for (int k = 0; k < kc; ++k) acc = mac<Acc>(acc, xs[k], Arith<T>::load(wcol + k * p.w_ks));
+      }
+    }
+    if (n < p.N) {
+      if (Bias) acc = acc + Arith<T>::load(Bias + g * p.bias_gs + n * p.bias_ns);
+      Out[r * p.N + n] = Arith<T>::store(acc);
+    }
+  }
+}
+
+dim3 tile_grid(int64_t M, int64_t N, int64_t batch) {
+  const int64_t nt = (N + kTile - 1) / kTile, mt = (M + kTile - 1) / kTile;
+  return dim3((unsigned)nt, (unsigned)(mt < 65535 ? mt : 65535), (unsigned)(batch < 65535 ? batch : 65535));
+}
+
+}  // namespace
+
+mm_status launch_simt_gemm(const GemmArgs& p, cudaStream_t stream) {
+  if (p.M == 0 || p.N == 0 || p.bm.count == 0) return MM_OK;
+  if ((p.N + kTile - 1) / kTile > 0x7fffffff) return MM_ERR_UNSUPPORTED;
+  const dim3 grid = tile_grid(p.M, p.N, p.bm.count);
+  switch (p.dtype) {
+    case MM_BF16: simt_gemm_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_F16: simt_gemm_kernel<__half><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_F32: simt_gemm_kernel<float><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_F64: simt_gemm_kernel<double><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_I32: simt_gemm_kernel<int32_t><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_I64: simt_gemm_kernel<int64_t><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_U32: simt_gemm_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_U64: simt_gemm_kernel<uint64_t><<<grid, kThreads, 0, stream>>>(p); break;
+    default: return MM_ERR_DTYPE;
+  }
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+mm_status launch_simt_qlinear(const QLinearArgs& p, cudaStream_t stream) {
+  if (p.M == 0 || p.N == 0 || p.bm.count == 0) return MM_OK;
+  if ((p.N + kTile - 1) / kTile > 0x7fffffff) return MM_ERR_UNSUPPORTED;
+  simt_qlinear_kernel<<<tile_grid(p.M, p.N, p.bm.count), kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+mm_status launch_simt_grouped(const GroupedArgs& p, unsigned* status, cudaStream_t stream) {
+  const int64_t rows = p.M * p.S;
+  if (rows == 0 || p.N == 0) return MM_OK;
+  const int64_t nb = (p.N + kThreads - 1) / kThreads;
+  if (nb > 0x7fffffff) return MM_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)nb, (unsigned)(rows < 65535 ? rows : 65535));
+  switch (p.dtype) {
+    case MM_BF16: simt_grouped_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p, status); break;
+    case MM_F16: simt_grouped_kernel<__half><<<grid, kThreads, 0, stream>>>(p, status); break;
+    case MM_F32: simt_grouped_kernel<float><<<grid, kThreads, 0, stream>>>(p, status); break;
+    case MM_F64: simt_grouped_kernel<double><<<grid, kThreads, 0, stream>>>(p, status); break;
+    default: return MM_ERR_DTYPE;
+  }
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+}  // namespace qg
