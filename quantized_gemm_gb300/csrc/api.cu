@@ -64,8 +64,10 @@ mm_status check_tensor(const mm_tensor* t) {
   return MM_OK;
 }
 
-// Dense row-major (strides of size-1 dimensions are not constrained).
+// Dense row-major (strides of size-1 dimensions are not constrained; an empty
+// tensor has no elements to place and is always accepted).
 bool is_dense(const mm_tensor* t) {
+  if (numel(t) == 0) return true;
   int64_t expect = 1;
   for (int d = t->ndim - 1; d >= 0; --d) {
     if (t->shape[d] != 1 && t->strides[d] != expect) return false;
@@ -92,6 +94,7 @@ struct MatmulPlan {
   int64_t M, N, K;
   BatchMap bm;
   MatView a, b;
+  int64_t a_bshape[kMaxBatchDims], b_bshape[kMaxBatchDims];   // each operand's own size per batch dim
   int out_ndim;
   int64_t out_shape[MM_MAX_DIMS];
 };
@@ -114,7 +117,7 @@ mm_status plan_matmul(const mm_tensor* A, const mm_tensor* B, MatmulPlan* p) {
   p->bm.nb = nb;
   p->bm.count = 1;
   for (int d = 0; d < nb; ++d) {
-    const int da = d - (nb - nba), db = d - (nbb >= 0 ? nb - nbb : nb);
+    const int da = d - (nb - nba), db = d - (nb - nbb);
     const int64_t sa = da >= 0 ? as[da] : 1, sb = db >= 0 ? bs[db] : 1;
     int64_t so;
     if (sa == sb || sb == 1) so = sa;
@@ -122,10 +125,14 @@ mm_status plan_matmul(const mm_tensor* A, const mm_tensor* B, MatmulPlan* p) {
     else return MM_ERR_SHAPE;
     p->bm.shape[d] = so;
     p->bm.count *= so;
+    p->a_bshape[d] = sa;
+    p->b_bshape[d] = sb;
     p->a.bstride[d] = (sa == 1) ? 0 : ast[da];
     p->b.bstride[d] = (sb == 1) ? 0 : bst[db];
   }
-  for (int d = nb; d < kMaxBatchDims; ++d) { p->bm.shape[d] = 1; p->a.bstride[d] = 0; p->b.bstride[d] = 0; }
+  for (int d = nb; d < kMaxBatchDims; ++d) {
+    p->bm.shape[d] = 1; p->a.bstride[d] = 0; p->b.bstride[d] = 0; p->a_bshape[d] = 1; p->b_bshape[d] = 1;
+  }
   p->a.ptr = A->data; p->a.rs = ast[an - 2]; p->a.cs = ast[an - 1];
   p->b.ptr = B->data; p->b.rs = bst[bn - 2]; p->b.cs = bst[bn - 1];
   int k = 0;
@@ -362,6 +369,7 @@ mm_status plan_qlinear(const mm_tensor* a, const mm_tensor* a_scale, const mm_te
   QLinearArgs& q = qp->q;
   memset(&q, 0, sizeof(q));
   q.M = qp->mp.M; q.N = qp->mp.N; q.K = qp->mp.K; q.bm = qp->mp.bm; q.a = qp->mp.a; q.b = qp->mp.b;
+  for (int d = 0; d < kMaxBatchDims; ++d) { q.a_bshape[d] = qp->mp.a_bshape[d]; q.b_bshape[d] = qp->mp.b_bshape[d]; }
   if ((s = param_view(a_scale, a, qp->mp, true, &q.sa)) != MM_OK) return s;
   if ((s = param_view(a_zp, a, qp->mp, true, &q.za)) != MM_OK) return s;
   if ((s = param_view(b_scale, b, qp->mp, false, &q.sb)) != MM_OK) return s;
@@ -383,7 +391,9 @@ mm_status mm_qlinear_matmul_workspace_size(const mm_tensor* a, const mm_tensor* 
   if ((s = plan_matmul(a, b, &p)) != MM_OK) return s;
   const int pol = g_policy.load();
   const bool want_tc = pol != MM_PATH_SIMT && (pol == MM_PATH_TENSOR || tensor_pays(p.M, p.N, p.K, p.bm.count));
-  *bytes = want_tc ? tc_qlinear_workspace_bytes(p.M, p.N, p.K, p.bm.count) : 0;
+  int64_t na = 1, nb = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) { na *= p.a_bshape[d]; nb *= p.b_bshape[d]; }
+  *bytes = want_tc ? tc_qlinear_workspace_bytes(p.M, p.N, p.K, na, nb) : 0;
   return MM_OK;
 }
 
@@ -402,7 +412,9 @@ mm_status mm_qlinear_matmul(const mm_tensor* a, const mm_tensor* a_scale, const 
   const int path = choose(tc_qlinear_supported(q), tensor_pays(q.M, q.N, q.K, q.bm.count));
   if (path < 0) return MM_ERR_UNSUPPORTED;
   if (path == MM_PATH_TENSOR) {
-    const size_t need = tc_qlinear_workspace_bytes(q.M, q.N, q.K, q.bm.count);
+    int64_t na = 1, nb = 1;
+    for (int d = 0; d < kMaxBatchDims; ++d) { na *= q.a_bshape[d]; nb *= q.b_bshape[d]; }
+    const size_t need = tc_qlinear_workspace_bytes(q.M, q.N, q.K, na, nb);
     if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255)))
       return MM_ERR_WORKSPACE;
     return finish(launch_tc_qlinear(q, workspace, device_status_ptr(), st), MM_PATH_TENSOR);
@@ -451,7 +463,7 @@ mm_status mm_grouped_matmul_workspace_size(const mm_tensor* input, const mm_tens
   const int pol = g_policy.load();
   const bool want_tc = pol != MM_PATH_SIMT &&
                        (pol == MM_PATH_TENSOR || tensor_pays(g.M * g.S, g.N, g.K, 1));
-  *bytes = want_tc ? tc_grouped_workspace_bytes(g.M, g.S, g.G) : 0;
+  *bytes = (want_tc && tc_grouped_supported(g)) ? tc_grouped_workspace_bytes(g) : 0;
   return MM_OK;
 }
 
@@ -471,7 +483,7 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights, co
   const int path = choose(tc_grouped_supported(g), tensor_pays(g.M * g.S, g.N, g.K, 1));
   if (path < 0) return MM_ERR_UNSUPPORTED;
   if (path == MM_PATH_TENSOR) {
-    const size_t need = tc_grouped_workspace_bytes(g.M, g.S, g.G);
+    const size_t need = tc_grouped_workspace_bytes(g);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
       return MM_ERR_WORKSPACE;
     return finish(launch_tc_grouped(g, workspace, status, st), MM_PATH_TENSOR);

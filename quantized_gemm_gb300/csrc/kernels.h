@@ -26,6 +26,7 @@ struct QLinearArgs {
   int64_t M, N, K;
   BatchMap bm;
   MatView a, b, y;           // a: rows M cols K; b: rows K cols N; y dense
+  int64_t a_bshape[kMaxBatchDims], b_bshape[kMaxBatchDims];  // operands' own batch sizes (1 = broadcast)
   VecView sa, za;            // indexed by row m (vs = 0 for per-tensor)
   VecView sb, zb;            // indexed by column n
   const void* ys;            // y_scale (one element)

@@ -11,11 +11,11 @@ bool tc_gemm_supported(const GemmArgs& g);
 mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t stream);
 
 bool tc_qlinear_supported(const QLinearArgs& q);
-size_t tc_qlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
+size_t tc_qlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_count);
 mm_status launch_tc_qlinear(const QLinearArgs& q, void* workspace, unsigned* status, cudaStream_t stream);
 
 bool tc_grouped_supported(const GroupedArgs& g);
-size_t tc_grouped_workspace_bytes(int64_t M, int64_t S, int64_t G);
+size_t tc_grouped_workspace_bytes(const GroupedArgs& g);
 mm_status launch_tc_grouped(const GroupedArgs& g, void* workspace, unsigned* status, cudaStream_t stream);
 
 }  // namespace qg

@@ -1,15 +1,613 @@
-// tcgen05 tensor-core kernels (sm_103a).
+// tcgen05 tensor-core GEMM for sm_103a (GB300), shared by the MatMul, Gemm,
+// QLinearMatMul and GroupedMatMul fast paths.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: one thread streams A and B tiles (BK = 64) into a
+//               4-stage shared-memory ring, 128-byte swizzled, completing on
+//               per-stage mbarriers (full[s]); it waits on empty[s] before
+//               reusing a stage.
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=256, K=16, fp32 accumulation) into one of two
+//               256-column TMEM accumulators and commits: empty[s] when a
+//               stage has been consumed, acc_full[b] when an accumulation
+//               segment is complete.
+//   warps 2-9   epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
+//               owns TMEM lanes 32*(w%4).. and one 128-column half), release
+//               the buffer (acc_empty[b]) and write the output.
+// Two TMEM accumulators let the epilogue of one segment overlap the MMAs of
+// the next.  Every mbarrier wait is bounded; a wait that runs out sets the
+// timeout bit of the device status word and the CTA winds down cleanly.
+//
+// Modes (template parameter):
+//   kDense    MatMul / Gemm: tiles over (batch, M/128, N/256) in a grouped
+//             raster for L2 reuse; epilogue y = alpha*acc + beta*C[bcast],
+//             rounded once to bf16/f16.
+//   kGrouped  GroupedMatMul: A rows are the routed (group-ordered) copy of the
+//             input rows, B is weights[g]; tiles come from the device-built
+//             per-group tile table; epilogue adds bias[g] and scatters each
+//             row to output[m, i, :].
+//   kQLinear  QLinearMatMul: operands are the zero-point-shifted int8/uint8
+//             values held exactly in f16 (|x| <= 255).  Products are exact in
+//             fp32 and a 256-deep partial sum is below 2^24, so each 256-deep
+//             segment accumulates exactly in fp32; the epilogue converts each
+//             segment to int32 and adds with wrap-around, then requantises.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "tc.h"
+#include "tc_internal.h"
+#include "tc_ptx.cuh"
 
 namespace qg {
 
-bool tc_gemm_supported(const GemmArgs&) { return false; }
-mm_status launch_tc_gemm(const GemmArgs&, unsigned*, cudaStream_t) { return MM_ERR_UNSUPPORTED; }
-bool tc_qlinear_supported(const QLinearArgs&) { return false; }
-size_t tc_qlinear_workspace_bytes(int64_t, int64_t, int64_t, int64_t) { return 0; }
-mm_status launch_tc_qlinear(const QLinearArgs&, void*, unsigned*, cudaStream_t) { return MM_ERR_UNSUPPORTED; }
-bool tc_grouped_supported(const GroupedArgs&) { return false; }
-size_t tc_grouped_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
-mm_status launch_tc_grouped(const GroupedArgs&, void*, unsigned*, cudaStream_t) { return MM_ERR_UNSUPPORTED; }
+using namespace ptx;
+
+namespace {
+
+constexpr int BM = kTileM, BN = kTileN, BK = kTileK;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;             // 16 KB
+constexpr int kBBytes = BN * BK * 2;             // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kGroupM = 16;                      // raster band height (tiles)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+
+struct Tile {
+  int64_t batch;     // dense: broadcast batch index
+  int64_t m0, n0;    // first output row / column of the tile
+  int32_t a_row;     // TMA coordinate of the first A row
+  int32_t a_b, b_b;  // TMA batch coordinates
+  int32_t rows;      // valid rows in the tile
+  int32_t g;         // grouped: group
+};
+
+template <int MODE>
+__device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti) {
+  if (t >= total) return false;
+  if (MODE == kGrouped) {
+    int lo = 0, hi = p.G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.g_tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int64_t local = t - p.g_tile_start[lo];
+    const int cnt = p.g_count[lo];
+    const int64_t mtg = (cnt + BM - 1) / BM;
+    const int64_t ntile = local / mtg, mtile = local - ntile * mtg;
+    ti.batch = 0;
+    ti.g = lo;
+    ti.m0 = mtile * BM;
+    ti.n0 = ntile * BN;
+    ti.a_row = p.g_offset[lo] + (int32_t)(mtile * BM);
+    ti.a_b = 0;
+    ti.b_b = lo;
+    ti.rows = (int32_t)min((int64_t)BM, (int64_t)cnt - mtile * BM);
+    return true;
+  }
+  const int64_t per_batch = p.mt * p.nt;
+  const int64_t b = t / per_batch;
+  const int64_t r = t - b * per_batch;
+  const int64_t band = (int64_t)kGroupM * p.nt;
+  const int64_t gband = r / band;
+  const int64_t w = r - gband * band;
+  const int64_t h = min((int64_t)kGroupM, p.mt - gband * kGroupM);
+  const int64_t mtile = gband * kGroupM + w % h;
+  const int64_t ntile = w / h;
+  ti.batch = b;
+  ti.g = 0;
+  ti.m0 = mtile * BM;
+  ti.n0 = ntile * BN;
+  ti.a_row = (int32_t)ti.m0;
+  ti.a_b = (int32_t)batch_offset(p.bm, p.a_bc, b);
+  ti.b_b = (int32_t)batch_offset(p.bm, p.b_bc, b);
+  ti.rows = (int32_t)min((int64_t)BM, p.M - ti.m0);
+  return true;
+}
+
+template <int MODE>
+__device__ __forceinline__ int64_t total_tiles(const TcParams& p) {
+  return MODE == kGrouped ? (int64_t)p.g_tile_start[p.G] : p.tiles;
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int MODE>
+__device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const TcParams& p, uint32_t sbase,
+                             uint32_t full0, uint32_t empty0, volatile int* abort) {
+  prefetch_tmap(tmA);
+  prefetch_tmap(tmB);
+  const int64_t total = total_tiles<MODE>(p);
+  uint32_t stage = 0, phase = 0;
+  uint32_t pending = 0, pend_parity = 0;   // bit s: a load into stage s was issued (and its parity)
+  Tile ti;
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.status, p.timeout_ns)) goto done;
+      const uint32_t full = full0 + 8 * stage;
+      mbar_arrive_expect_tx(full, kStageBytes);
+      const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
+      const int32_t k0 = kb * BK;
+      if (!p.a_mn) {
+        tma_load_3d(sa, tmA, k0, ti.a_row, ti.a_b, full);
+      } else {
+        tma_load_3d(sa, tmA, ti.a_row, k0, ti.a_b, full);
+        tma_load_3d(sa + 8192, tmA, ti.a_row + 64, k0, ti.a_b, full);
+      }
+      if (!p.b_mn) {
+        tma_load_3d(sb, tmB, k0, (int32_t)ti.n0, ti.b_b, full);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * 8192, tmB, (int32_t)ti.n0 + 64 * j, k0, ti.b_b, full);
+      }
+      pending |= 1u << stage;
+      pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    }
+  }
+done:
+  // Let every issued copy land before the CTA can exit.
+  for (int s = 0; s < kStages; ++s)
+    if (pending & (1u << s)) mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.timeout_ns);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+template <int MODE>
+__device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32_t full0, uint32_t empty0,
+                        uint32_t accf0, uint32_t acce0, uint32_t drain, volatile int* abort) {
+  const int64_t total = total_tiles<MODE>(p);
+  uint32_t stage = 0, phase = 0, seg = 0;
+  Tile ti;
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+    for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_seg) {
+      const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
+      if (!mbar_wait(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns)) goto done;
+      tc_fence_after();
+      const uint32_t d = tmem + buf * BN;
+      const int kb1 = min(kb0 + p.kb_per_seg, p.num_kb);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns)) goto done;
+        tc_fence_after();
+        const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          // K-major: advance 32 bytes inside the 128-byte swizzle row.
+          // MN-major: advance two 8-row (1024-byte) swizzle atoms.
+          const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
+          tc_mma_f16(d, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(empty0 + 8 * stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      tc_commit(accf0 + 8 * buf);
+      ++seg;
+    }
+  }
+done:
+  tc_commit(drain);
+  mbar_wait_teardown(drain, 0, p.timeout_ns);
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int f16) {
+  if (f16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float unpack16(uint16_t x, int f16) {
+  return f16 ? __half2float(__ushort_as_half(x)) : __bfloat162float(__ushort_as_bfloat16(x));
+}
+
+// v[j] += beta * C[n + j] for the 32 columns starting at n.
+__device__ __forceinline__ void add_c32(const TcParams& p, const uint16_t* crow, int64_t n, float (&v)[32]) {
+  if (p.c_vec && n + 32 <= p.N) {
+    const uint4* src = reinterpret_cast<const uint4*>(crow + n);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(src + q);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[q * 8 + 2 * e] = __fmaf_rn(p.beta, unpack16((uint16_t)(w[e] & 0xFFFF), p.out_f16), v[q * 8 + 2 * e]);
+        v[q * 8 + 2 * e + 1] = __fmaf_rn(p.beta, unpack16((uint16_t)(w[e] >> 16), p.out_f16), v[q * 8 + 2 * e + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N) v[j] = __fmaf_rn(p.beta, unpack16(crow[(n + j) * p.c_cs], p.out_f16), v[j]);
+  }
+}
+
+__device__ __forceinline__ void store32_16(const TcParams& p, uint16_t* yrow, int64_t n, const float (&v)[32]) {
+  if (p.y_vec && n + 32 <= p.N) {
+    uint4* dst = reinterpret_cast<uint4*>(yrow + n);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16), pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
+                          pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16), pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N) {
+        const uint32_t w = pack2(v[j], 0.f, p.out_f16);
+        yrow[n + j] = (uint16_t)(w & 0xFFFF);
+      }
+  }
+}
+
+__device__ __forceinline__ float load_scale(const void* base, int64_t off, int is_f16) {
+  return is_f16 ? __half2float(static_cast<const __half*>(base)[off]) : static_cast<const float*>(base)[off];
+}
+__device__ __forceinline__ float load_q8(const void* base, int64_t off, int is_signed) {
+  const uint8_t u = static_cast<const uint8_t*>(base)[off];
+  return is_signed ? (float)(int8_t)u : (float)u;
+}
+
+// ------------------------------------------------------------------ epilogue
+
+template <int MODE>
+__device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3, half = (warp - 2) >> 2;
+  const int rloc = quad * 32 + lane;
+  const uint32_t tlane = (uint32_t)(quad * 32) << 16;
+  const int64_t total = total_tiles<MODE>(p);
+  const int nseg = (p.num_kb + p.kb_per_seg - 1) / p.kb_per_seg;
+  uint32_t seg = 0;
+  Tile ti;
+  float ys = 0.f, yz = 0.f, qmin = 0.f, qmax = 0.f;
+  if (MODE == kQLinear) {
+    ys = load_scale(p.ys, 0, p.ys_f16);
+    yz = load_q8(p.yz, 0, p.y_signed);
+    qmin = p.y_signed ? -128.f : 0.f;
+    qmax = p.y_signed ? 127.f : 255.f;
+  }
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+    const bool row_ok = rloc < ti.rows;
+    const int64_t ncol0 = ti.n0 + half * 128;
+    if (MODE == kQLinear) {
+      int32_t acc[4][32];
+      for (int s = 0; s < nseg; ++s, ++seg) {
+        const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
+        tc_fence_after();
+        const uint32_t taddr = tmem + tlane + buf * BN + half * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int32_t v = __float2int_rn(__uint_as_float(r[j]));   // exact: |v| < 2^24
+            acc[c][j] = s == 0 ? v : (int32_t)((uint32_t)acc[c][j] + (uint32_t)v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+      }
+      if (row_ok) {
+        const int64_t m = ti.m0 + rloc;
+        const float sa = load_scale(p.sa.ptr, batch_offset(p.bm, p.sa.bstride, ti.batch) + m * p.sa.vs, p.sa_f16);
+        const int64_t sboff = batch_offset(p.bm, p.sb.bstride, ti.batch);
+        uint8_t* yrow = static_cast<uint8_t*>(p.y) + batch_offset(p.bm, p.y_bstride, ti.batch) + m * p.y_rs;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t n = ncol0 + c * 32;
+          if (n >= p.N) break;
+          uint32_t packed[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = q * 4 + e;
+              const float sb = (n + j < p.N) ? load_scale(p.sb.ptr, sboff + (n + j) * p.sb.vs, p.sb_f16) : 1.f;
+              const float tq = requant_f32(acc[c][j], sa, sb, ys, yz, qmin, qmax);
+              w |= ((uint32_t)(int32_t)tq & 0xFFu) << (8 * e);
+            }
+            packed[q] = w;
+          }
+          if (p.y_vec && n + 32 <= p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + n);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          } else {
+            for (int j = 0; j < 32 && n + j < p.N; ++j) yrow[n + j] = (uint8_t)(packed[j >> 2] >> (8 * (j & 3)));
+          }
+        }
+      }
+    } else {
+      const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
+      ++seg;
+      if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
+      tc_fence_after();
+      const uint32_t taddr = tmem + tlane + buf * BN + half * 128;
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+      if (!row_ok) continue;
+      uint16_t* yrow;
+      const uint16_t* crow = nullptr;
+      if (MODE == kGrouped) {
+        const int64_t orow = p.g_rowlist[ti.a_row + rloc];
+        yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
+        if (p.c) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
+      } else {
+        const int64_t m = ti.m0 + rloc;
+        yrow = static_cast<uint16_t*>(p.y) + batch_offset(p.bm, p.y_bstride, ti.batch) + m * p.y_rs;
+        if (p.c) crow = static_cast<const uint16_t*>(p.c) + batch_offset(p.bm, p.c_bstride, ti.batch) + m * p.c_rs;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t n = ncol0 + c * 32;
+        if (n >= p.N) break;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[c][j]);
+        if (crow) add_c32(p, crow, n, v);
+        store32_16(p, yrow, n, v);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* ctrl = smem_raw + (sbase - raw) + kStages * kStageBytes;
+  const uint32_t cbase = sbase + kStages * kStageBytes;
+  const uint32_t full0 = cbase, empty0 = cbase + 8 * kStages, accf0 = cbase + 16 * kStages;
+  const uint32_t acce0 = accf0 + 16, drain = acce0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 16 * kStages + 40);
+  volatile int* abort = reinterpret_cast<volatile int*>(ctrl + 16 * kStages + 44);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<MODE>(&tmA, &tmB, p, sbase, full0, empty0, abort);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<MODE>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
+  } else {
+    run_epilogue<MODE>(p, tmem, accf0, acce0, abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int64_t gcd64(int64_t a, int64_t b) {
+  while (b) { const int64_t t = a % b; a = b; b = t; }
+  return a;
+}
+
+int sm_count() {
+  static int counts[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) return 148;
+  if (!counts[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = c > 0 ? c : 148;
+  }
+  return counts[dev];
+}
+
+}  // namespace
+
+// A 16-bit operand of rows `mn_len` (M of A, N of B) and depth `k_len`, with
+// element strides `mn_stride` / `k_stride` and batch strides `bstride` over the
+// broadcast batch `bm`, described as a 3-D tensor map (contiguous dimension,
+// other matrix dimension, batch).  The batch coordinate of batch index b is
+// sum_d i_d * bc[d]; false when the layout does not fit TMA.
+bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int64_t mn_stride, int64_t k_stride,
+                  const BatchMap& bm, const int64_t* bstride, int box_mn, OperandPlan* out) {
+  auto encode = encode_fn();
+  if (!encode || !ptr || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+  if (mn_len < 1 || k_len < 1 || mn_len > 0x7fffffffLL || k_len > 0x7fffffffLL) return false;
+  int64_t unit = 0;
+  for (int d = 0; d < bm.nb; ++d)
+    if (bm.shape[d] > 1 && bstride[d] != 0) unit = gcd64(unit, bstride[d]);
+  int64_t nbat = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) out->bc[d] = 0;
+  if (unit != 0) {
+    if (unit % 8) return false;
+    int64_t maxc = 0;
+    for (int d = 0; d < bm.nb; ++d)
+      if (bm.shape[d] > 1 && bstride[d] != 0) {
+        out->bc[d] = bstride[d] / unit;
+        maxc += (bm.shape[d] - 1) * out->bc[d];
+      }
+    nbat = maxc + 1;
+    if (nbat > 0x7fffffffLL) return false;
+  }
+  const CUtensorMapDataType dt = dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (k_stride == 1 && mn_stride > 0 && mn_stride % 8 == 0) {
+    out->mn_major = 0;
+    dims[0] = (cuuint64_t)k_len; dims[1] = (cuuint64_t)mn_len; dims[2] = (cuuint64_t)nbat;
+    strides[0] = (cuuint64_t)mn_stride * 2;
+    box[0] = 64; box[1] = (cuuint32_t)box_mn; box[2] = 1;
+  } else if (mn_stride == 1 && k_stride > 0 && k_stride % 8 == 0) {
+    out->mn_major = 1;
+    dims[0] = (cuuint64_t)mn_len; dims[1] = (cuuint64_t)k_len; dims[2] = (cuuint64_t)nbat;
+    strides[0] = (cuuint64_t)k_stride * 2;
+    box[0] = 64; box[1] = 64; box[2] = 1;
+  } else {
+    return false;
+  }
+  strides[1] = unit != 0 ? (cuuint64_t)unit * 2 : (cuuint64_t)(((strides[0] * dims[1]) + 15) & ~15ull);
+  if (strides[0] >= (1ull << 40) || strides[1] >= (1ull << 40)) return false;
+  const CUresult r = encode(&out->map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint32_t make_idesc(int f16, int a_mn, int b_mn) {
+  return (1u << 4)                              // D: fp32
+         | ((f16 ? 0u : 1u) << 7)               // A: f16 (0) / bf16 (1)
+         | ((f16 ? 0u : 1u) << 10)              // B: f16 (0) / bf16 (1)
+         | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
+         | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+void init_params(TcParams* p) {
+  memset(p, 0, sizeof(*p));
+  p->timeout_ns = 2000000000ull;
+  p->alpha = 1.f;
+  p->kb_per_seg = 1 << 30;
+}
+
+mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcParams& p, int64_t grid_tiles,
+                    cudaStream_t stream) {
+  p.a_mn = a.mn_major;
+  p.b_mn = b.mn_major;
+  for (int d = 0; d < kMaxBatchDims; ++d) { p.a_bc[d] = a.bc[d]; p.b_bc[d] = b.bc[d]; }
+  p.num_kb = (int)((p.K + BK - 1) / BK);
+  if (p.kb_per_seg > p.num_kb) p.kb_per_seg = p.num_kb > 0 ? p.num_kb : 1;
+  const int sms = sm_count();
+  const int grid = (int)(grid_tiles < sms ? (grid_tiles > 0 ? grid_tiles : 1) : sms);
+  cudaError_t e = cudaSuccess;
+  switch (mode) {
+    case kDense:
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e == cudaSuccess) tc_gemm_kernel<kDense><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      break;
+    case kGrouped:
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e == cudaSuccess) tc_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      break;
+    case kQLinear:
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kQLinear>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e == cudaSuccess) tc_gemm_kernel<kQLinear><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      break;
+    default:
+      return MM_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return MM_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+int sm_count_public() { return sm_count(); }
+
+// ------------------------------------------------------------------ MatMul / Gemm
+
+namespace {
+
+bool plan_dense(const GemmArgs& g, OperandPlan* a, OperandPlan* b) {
+  if (g.dtype != MM_BF16 && g.dtype != MM_F16) return false;
+  if (g.M < 2 || g.N < 2 || g.K < 1) return false;
+  if (g.y.cs != 1) return false;
+  if (!plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM, a)) return false;
+  if (!plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, BN, b)) return false;
+  return true;
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const GemmArgs& g) {
+  OperandPlan a, b;
+  return plan_dense(g, &a, &b);
+}
+
+mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t stream) {
+  OperandPlan a, b;
+  if (!plan_dense(g, &a, &b) || !status) return MM_ERR_UNSUPPORTED;
+  TcParams p;
+  init_params(&p);
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.mt = (g.M + BM - 1) / BM;
+  p.nt = (g.N + BN - 1) / BN;
+  p.bm = g.bm;
+  p.tiles = p.mt * p.nt * g.bm.count;
+  p.out_f16 = g.dtype == MM_F16;
+  p.idesc = make_idesc(p.out_f16, a.mn_major, b.mn_major);
+  p.y = const_cast<void*>(g.y.ptr);
+  for (int d = 0; d < kMaxBatchDims; ++d) { p.y_bstride[d] = g.y.bstride[d]; p.c_bstride[d] = g.c.bstride[d]; }
+  p.y_rs = g.y.rs;
+  p.y_vec = (reinterpret_cast<uintptr_t>(g.y.ptr) % 16 == 0) && (g.y.rs % 8 == 0);
+  for (int d = 0; d < g.bm.nb; ++d) p.y_vec = p.y_vec && (g.y.bstride[d] % 8 == 0);
+  p.alpha = g.alpha;
+  p.beta = g.beta;
+  if (g.c.ptr) {
+    p.c = g.c.ptr;
+    p.c_rs = g.c.rs;
+    p.c_cs = g.c.cs;
+    p.c_vec = g.c.cs == 1 && (reinterpret_cast<uintptr_t>(g.c.ptr) % 16 == 0) && (g.c.rs % 8 == 0);
+    for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % 8 == 0);
+  }
+  p.status = status;
+  return launch_tc(kDense, a, b, p, p.tiles, stream);
+}
 
 }  // namespace qg

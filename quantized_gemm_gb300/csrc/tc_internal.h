@@ -1,0 +1,66 @@
+// Internal interface of the tcgen05 GEMM (tc_gemm.cu) used by the operator
+// front ends (MatMul/Gemm in tc_gemm.cu, QLinearMatMul and GroupedMatMul in
+// tc_prep.cu).
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace qg {
+
+constexpr int kTileM = 128;   // UMMA M (TMEM lanes)
+constexpr int kTileN = 256;   // UMMA N (TMEM columns per accumulator)
+constexpr int kTileK = 64;    // one 128-byte swizzle row of 16-bit elements
+
+enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2 };
+
+struct TcParams {
+  int64_t M, N, K;
+  int64_t mt, nt, tiles;                       // tile counts (dense / qlinear)
+  BatchMap bm;
+  int64_t a_bc[kMaxBatchDims], b_bc[kMaxBatchDims];   // batch index -> TMA batch coordinate
+  int a_mn, b_mn;                              // operand is MN-major in shared memory
+  int num_kb, kb_per_seg;                      // k-blocks; k-blocks per accumulation segment
+  uint32_t idesc;                              // tcgen05 instruction descriptor
+  // output: dense/qlinear y + boff(batch) + m*y_rs + n; grouped y + out_row*y_rs + n
+  void* y;
+  int64_t y_bstride[kMaxBatchDims];
+  int64_t y_rs;
+  int y_vec, out_f16;
+  // float epilogue: v = alpha*acc + beta*C
+  float alpha, beta;
+  const void* c;
+  int64_t c_bstride[kMaxBatchDims];
+  int64_t c_rs, c_cs, c_gs;                    // c_gs: grouped bias row stride per group
+  int c_vec;
+  // QLinear epilogue
+  VecView sa, sb;
+  const void* ys;
+  const void* yz;
+  int sa_f16, sb_f16, ys_f16, y_signed;
+  // GroupedMatMul routing tables (device, in the workspace)
+  const int32_t* g_count;
+  const int32_t* g_offset;
+  const int32_t* g_tile_start;
+  const int32_t* g_rowlist;
+  int G;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+struct OperandPlan {
+  CUtensorMap map;
+  int mn_major;
+  int64_t bc[kMaxBatchDims];
+};
+
+bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int64_t mn_stride, int64_t k_stride,
+                  const BatchMap& bm, const int64_t* bstride, int box_mn, OperandPlan* out);
+uint32_t make_idesc(int f16, int a_mn, int b_mn);
+void init_params(TcParams* p);
+mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcParams& p, int64_t grid_tiles,
+                    cudaStream_t stream);
+int sm_count_public();
+
+}  // namespace qg

@@ -1,0 +1,421 @@
+// Front ends of the tensor-core path for QLinearMatMul and GroupedMatMul: the
+// kernels that prepare operands in the caller's workspace, then the launch of
+// the shared tcgen05 GEMM (tc_gemm.cu).
+//
+// QLinearMatMul (QLinear page, summary): acc = sum_k (a - a_zp)(b - b_zp).
+//   GB300 has no int8 tensor-core instruction (tcgen05 kind::i8 does not exist
+//   on sm_103a), so each operand is rewritten once as the exact f16 value of
+//   (x - zero_point), |x - zp| <= 255, into the workspace; the GEMM runs on the
+//   f16 pipe with segment-exact fp32 accumulation and an int32 epilogue.
+//
+// GroupedMatMul (GroupedMatMul - 29, summary): rows (m, i) are routed to their
+//   group on the device: a histogram of group_indices, an exclusive scan into
+//   per-group row offsets and per-group tile ranges, and a scatter that writes
+//   each row's output index and copies input[m] into a group-ordered row
+//   buffer.  The GEMM then multiplies each group's contiguous rows by
+//   weights[g] in place (the [M*S, K, N] selected weights are never formed) and
+//   scatters results to output[m, i, :].
+#include <cstring>
+
+#include "tc.h"
+#include "tc_internal.h"
+
+namespace qg {
+namespace {
+
+constexpr int64_t kAlign = 256;
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ QLinear: operand shift to f16
+
+struct ShiftArgs {
+  const uint8_t* src;
+  int is_signed;
+  int nb;
+  int64_t own_shape[kMaxBatchDims];   // operand's own batch shape (1 where broadcast)
+  int64_t src_bstride[kMaxBatchDims];
+  int64_t src_rs, src_cs;
+  const uint8_t* zp;
+  int64_t zp_bstride[kMaxBatchDims];
+  int64_t zp_vs;
+  int zp_per_col;                      // zero point indexed by column (b) instead of row (a)
+  int64_t rows, cols, ld, count;       // dst: [count, rows, ld] f16
+  __half* dst;
+};
+
+__device__ __forceinline__ int load_i8(const uint8_t* p, int is_signed) {
+  return is_signed ? (int)(int8_t)*p : (int)*p;
+}
+
+__global__ void __launch_bounds__(256) shift_to_f16_kernel(const ShiftArgs p) {
+  const int64_t cgroups = (p.cols + 7) / 8;
+  const int64_t total = p.count * p.rows * cgroups;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t cg = idx % cgroups;
+    const int64_t rest = idx / cgroups;
+    const int64_t r = rest % p.rows;
+    int64_t mat = rest / p.rows;
+    const int64_t mat_index = mat;
+    int64_t soff = 0, zoff = 0;
+    for (int d = p.nb - 1; d >= 0; --d) {
+      const int64_t i = mat % p.own_shape[d];
+      mat /= p.own_shape[d];
+      soff += i * p.src_bstride[d];
+      zoff += i * p.zp_bstride[d];
+    }
+    const int64_t c0 = cg * 8;
+    const uint8_t* srow = p.src + soff + r * p.src_rs;
+    int zrow = 0;
+    if (!p.zp_per_col) zrow = load_i8(p.zp + zoff + r * p.zp_vs, p.is_signed);
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float v[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t c = c0 + e + u;
+        int x = 0;
+        if (c < p.cols) {
+          const int z = p.zp_per_col ? load_i8(p.zp + zoff + c * p.zp_vs, p.is_signed) : zrow;
+          x = load_i8(srow + c * p.src_cs, p.is_signed) - z;   // |x| <= 255: exact in f16
+        }
+        v[u] = (float)x;
+      }
+      __half2 h = __floats2half2_rn(v[0], v[1]);
+      w[e / 2] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p.dst + (mat_index * p.rows + r) * p.ld + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+mm_status launch_shift(const ShiftArgs& s, cudaStream_t stream) {
+  const int64_t total = s.count * s.rows * ((s.cols + 7) / 8);
+  if (total == 0) return MM_OK;
+  const int64_t blocks = (total + 255) / 256;
+  const int grid = (int)(blocks < 4 * 152 * 8 ? blocks : 4 * 152 * 8);
+  shift_to_f16_kernel<<<grid, 256, 0, stream>>>(s);
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+struct QLayout {
+  int64_t a_count, b_count, kp, np;
+  size_t a_bytes, b_bytes;
+};
+
+QLayout qlayout(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_count) {
+  QLayout l;
+  l.a_count = a_count;
+  l.b_count = b_count;
+  l.kp = round_up(K, 8);
+  l.np = round_up(N, 8);
+  l.a_bytes = (size_t)round_up(a_count * M * l.kp * 2, kAlign);
+  l.b_bytes = (size_t)round_up(b_count * K * l.np * 2, kAlign);
+  return l;
+}
+
+int64_t own_count(const int64_t* shape) {
+  int64_t n = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) n *= shape[d];
+  return n;
+}
+
+// Element strides, over the broadcast batch, of a dense [own batch..., rows, ld]
+// copy of an operand whose own batch shape is `own` (0 where broadcast).
+void dense_batch_strides(const BatchMap& bm, const int64_t* own, int64_t matrix_elems, int64_t* out) {
+  int64_t acc = matrix_elems;
+  for (int d = kMaxBatchDims - 1; d >= 0; --d) {
+    out[d] = (d < bm.nb && own[d] > 1) ? acc : 0;
+    if (d < bm.nb) acc *= own[d];
+  }
+}
+
+bool plan_qlinear(const QLinearArgs& q, const QLayout& l, void* ws, OperandPlan* a, OperandPlan* b) {
+  if (q.M < 2 || q.N < 2 || q.K < 1) return false;
+  if (q.M > 0x7fffffffLL || q.N > 0x7fffffffLL || q.K > 0x7fffffffLL) return false;
+  if (q.y.cs != 1) return false;
+  // Tensor maps are only encoded once the workspace address is known; before
+  // that a 256-aligned stand-in address checks the layout rules.
+  char* base = ws ? static_cast<char*>(ws) : reinterpret_cast<char*>(kAlign);
+  int64_t abs_[kMaxBatchDims], bbs[kMaxBatchDims];
+  dense_batch_strides(q.bm, q.a_bshape, q.M * l.kp, abs_);
+  dense_batch_strides(q.bm, q.b_bshape, q.K * l.np, bbs);
+  if (!plan_operand(base, MM_F16, q.M, q.K, l.kp, 1, q.bm, abs_, kTileM, a)) return false;
+  if (!plan_operand(base + l.a_bytes, MM_F16, q.N, q.K, 1, l.np, q.bm, bbs, kTileN, b)) return false;
+  return true;
+}
+
+}  // namespace
+
+size_t tc_qlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_count) {
+  const QLayout l = qlayout(M, N, K, a_count, b_count);
+  return l.a_bytes + l.b_bytes;
+}
+
+bool tc_qlinear_supported(const QLinearArgs& q) {
+  const QLayout l = qlayout(q.M, q.N, q.K, own_count(q.a_bshape), own_count(q.b_bshape));
+  OperandPlan a, b;
+  return plan_qlinear(q, l, nullptr, &a, &b);
+}
+
+mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cudaStream_t stream) {
+  const QLayout l = qlayout(q.M, q.N, q.K, own_count(q.a_bshape), own_count(q.b_bshape));
+  OperandPlan a, b;
+  if (!ws || !status || !plan_qlinear(q, l, ws, &a, &b)) return MM_ERR_UNSUPPORTED;
+  __half* a16 = static_cast<__half*>(ws);
+  __half* b16 = reinterpret_cast<__half*>(static_cast<char*>(ws) + l.a_bytes);
+
+  // 1. a - a_zero_point (per row) and b - b_zero_point (per column) as exact f16.
+  ShiftArgs sa;
+  memset(&sa, 0, sizeof(sa));
+  sa.src = static_cast<const uint8_t*>(q.a.ptr); sa.is_signed = q.a_signed; sa.nb = q.bm.nb;
+  sa.src_rs = q.a.rs; sa.src_cs = q.a.cs;
+  sa.zp = static_cast<const uint8_t*>(q.za.ptr); sa.zp_vs = q.za.vs; sa.zp_per_col = 0;
+  sa.rows = q.M; sa.cols = q.K; sa.ld = l.kp; sa.count = l.a_count; sa.dst = a16;
+  ShiftArgs sb = sa;
+  sb.src = static_cast<const uint8_t*>(q.b.ptr); sb.is_signed = q.b_signed;
+  sb.src_rs = q.b.rs; sb.src_cs = q.b.cs;
+  sb.zp = static_cast<const uint8_t*>(q.zb.ptr); sb.zp_vs = q.zb.vs; sb.zp_per_col = 1;
+  sb.rows = q.K; sb.cols = q.N; sb.ld = l.np; sb.count = l.b_count; sb.dst = b16;
+  for (int d = 0; d < kMaxBatchDims; ++d) {
+    sa.own_shape[d] = d < q.bm.nb ? q.a_bshape[d] : 1;
+    sa.src_bstride[d] = q.a.bstride[d];
+    sa.zp_bstride[d] = q.za.bstride[d];
+    sb.own_shape[d] = d < q.bm.nb ? q.b_bshape[d] : 1;
+    sb.src_bstride[d] = q.b.bstride[d];
+    sb.zp_bstride[d] = q.zb.bstride[d];
+  }
+  mm_status st = launch_shift(sa, stream);
+  if (st == MM_OK) st = launch_shift(sb, stream);
+  if (st != MM_OK) return st;
+
+  // 2. The f16 GEMM with 256-deep exact segments and the requantising epilogue.
+  TcParams p;
+  init_params(&p);
+  p.M = q.M; p.N = q.N; p.K = q.K;
+  p.mt = (q.M + kTileM - 1) / kTileM;
+  p.nt = (q.N + kTileN - 1) / kTileN;
+  p.bm = q.bm;
+  p.tiles = p.mt * p.nt * q.bm.count;
+  p.kb_per_seg = 256 / kTileK;
+  p.idesc = make_idesc(1, a.mn_major, b.mn_major);
+  p.y = const_cast<void*>(q.y.ptr);
+  for (int d = 0; d < kMaxBatchDims; ++d) p.y_bstride[d] = q.y.bstride[d];
+  p.y_rs = q.y.rs;
+  p.y_vec = (reinterpret_cast<uintptr_t>(q.y.ptr) % 16 == 0) && (q.y.rs % 16 == 0);
+  for (int d = 0; d < q.bm.nb; ++d) p.y_vec = p.y_vec && (q.y.bstride[d] % 16 == 0);
+  p.sa = q.sa; p.sb = q.sb; p.ys = q.ys; p.yz = q.yz;
+  p.sa_f16 = q.sa_f16; p.sb_f16 = q.sb_f16; p.ys_f16 = q.ys_f16; p.y_signed = q.y_signed;
+  p.status = status;
+  return launch_tc(kQLinear, a, b, p, p.tiles, stream);
+}
+
+// ------------------------------------------------------------------ GroupedMatMul: routing
+
+namespace {
+
+struct GLayout {
+  int64_t kp;
+  size_t off_count, off_cursor, off_offset, off_tiles, off_rowlist, off_x, total;
+};
+
+GLayout glayout(int64_t M, int64_t S, int64_t G, int64_t K, int elem) {
+  GLayout l;
+  l.kp = round_up(K, 8);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = (size_t)round_up((int64_t)(o + bytes), kAlign); return at; };
+  l.off_count = take((size_t)G * 4);
+  l.off_cursor = take((size_t)G * 4);
+  l.off_offset = take((size_t)(G + 1) * 4);
+  l.off_tiles = take((size_t)(G + 1) * 4);
+  l.off_rowlist = take((size_t)(M * S) * 4);
+  l.off_x = take((size_t)(M * S) * (size_t)l.kp * (size_t)elem);
+  l.total = o;
+  return l;
+}
+
+__device__ __forceinline__ int64_t load_index(const void* gi, int64_t off, int ind64) {
+  return ind64 ? static_cast<const int64_t*>(gi)[off] : (int64_t) static_cast<const int32_t*>(gi)[off];
+}
+
+__global__ void route_count_kernel(const void* gi, int ind64, int64_t gi_ms, int64_t gi_ss, int64_t M, int64_t S,
+                                   int64_t G, int32_t* count, unsigned* status) {
+  const int64_t total = M * S;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = e / S, i = e - m * S;
+    const int64_t g = load_index(gi, m * gi_ms + i * gi_ss, ind64);
+    if (g >= 0 && g < G) atomicAdd(count + g, 1);
+    else atomicOr(status, kStatusIndexRange);
+  }
+}
+
+// One block: offset[g] = sum_{h<g} count[h]; tile_start[g] = sum_{h<g} ceil(count[h]/128) * nt.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, int64_t G, int64_t nt,
+                                                          int32_t* offset, int32_t* tile_start) {
+  __shared__ int64_t part_rows[1024], part_tiles[1024];
+  const int t = threadIdx.x, T = blockDim.x;
+  const int64_t per = (G + T - 1) / T;
+  const int64_t lo = min(G, (int64_t)t * per), hi = min(G, lo + per);
+  int64_t rows = 0, tiles = 0;
+  for (int64_t g = lo; g < hi; ++g) {
+    rows += count[g];
+    tiles += (count[g] + kTileM - 1) / kTileM * nt;
+  }
+  part_rows[t] = rows;
+  part_tiles[t] = tiles;
+  __syncthreads();
+  if (t == 0) {
+    int64_t r = 0, k = 0;
+    for (int u = 0; u < T; ++u) {
+      const int64_t a = part_rows[u], b = part_tiles[u];
+      part_rows[u] = r;
+      part_tiles[u] = k;
+      r += a;
+      k += b;
+    }
+  }
+  __syncthreads();
+  rows = part_rows[t];
+  tiles = part_tiles[t];
+  for (int64_t g = lo; g < hi; ++g) {
+    offset[g] = (int32_t)rows;
+    tile_start[g] = (int32_t)tiles;
+    rows += count[g];
+    tiles += (count[g] + kTileM - 1) / kTileM * nt;
+  }
+  if (hi == G && lo < hi) {
+    offset[G] = (int32_t)rows;
+    tile_start[G] = (int32_t)tiles;
+  }
+  if (G == 0 && t == 0) {
+    offset[0] = 0;
+    tile_start[0] = 0;
+  }
+}
+
+// One block per routed row (m, i): claim a slot in the group's row range,
+// record the output row, copy input[m] into the group-ordered buffer.  Rows
+// with an invalid index are written as zeros instead (never reading weights).
+template <typename T>
+__global__ void __launch_bounds__(128) route_scatter_kernel(const GroupedArgs g, const int32_t* offset,
+                                                            int32_t* cursor, int32_t* rowlist, T* xperm,
+                                                            int64_t kp) {
+  __shared__ int64_t s_pos;
+  const int64_t total = g.M * g.S;
+  const T* X = static_cast<const T*>(g.x);
+  T* Out = static_cast<T*>(g.out);
+  for (int64_t e = blockIdx.x; e < total; e += gridDim.x) {
+    const int64_t m = e / g.S, i = e - m * g.S;
+    const int64_t grp = load_index(g.gi, m * g.gi_ms + i * g.gi_ss, g.ind64);
+    __syncthreads();
+    if (threadIdx.x == 0) s_pos = (grp >= 0 && grp < g.G) ? (int64_t)offset[grp] + atomicAdd(cursor + grp, 1) : -1;
+    __syncthreads();
+    const int64_t pos = s_pos;
+    if (pos < 0) {
+      for (int64_t n = threadIdx.x; n < g.N; n += blockDim.x) Out[e * g.N + n] = T(0.f);
+      continue;
+    }
+    if (threadIdx.x == 0) rowlist[pos] = (int32_t)e;
+    const T* src = X + m * g.x_rs;
+    T* dst = xperm + pos * kp;
+    const bool vec = g.x_cs == 1 && ((reinterpret_cast<uintptr_t>(src) & 15) == 0) && (g.K % 8 == 0);
+    if (vec) {
+      for (int64_t k = threadIdx.x * 8; k < g.K; k += blockDim.x * 8)
+        *reinterpret_cast<uint4*>(dst + k) = *reinterpret_cast<const uint4*>(src + k);
+    } else {
+      for (int64_t k = threadIdx.x; k < g.K; k += blockDim.x) dst[k] = src[k * g.x_cs];
+    }
+  }
+}
+
+bool plan_grouped_b(const GroupedArgs& g, OperandPlan* b) {
+  BatchMap bm;
+  memset(&bm, 0, sizeof(bm));
+  bm.nb = 1;
+  bm.shape[0] = g.G;
+  bm.count = g.G;
+  for (int d = 1; d < kMaxBatchDims; ++d) bm.shape[d] = 1;
+  int64_t bs[kMaxBatchDims] = {g.w_gs, 0, 0, 0, 0, 0};
+  if (!plan_operand(g.w, g.dtype, g.N, g.K, g.w_ns, g.w_ks, bm, bs, kTileN, b)) return false;
+  // Tile coordinates address weights[g] directly as batch coordinate g.
+  return g.G <= 1 || b->bc[0] == 1;
+}
+
+}  // namespace
+
+size_t tc_grouped_workspace_bytes(const GroupedArgs& g) {
+  return glayout(g.M, g.S, g.G, g.K, g.dtype == MM_F64 ? 8 : g.dtype == MM_F32 ? 4 : 2).total;
+}
+
+bool tc_grouped_supported(const GroupedArgs& g) {
+  if (g.dtype != MM_BF16 && g.dtype != MM_F16) return false;
+  if (g.N < 8 || g.K < 1 || g.G < 1) return false;
+  if (g.M * g.S > 0x7fffffffLL || g.G > 0x7fffffffLL || g.N > 0x7fffffffLL || g.K > 0x7fffffffLL) return false;
+  // an upper bound on the tile count must fit the int32 tile table
+  const int64_t nt = (g.N + kTileN - 1) / kTileN;
+  if ((g.M * g.S / kTileM + g.G + 1) * nt > 0x7fffffffLL) return false;
+  OperandPlan b;
+  return plan_grouped_b(g, &b);
+}
+
+mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cudaStream_t stream) {
+  OperandPlan a, b;
+  if (!ws || !status || !plan_grouped_b(g, &b)) return MM_ERR_UNSUPPORTED;
+  const GLayout l = glayout(g.M, g.S, g.G, g.K, 2);
+  char* base = static_cast<char*>(ws);
+  int32_t* count = reinterpret_cast<int32_t*>(base + l.off_count);
+  int32_t* cursor = reinterpret_cast<int32_t*>(base + l.off_cursor);
+  int32_t* offset = reinterpret_cast<int32_t*>(base + l.off_offset);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(base + l.off_tiles);
+  int32_t* rowlist = reinterpret_cast<int32_t*>(base + l.off_rowlist);
+  void* xperm = base + l.off_x;
+  const int64_t rows = g.M * g.S;
+  const int64_t nt = (g.N + kTileN - 1) / kTileN;
+
+  BatchMap bm1;
+  memset(&bm1, 0, sizeof(bm1));
+  bm1.nb = 0;
+  bm1.count = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) bm1.shape[d] = 1;
+  int64_t zero[kMaxBatchDims] = {0, 0, 0, 0, 0, 0};
+  if (!plan_operand(xperm, g.dtype, rows, g.K, l.kp, 1, bm1, zero, kTileM, &a)) return MM_ERR_UNSUPPORTED;
+
+  if (cudaMemsetAsync(count, 0, l.off_offset - l.off_count, stream) != cudaSuccess) return MM_ERR_CUDA;
+  const int64_t cb = (rows + 255) / 256;
+  route_count_kernel<<<(unsigned)(cb < 4096 ? cb : 4096), 256, 0, stream>>>(g.gi, g.ind64, g.gi_ms, g.gi_ss, g.M,
+                                                                          g.S, g.G, count, status);
+  route_scan_kernel<<<1, 1024, 0, stream>>>(count, g.G, nt, offset, tile_start);
+  const unsigned sgrid = (unsigned)(rows < 65536 ? rows : 65536);
+  if (g.dtype == MM_BF16)
+    route_scatter_kernel<__nv_bfloat16><<<sgrid, 128, 0, stream>>>(g, offset, cursor, rowlist,
+                                                                   static_cast<__nv_bfloat16*>(xperm), l.kp);
+  else
+    route_scatter_kernel<__half><<<sgrid, 128, 0, stream>>>(g, offset, cursor, rowlist, static_cast<__half*>(xperm),
+                                                            l.kp);
+  if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
+
+  TcParams p;
+  init_params(&p);
+  p.M = rows; p.N = g.N; p.K = g.K;
+  p.nt = nt;
+  p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major);
+  p.out_f16 = g.dtype == MM_F16;
+  p.y = g.out;
+  p.y_rs = g.N;
+  p.y_vec = (reinterpret_cast<uintptr_t>(g.out) % 16 == 0) && (g.N % 8 == 0);
+  if (g.bias) {
+    p.c = g.bias;
+    p.beta = 1.f;
+    p.c_gs = g.bias_gs;
+    p.c_cs = g.bias_ns;
+    p.c_vec = g.bias_ns == 1 && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0) && (g.bias_gs % 8 == 0);
+  }
+  p.g_count = count; p.g_offset = offset; p.g_tile_start = tile_start; p.g_rowlist = rowlist;
+  p.G = (int)g.G;
+  p.status = status;
+  // The tile count is known only on the device: one persistent CTA per SM.
+  return launch_tc(kGrouped, a, b, p, sm_count_public(), stream);
+}
+
+}  // namespace qg

@@ -28,7 +28,7 @@ def to_np(t):
 
 def from_np(a, device):
     """Device tensor holding numpy array ``a`` (unsigned 32/64-bit types included)."""
-    a = np.ascontiguousarray(a)
+    a = np.array(a, order="C", copy=True)   # keeps 0-d arrays 0-d
     if a.dtype == np.uint32:
         return torch.from_numpy(a.view(np.int32)).view(torch.uint32).to(device)
     if a.dtype == np.uint64:

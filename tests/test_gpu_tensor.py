@@ -1,0 +1,270 @@
+"""GPU parity of the tcgen05 tensor-core path against the oracle, through the C ABI.
+
+The planner is forced onto the tensor-core kernels (and each test checks that
+they actually ran: mm_last_path() == MM_PATH_TENSOR).  Shapes span several
+128 x 256 tiles with ragged edges in M, N and K; both operand majornesses
+(transA / transB), batch broadcast on either operand, every C broadcast shape,
+exact-integer QLinearMatMul at extreme values, and GroupedMatMul routing edge
+cases (empty groups, one group, invalid indices).
+"""
+
+import contextlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_gemm_gb300 as qg
+from helpers import TOL, max_rel_err, rand_tensor, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+HALF = [torch.bfloat16, torch.float16]
+
+
+@contextlib.contextmanager
+def tensor_path():
+    qg.mm_set_path_policy(qg.MM_PATH_TENSOR)
+    try:
+        yield
+    finally:
+        qg.mm_set_path_policy(qg.MM_PATH_AUTO)
+
+
+def ran_on_tensor_cores():
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
+@pytest.mark.parametrize("dtype", HALF, ids=str)
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 328), (129, 257, 65), (64, 40, 1000), (520, 96, 8)])
+def test_gemm_tensor(dtype, tA, tB, M, N, K):
+    A = rand_tensor((K, M) if tA else (M, K), dtype, 1, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), dtype, 2, DEV)
+    C = rand_tensor((1, N), dtype, 3, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 0.5, 2.0, tA, tB)
+    ran_on_tensor_cores()
+    a, b, c = to_np(A), to_np(B), to_np(C)
+    ref = oracle.gemm(a, b, c, alpha=0.5, beta=2.0, transA=tA, transB=tB)
+    scale = oracle.gemm_abs_scale(a, b, c, alpha=0.5, beta=2.0, transA=tA, transB=tB)
+    assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("c_shape", [None, (), (1,), (300,), (1, 300), (200, 1), (200, 300)])
+def test_gemm_tensor_c_broadcast(c_shape):
+    M, N, K = 200, 300, 136
+    A = rand_tensor((M, K), torch.bfloat16, 4, DEV)
+    B = rand_tensor((K, N), torch.bfloat16, 5, DEV)
+    C = None if c_shape is None else rand_tensor(c_shape, torch.bfloat16, 6, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, -1.5, 0.25)
+    ran_on_tensor_cores()
+    c = None if C is None else to_np(C)
+    ref = oracle.gemm(to_np(A), to_np(B), c, alpha=-1.5, beta=0.25)
+    scale = oracle.gemm_abs_scale(to_np(A), to_np(B), c, alpha=-1.5, beta=0.25)
+    assert max_rel_err(to_np(Y), ref, scale) <= 1e-2
+
+
+@pytest.mark.parametrize("dtype", HALF, ids=str)
+@pytest.mark.parametrize("sa,sb", [((3, 2, 130, 72), (1, 2, 72, 260)), ((1, 2, 130, 72), (3, 2, 72, 260)),
+                                   ((4, 300, 128), (128, 264)), ((2, 64, 200), (2, 200, 512))])
+def test_matmul_tensor_batched_broadcast(dtype, sa, sb):
+    A = rand_tensor(sa, dtype, 7, DEV)
+    B = rand_tensor(sb, dtype, 8, DEV)
+    with tensor_path():
+        Y = qg.mm_matmul(A, B)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= TOL[dtype]
+
+
+def test_matmul_tensor_transposed_views():
+    # A given as the transpose of a contiguous [K, M] tensor (MN-major A).
+    At = rand_tensor((2, 96, 160), torch.bfloat16, 9, DEV)
+    A = At.transpose(1, 2)
+    B = rand_tensor((96, 300), torch.bfloat16, 10, DEV)
+    with tensor_path():
+        Y = qg.mm_matmul(A, B)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= 1e-2
+
+
+def test_tensor_path_rejects_unaligned_layout():
+    A = rand_tensor((100, 33), torch.bfloat16, 11, DEV)   # row stride 33 elements: not 16-byte aligned
+    B = rand_tensor((33, 64), torch.bfloat16, 12, DEV)
+    with tensor_path():
+        with pytest.raises(qg.MMError) as e:
+            qg.mm_matmul(A, B)
+    assert e.value.name == "MM_ERR_UNSUPPORTED"
+    Y = qg.mm_matmul(A, B)     # the planner falls back to the CUDA-core kernel
+    assert qg.mm_last_path() == qg.MM_PATH_SIMT
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= 1e-2
+
+
+# ------------------------------------------------------------------ QLinearMatMul
+
+def _q(d):
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    with tensor_path():
+        y = qg.mm_qlinear_matmul(*[d[k] for k in keys])
+    ran_on_tensor_cores()
+    ref = oracle.qlinear_matmul(*[d[k].cpu().numpy() for k in keys])
+    got = y.cpu().numpy()
+    assert got.dtype == ref.dtype and got.shape == ref.shape
+    mism = np.argwhere(got != ref)
+    assert mism.size == 0, "%d mismatches, first at %s: %s vs %s" % (
+        len(mism), mism[0], got[tuple(mism[0])], ref[tuple(mism[0])])
+
+
+def _qcase(M, K, N, ta, tb, ty, gran, sdt=torch.float32, batch_a=(), batch_b=(), seed=0):
+    g = np.random.default_rng(seed)
+    r = lambda t, shape, lo=None, hi=None: rand_tensor(shape, t, int(g.integers(1 << 30)), DEV, lo, hi)
+    za_rng = (-20, 20) if ta == torch.int8 else (100, 140)
+    zb_rng = (-20, 20) if tb == torch.int8 else (100, 140)
+    if gran == "tensor":
+        sas, sbs = (), ()
+    elif gran == "vector":
+        sas, sbs = (M,), (N,)
+    else:
+        sas, sbs = batch_a + (M, 1), batch_b + (1, N)
+    return {
+        "a": r(ta, batch_a + (M, K)), "b": r(tb, batch_b + (K, N)),
+        "a_scale": torch.from_numpy(np.asarray(g.uniform(0.003, 0.01, sas), np.float32)).to(sdt).to(DEV),
+        "a_zero_point": r(ta, sas, *za_rng),
+        "b_scale": torch.from_numpy(np.asarray(g.uniform(0.003, 0.01, sbs), np.float32)).to(sdt).to(DEV),
+        "b_zero_point": r(tb, sbs, *zb_rng),
+        "y_scale": torch.tensor(0.005 * np.sqrt(K), dtype=sdt, device=DEV),
+        "y_zero_point": torch.tensor(-9 if ty == torch.int8 else 120, dtype=ty, device=DEV),
+    }
+
+
+@pytest.mark.parametrize("ta,tb,ty", [(torch.int8, torch.int8, torch.int8), (torch.uint8, torch.uint8, torch.uint8),
+                                      (torch.int8, torch.uint8, torch.uint8), (torch.uint8, torch.int8, torch.int8)],
+                         ids=str)
+@pytest.mark.parametrize("gran", ["tensor", "vector", "matrix"])
+@pytest.mark.parametrize("M,K,N", [(300, 520, 264), (129, 1000, 257), (200, 64, 40)])
+def test_qlinear_tensor(ta, tb, ty, gran, M, K, N):
+    _q(_qcase(M, K, N, ta, tb, ty, gran))
+
+
+def test_qlinear_tensor_f16_scales_and_batch():
+    _q(_qcase(150, 300, 200, torch.int8, torch.int8, torch.int8, "matrix", torch.float16,
+              batch_a=(2, 3), batch_b=(2, 3)))
+    _q(_qcase(150, 300, 200, torch.uint8, torch.int8, torch.int8, "tensor", torch.float16,
+              batch_a=(3,), batch_b=(1,)))
+
+
+def _swamping_case(K, rows=256, cols=256):
+    """Shifted operands whose running sums reach +-3.9e6 and then cancel.
+
+    uint8 a with a_zero_point 128 and uint8 b with b_zero_point 0.  In every
+    256-deep block of k: 120 terms of (+127)*255 = +32385, 16 terms of
+    s_r * j (s_r in {-1, 0, 1} per row, j = 0..15), 120 terms of
+    (-128)*253 = -32384.  Each block sums to 120 + 120 * s_r in {0, 120, 240},
+    so with unit scales the uint8 output is the exact accumulator: any bit lost
+    while the running sum is near 2^22 changes the result.
+    """
+    a = torch.empty((rows, K), dtype=torch.uint8)
+    b = torch.empty((K, cols), dtype=torch.uint8)
+    s_r = torch.tensor([(-1, 0, 1)[r % 3] for r in range(rows)], dtype=torch.int32)
+    for k0 in range(0, K, 256):
+        a[:, k0:k0 + 120] = 255
+        a[:, k0 + 120:k0 + 136] = (128 + s_r).to(torch.uint8)[:, None]
+        a[:, k0 + 136:k0 + 256] = 0
+        b[k0:k0 + 120, :] = 255
+        b[k0 + 120:k0 + 136, :] = torch.arange(16, dtype=torch.uint8)[:, None]
+        b[k0 + 136:k0 + 256, :] = 253
+    one = torch.tensor(1.0, device=DEV)
+    return {
+        "a": a.to(DEV), "a_scale": one, "a_zero_point": torch.tensor(128, dtype=torch.uint8, device=DEV),
+        "b": b.to(DEV), "b_scale": one, "b_zero_point": torch.tensor(0, dtype=torch.uint8, device=DEV),
+        "y_scale": one * (K // 256), "y_zero_point": torch.tensor(0, dtype=torch.uint8, device=DEV),
+    }
+
+
+@pytest.mark.parametrize("K", [256, 1024])
+def test_qlinear_tensor_accumulation_is_exact(K):
+    d = _swamping_case(K)
+    _q(d)
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    with tensor_path():
+        y = qg.mm_qlinear_matmul(*[d[k] for k in keys]).cpu()
+    want = torch.tensor([(0, 120, 240)[r % 3] for r in range(256)], dtype=torch.uint8)[:, None].expand(256, 256)
+    assert torch.equal(y, want)
+
+
+def test_f16_mma_keeps_integer_sums_exact():
+    # The same premise on the f16 Gemm path: integer products of magnitude
+    # 65025 accumulated to +-8.3e6 and cancelled; the f16 output holds the
+    # small exact remainder (|y| <= 2048 is exact in f16).
+    K, M, N = 256, 128, 256
+    A = torch.zeros((M, K), dtype=torch.float16)
+    B = torch.zeros((K, N), dtype=torch.float16)
+    A[:, :127] = 255.0
+    A[:, 127:129] = torch.arange(M, dtype=torch.float16)[:, None] % 7 - 3
+    A[:, 129:] = -255.0
+    B[:, :] = 255.0
+    B[127:129, :] = (torch.arange(N) % 5).to(torch.float16)[None, :]
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    with tensor_path():
+        Y = qg.mm_matmul(Ad, Bd)
+    ran_on_tensor_cores()
+    ref = oracle.matmul(A.double().numpy(), B.double().numpy())
+    assert np.array_equal(Y.double().cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ GroupedMatMul
+
+def _grouped(x, w, gi, bias):
+    with tensor_path():
+        out = qg.mm_grouped_matmul(x, w, gi, bias)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    xa, wa = to_np(x), to_np(w)
+    ba = None if bias is None else to_np(bias)
+    gia = gi.cpu().numpy()
+    G = w.shape[0]
+    bad = (gia < 0) | (gia >= G)
+    gclip = np.where(bad, 0, gia)
+    ref = oracle.grouped_matmul(xa, wa, gclip, ba)
+    scale = oracle.grouped_abs_scale(xa, wa, gclip, ba)
+    err = np.abs(to_np(out) - ref) / (scale + 1e-30)
+    assert np.max(err[~bad], initial=0) <= TOL[x.dtype]
+    assert np.all(to_np(out)[bad] == 0)
+    return bad.any()
+
+
+@pytest.mark.parametrize("dtype", HALF, ids=str)
+@pytest.mark.parametrize("ind", [torch.int32, torch.int64], ids=str)
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_grouped_tensor(dtype, ind, with_bias):
+    M, K, N, G, S = 300, 200, 520, 6, 2
+    x = rand_tensor((M, K), dtype, 21, DEV)
+    w = rand_tensor((G, K, N), dtype, 22, DEV)
+    p = np.array([0.5, 0.2, 0.0, 0.2, 0.05, 0.05])       # group 2 unused
+    gi = torch.from_numpy(np.random.default_rng(23).choice(G, size=(M, S), p=p)).to(ind).to(DEV)
+    bias = rand_tensor((G, N), dtype, 24, DEV) if with_bias else None
+    _grouped(x, w, gi, bias)
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
+def test_grouped_tensor_single_group_and_k_tail():
+    x = rand_tensor((260, 72), torch.bfloat16, 25, DEV)
+    w = rand_tensor((1, 72, 264), torch.bfloat16, 26, DEV)
+    gi = torch.zeros((260, 1), dtype=torch.int64, device=DEV)
+    _grouped(x, w, gi, rand_tensor((1, 264), torch.bfloat16, 27, DEV))
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
+def test_grouped_tensor_invalid_indices():
+    M, K, N, G = 140, 64, 256, 4
+    x = rand_tensor((M, K), torch.bfloat16, 28, DEV)
+    w = rand_tensor((G, K, N), torch.bfloat16, 29, DEV)
+    gi = torch.from_numpy(np.random.default_rng(30).integers(-2, G + 2, size=(M, 2))).to(torch.int32).to(DEV)
+    assert _grouped(x, w, gi, None)
+    assert qg.mm_get_device_status() == "MM_ERR_INDEX_RANGE"
+    assert qg.mm_get_device_status() == "MM_OK"
