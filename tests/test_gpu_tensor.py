@@ -39,8 +39,10 @@ def ran_on_tensor_cores():
 
 @pytest.mark.parametrize("dtype", HALF, ids=str)
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 328), (129, 257, 65), (64, 40, 1000), (520, 96, 8)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 328), (136, 264, 72), (64, 40, 1000), (520, 96, 8)])
 def test_gemm_tensor(dtype, tA, tB, M, N, K):
+    # Every dimension that is a stored row stride is a multiple of 8 (16 bytes),
+    # as TMA requires; the ragged tiles come from M, N, K modulo 128/256/64.
     A = rand_tensor((K, M) if tA else (M, K), dtype, 1, DEV)
     B = rand_tensor((N, K) if tB else (K, N), dtype, 2, DEV)
     C = rand_tensor((1, N), dtype, 3, DEV)
@@ -53,9 +55,23 @@ def test_gemm_tensor(dtype, tA, tB, M, N, K):
     assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("c_shape", [None, (), (1,), (300,), (1, 300), (200, 1), (200, 300)])
+@pytest.mark.parametrize("M,N,K", [(129, 257, 72), (131, 9, 200)])
+def test_gemm_tensor_odd_m_n(M, N, K):
+    # transA = 0, transB = 1: the stored strides are K and K; M and N are odd,
+    # so the output rows are not 16-byte aligned and take the scalar stores.
+    A = rand_tensor((M, K), torch.bfloat16, 13, DEV)
+    B = rand_tensor((N, K), torch.bfloat16, 14, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, None, 1.0, 1.0, 0, 1)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    ref = oracle.gemm(a, b, transB=1)
+    assert max_rel_err(to_np(Y), ref, oracle.gemm_abs_scale(a, b, transB=1)) <= 1e-2
+
+
+@pytest.mark.parametrize("c_shape", [None, (), (1,), (296,), (1, 296), (200, 1), (200, 296)])
 def test_gemm_tensor_c_broadcast(c_shape):
-    M, N, K = 200, 300, 136
+    M, N, K = 200, 296, 136
     A = rand_tensor((M, K), torch.bfloat16, 4, DEV)
     B = rand_tensor((K, N), torch.bfloat16, 5, DEV)
     C = None if c_shape is None else rand_tensor(c_shape, torch.bfloat16, 6, DEV)
@@ -69,7 +85,7 @@ def test_gemm_tensor_c_broadcast(c_shape):
 
 
 @pytest.mark.parametrize("dtype", HALF, ids=str)
-@pytest.mark.parametrize("sa,sb", [((3, 2, 130, 72), (1, 2, 72, 260)), ((1, 2, 130, 72), (3, 2, 72, 260)),
+@pytest.mark.parametrize("sa,sb", [((3, 2, 130, 72), (1, 2, 72, 264)), ((1, 2, 130, 72), (3, 2, 72, 264)),
                                    ((4, 300, 128), (128, 264)), ((2, 64, 200), (2, 200, 512))])
 def test_matmul_tensor_batched_broadcast(dtype, sa, sb):
     A = rand_tensor(sa, dtype, 7, DEV)
@@ -85,7 +101,7 @@ def test_matmul_tensor_transposed_views():
     # A given as the transpose of a contiguous [K, M] tensor (MN-major A).
     At = rand_tensor((2, 96, 160), torch.bfloat16, 9, DEV)
     A = At.transpose(1, 2)
-    B = rand_tensor((96, 300), torch.bfloat16, 10, DEV)
+    B = rand_tensor((96, 304), torch.bfloat16, 10, DEV)
     with tensor_path():
         Y = qg.mm_matmul(A, B)
     ran_on_tensor_cores()
