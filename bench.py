@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the ONNX matrix-product kernels on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line.  The headline workload is the bf16 Gemm M=N=K=8192,
+transB=1, alpha=0.5, beta=2.0, C[1,8192] (one step = one mm_gemm call = one
+tcgen05 kernel launch); the metric is achieved TFLOP/s (2*M*N*K per step) and
+its fraction of the measured dense bf16 peak.  The other four workloads
+(f32 MatMul, batched broadcast bf16 MatMul, int8 QLinearMatMul, bf16
+GroupedMatMul) are timed the same way and reported under "workloads".
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize(), timed with CUDA events on the stream the library
+launches on; the max over ranks is reported.  The Gemm inputs (A and B,
+256 MiB) are larger than L2 (129 MB); the small f32 workload flushes L2
+(writes 256 MiB) between timed iterations.  nvidia-smi samples the SM clock
+and throttle reasons while the timed loop runs.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent problems, no data-path collective: weak scaling); the
+process group is used only for barriers and the max of the timings.
+"""
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "achieved TFLOPS/TOPS and % of GB300 dense tensor peak, per config"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 10 ** 6
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples, 100 ms apart, for one GPU."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        self.samples = []
+        self.proc = None
+        self.window = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = self.samples
+        if self.window:
+            inside = [s for s in rows if self.window[0] - 0.05 <= s[0] <= self.window[1] + 0.05]
+            rows = inside or rows
+        mhz, maxes, reasons = [], [], set()
+        for _, p in rows:
+            try:
+                mhz.append(float(p[1]))
+                maxes.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def l2_flusher(device):
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+def time_loop(step, steps, warmup, world, stream, flush=None, sampler=None):
+    """Average ms per step (max over ranks).  Back-to-back when flush is None,
+    else each step timed alone after an L2 flush."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+    else:
+        total = 0.0
+        for _ in range(steps):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+        ms = total / steps
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if sampler is not None:
+        sampler.mark(t_wall0, t_wall1)
+    barrier(world)
+    return max_over_ranks(ms, world), t_wall1 - t_wall0
+
+
+KERNEL_SOURCES = ("common.cuh", "tc_internal.h", "tc_ptx.cuh", "tc_gemm.cu")
+
+
+def source_hash():
+    """Hash of the tensor-core GEMM's sources: a stored ncu traffic figure is
+    valid only while this hash is unchanged."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_gemm_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(name):
+    """dram bytes per launch recorded from an ncu capture in profiles/<name>.md, if current."""
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------ workloads
+
+def gemm_case(dev, M=8192, N=8192, K=8192):
+    import quantized_gemm_gb300 as qg
+    d = workloads.gemm_bf16(device=dev, M=M, N=N, K=K)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], d["transA"], d["transB"], out=Y)
+    return d, Y, step
+
+
+def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
+    """The four other workloads: one call of the public API per step."""
+    import quantized_gemm_gb300 as qg
+    out = {}
+    bf16_peak = peaks["bf16_tflops"]
+    hbm = peaks["hbm_gbs"]
+
+    # 1. f32 MatMul [4,128,64] @ [64,96] and [64] @ [4,64,96]: latency-bound.
+    d = workloads.matmul_f32(device=dev)
+    Y1 = torch.empty((4, 128, 96), dtype=torch.float32, device=dev)
+    Y2 = torch.empty((4, 96), dtype=torch.float32, device=dev)
+
+    def s1():
+        qg.mm_matmul(d["A"], d["B"], out=Y1)
+        qg.mm_matmul(d["A1"], d["B1"], out=Y2)
+    ms, _ = time_loop(s1, 50, 5, world, stream, flush=l2_flusher(dev))
+    flops = 2 * 4 * 128 * 64 * 96 + 2 * 4 * 64 * 96
+    nbytes = 4 * (4 * 128 * 64 + 64 * 96 + 4 * 128 * 96 + 64 + 4 * 64 * 96 + 4 * 96)
+    out["matmul_f32"] = {"value": flops / ms / 1e9, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
+                         "bound": "latency", "hbm_gbs": nbytes / ms / 1e6, "kernels_per_call": 2,
+                         "l2": "flushed between iterations"}
+    del d, Y1, Y2
+
+    # 3. bf16 batched MatMul A[8,32,2048,128] @ B[1,32,128,2048]: HBM-bound (2.15 GB output).
+    d = workloads.matmul_bf16_bcast(device=dev)
+    Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
+    ms, _ = time_loop(lambda: qg.mm_matmul(d["A"], d["B"], out=Y), 20, 3, world, stream)
+    flops = 2 * 256 * 2048 * 2048 * 128
+    nbytes = (d["A"].numel() + d["B"].numel() + Y.numel()) * 2
+    gbs = nbytes / ms / 1e6
+    out["matmul_bf16_bcast"] = {"value": flops / ms / 1e9, "unit": "TFLOP/s", "ms_per_call": ms,
+                                "bound": "hbm", "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
+                                "kernels_per_call": 1, "l2": "inputs+output larger than L2"}
+    del d, Y
+    torch.cuda.empty_cache()
+
+    # 4. int8 QLinearMatMul 16384 x 4096 x 4096 (runs on the f16 tensor pipe).
+    d = workloads.qlinear_s8(device=dev)
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    yq = torch.empty((16384, 4096), dtype=torch.int8, device=dev)
+    ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
+    ms, _ = time_loop(lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws), 20, 3, world,
+                      stream)
+    ops = 2 * 16384 * 4096 * 4096
+    tops = ops / ms / 1e9
+    sat = float(((yq == 127) | (yq == -128)).float().mean().item())
+    out["qlinear_s8"] = {"value": tops, "unit": "TOP/s", "ms_per_call": ms, "bound": "tensor",
+                         "pipe": "f16 (no int8 tensor-core instruction on sm_103a)", "peak_tflops": bf16_peak,
+                         "frac": tops / bf16_peak, "kernels_per_call": 3, "saturated_fraction": sat,
+                         "l2": "inputs+workspace larger than L2"}
+    del d, yq, ws
+    torch.cuda.empty_cache()
+
+    # 5. bf16 GroupedMatMul M=16384, S=2, G=64, K=4096, N=14336.
+    d = workloads.grouped_bf16(device=dev)
+    yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(qg.mm_grouped_matmul_workspace_size(d["input"], d["weights"], d["group_indices"]),
+                     dtype=torch.uint8, device=dev)
+    ms, _ = time_loop(lambda: qg.mm_grouped_matmul(d["input"], d["weights"], d["group_indices"], d["bias"],
+                                                   out=yo, workspace=ws), 10, 3, world, stream)
+    flops = 2 * 16384 * 2 * 4096 * 14336
+    tf = flops / ms / 1e9
+    out["grouped_bf16"] = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor",
+                           "peak_tflops": bf16_peak, "frac": tf / bf16_peak, "kernels_per_call": 4,
+                           "l2": "weights (7.5 GB) larger than L2"}
+    del d, yo, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_gemm(d, rows):
+    """The oracle (numpy float64, BLAS threads) on the first `rows` rows of the Gemm workload."""
+    import oracle
+    A = d["A"][:rows].double().cpu().numpy()
+    B = d["B"].double().cpu().numpy()
+    C = d["C"].double().cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.gemm(A, B, C, alpha=d["alpha"], beta=d["beta"], transA=d["transA"], transB=d["transB"])
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * B.shape[0] * B.shape[1]
+    return flops / dt / 1e12, dt
+
+
+def blas_threads():
+    try:
+        return int(os.environ.get("OPENBLAS_NUM_THREADS", "0")) or (os.cpu_count() or 1)
+    except ValueError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded row sample of the Gemm."""
+    if rank != 0:
+        return
+    dev = "cpu"
+    d = workloads.gemm_bf16(device=dev)
+    A = d["A"].double().numpy()
+    B = d["B"].double().numpy()
+    C = d["C"].double().numpy()
+    import oracle
+    total_steps = args.steps + args.warmup
+    rows = int(max(8, min(512, 60.0 / max(1, total_steps) / 2e-3)))
+    for i in range(args.warmup):
+        oracle.gemm(A[:rows], B, C, alpha=d["alpha"], beta=d["beta"], transB=1)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows) % (A.shape[0] - rows + 1)
+        oracle.gemm(A[r0:r0 + rows], B, C, alpha=d["alpha"], beta=d["beta"], transB=1)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    tflops = 2.0 * rows * 8192 * 8192 / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gemm_bf16", "M": 8192, "N": 8192, "K": 8192, "transB": 1,
+                   "alpha": 0.5, "beta": 2.0, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": "%d rows of the 8192^3 Gemm per step (numpy float64)" % rows},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import quantized_gemm_gb300 as qg
+    from quantized_gemm_gb300 import build as qbuild
+    qbuild.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = measured_peaks()
+
+    M = N = K = 8192
+    d, Y, step = gemm_case(dev, M, N, K)
+    sampler = ClockSampler(dev)
+    ms, wall = time_loop(step, args.steps, args.warmup, world, stream, sampler=sampler)
+    clocks = sampler.stop()
+    flops = 2.0 * M * N * K
+    tflops_rank = flops / ms / 1e9
+    value = tflops_rank * world
+    peak_kind = "bf16_tflops_sustained" if wall > 1.0 else "bf16_tflops"
+    peak = peaks.get(peak_kind, peaks["bf16_tflops"])
+    status = qg.mm_get_device_status()
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR, "the Gemm did not run on the tensor-core kernel"
+
+    # e2e: the same call from pinned host buffers, copies inside the timed region.
+    e2e = None
+    if not args.skip_e2e:
+        hA = d["A"].cpu().pin_memory()
+        hB = d["B"].cpu().pin_memory()
+        hC = d["C"].cpu().pin_memory()
+        hY = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        dA, dB, dC = torch.empty_like(d["A"]), torch.empty_like(d["B"]), torch.empty_like(d["C"])
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dC.copy_(hC, non_blocking=True)
+            qg.mm_gemm(dA, dB, dC, d["alpha"], d["beta"], 0, 1, out=Y)
+            hY.copy_(Y, non_blocking=True)
+        e_steps = max(3, min(args.steps, 30))
+        ems, _ = time_loop(e2e_step, e_steps, 2, world, stream)
+        e2e = {"value": flops / ems / 1e9 * world, "unit": "TFLOP/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": (hA.numel() + hB.numel() + hC.numel()) * 2,
+               "d2h_bytes_per_step": hY.numel() * 2}
+        del hA, hB, hC, hY, dA, dB, dC
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        rows = 2048
+        cpu_tf, cpu_s = cpu_baseline_gemm(d, rows)
+        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": "first %d of 8192 rows of the Gemm (numpy float64 BLAS), %.1f s" % (rows, cpu_s)}
+    del d, Y
+    torch.cuda.empty_cache()
+
+    extras = {}
+    if not args.skip_extras:
+        extras = bench_extra_workloads(dev, world, stream, peaks, peak_kind)
+
+    traffic = stored_traffic("tc_gemm_kernel_gemm_bf16_8192")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1)/sqrt(8192) A, B and N(0,1) C, rounded to bf16",
+        "config": {"workload": "gemm_bf16", "M": M, "N": N, "K": K, "transA": 0, "transB": 1, "alpha": 0.5,
+                   "beta": 2.0, "C": [1, N], "parallelism": "independent replicas x%d" % world,
+                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB)"},
+        "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops_rank / peak, "traffic": traffic,
+                     "peak_source": "%s %s (MEASURED_PEAKS.json)" % (peak_src, peak_kind),
+                     "kernel": "tc_gemm_kernel<kDense>", "algorithmic": "2*M*N*K = %.4g FLOP per launch" % flops},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "device_status": status,
+        "workloads": extras,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -17,6 +17,7 @@ import torch
 __all__ = [
     "MMError", "mm_matmul", "mm_gemm", "mm_qlinear_matmul", "mm_grouped_matmul",
     "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_version", "library_path",
+    "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
 ]
 
@@ -124,11 +125,30 @@ def _out_shape(fn, *args):
     return tuple(shape[i] for i in range(nd.value))
 
 
-def _workspace(nbytes, device):
+def _workspace(nbytes, device, given=None):
+    """(tensor, size) of a workspace of at least ``nbytes``: ``given`` when it is large enough."""
     if nbytes == 0:
         return None, 0
+    if given is not None:
+        if given.numel() * given.element_size() < nbytes:
+            raise ValueError("workspace of %d bytes is smaller than the %d required" % (given.numel(), nbytes))
+        return given, given.numel() * given.element_size()
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
     return ws, nbytes
+
+
+def mm_qlinear_matmul_workspace_size(a, b):
+    nbytes = ctypes.c_size_t()
+    _check(_lib().mm_qlinear_matmul_workspace_size(_ref(_desc(a)), _ref(_desc(b)), ctypes.byref(nbytes)),
+           "mm_qlinear_matmul_workspace_size")
+    return nbytes.value
+
+
+def mm_grouped_matmul_workspace_size(input, weights, group_indices):
+    nbytes = ctypes.c_size_t()
+    _check(_lib().mm_grouped_matmul_workspace_size(_ref(_desc(input)), _ref(_desc(weights)), _ref(_desc(group_indices)),
+                                                   ctypes.byref(nbytes)), "mm_grouped_matmul_workspace_size")
+    return nbytes.value
 
 
 def mm_version():
@@ -165,7 +185,7 @@ def mm_gemm(A, B, C=None, alpha=1.0, beta=1.0, transA=0, transB=0, out=None, str
 
 
 def mm_qlinear_matmul(a, a_scale, a_zero_point, b, b_scale, b_zero_point, y_scale, y_zero_point,
-                      out=None, stream=None):
+                      out=None, stream=None, workspace=None):
     """Quantized matmul of int8/uint8 tensors (QLinearMatMul, opset 10); y has y_zero_point's type."""
     lib = _lib()
     da, db = _desc(a), _desc(b)
@@ -174,7 +194,7 @@ def mm_qlinear_matmul(a, a_scale, a_zero_point, b, b_scale, b_zero_point, y_scal
     nbytes = ctypes.c_size_t()
     _check(lib.mm_qlinear_matmul_workspace_size(_ref(da), _ref(db), ctypes.byref(nbytes)),
            "mm_qlinear_matmul_workspace_size")
-    ws, wsb = _workspace(nbytes.value, a.device)
+    ws, wsb = _workspace(nbytes.value, a.device, workspace)
     _check(lib.mm_qlinear_matmul(_ref(da), _ref(_desc(a_scale)), _ref(_desc(a_zero_point)), _ref(db),
                                  _ref(_desc(b_scale)), _ref(_desc(b_zero_point)), _ref(_desc(y_scale)),
                                  _ref(_desc(y_zero_point)), _ref(_desc(y)),
@@ -183,7 +203,7 @@ def mm_qlinear_matmul(a, a_scale, a_zero_point, b, b_scale, b_zero_point, y_scal
     return y
 
 
-def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream=None):
+def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream=None, workspace=None):
     """output[m, i] = input[m] @ weights[group_indices[m, i]] (+ bias[g]) (GroupedMatMul, opset 29)."""
     lib = _lib()
     dx, dw, dg = _desc(input), _desc(weights), _desc(group_indices)
@@ -192,7 +212,7 @@ def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream
     nbytes = ctypes.c_size_t()
     _check(lib.mm_grouped_matmul_workspace_size(_ref(dx), _ref(dw), _ref(dg), ctypes.byref(nbytes)),
            "mm_grouped_matmul_workspace_size")
-    ws, wsb = _workspace(nbytes.value, input.device)
+    ws, wsb = _workspace(nbytes.value, input.device, workspace)
     _check(lib.mm_grouped_matmul(_ref(dx), _ref(dw), _ref(dg), _ref(_desc(bias)), _ref(_desc(y)),
                                  None if ws is None else ws.data_ptr(), wsb, _stream(input, stream)),
            "mm_grouped_matmul")

@@ -1,0 +1,102 @@
+"""Parity at the benchmark sizes, in the launch configuration bench.py times.
+
+Each workload runs once at full size through the public API (auto planner,
+which must choose the tensor-core kernels for the four large workloads); the
+oracle then recomputes sampled output rows from the same inputs (rows of a
+matmul depend only on the matching rows of A, so the oracle is given those
+rows): tile-boundary rows plus seeded random ones.  Float rows are held to the
+per-element bound, QLinearMatMul rows must be bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_gemm_gb300 as qg
+import workloads
+from helpers import max_rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _rows(n, extra, seed):
+    fixed = [0, 1, 127, 128, 255, 256, n // 2, n - 129, n - 128, n - 1]
+    rnd = np.random.default_rng(seed).choice(n, size=extra, replace=False)
+    return sorted(set(int(r) for r in fixed + list(rnd) if 0 <= r < n))
+
+
+def test_matmul_f32_full():
+    d = workloads.matmul_f32(device=DEV)
+    for a, b in ((d["A"], d["B"]), (d["A1"], d["B1"])):
+        y = qg.mm_matmul(a, b)
+        an, bn = to_np(a), to_np(b)
+        assert max_rel_err(to_np(y), oracle.matmul(an, bn), oracle.matmul_abs_scale(an, bn)) <= 1e-5
+
+
+def test_gemm_bf16_8192_sampled_rows():
+    d = workloads.gemm_bf16(device=DEV)
+    Y = qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], d["transA"], d["transB"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    rows = _rows(8192, 22, 1)
+    A = to_np(d["A"][rows])
+    B = to_np(d["B"])
+    C = to_np(d["C"])
+    kw = dict(alpha=d["alpha"], beta=d["beta"], transA=0, transB=1)
+    ref = oracle.gemm(A, B, C, **kw)
+    assert max_rel_err(to_np(Y[rows]), ref, oracle.gemm_abs_scale(A, B, C, **kw)) <= 1e-2
+    assert torch.isfinite(Y.float()).all()
+
+
+def test_matmul_bf16_bcast_sampled():
+    d = workloads.matmul_bf16_bcast(device=DEV)
+    Y = qg.mm_matmul(d["A"], d["B"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    g = np.random.default_rng(2)
+    for b0, b1 in [(0, 0), (7, 31), (3, 17)] + [tuple(g.integers(0, (8, 32))) for _ in range(3)]:
+        rows = _rows(2048, 6, int(b0 * 32 + b1))
+        A = to_np(d["A"][b0, b1][rows])
+        B = to_np(d["B"][0, b1])
+        ref = oracle.matmul(A, B)
+        assert max_rel_err(to_np(Y[b0, b1][rows]), ref, oracle.matmul_abs_scale(A, B)) <= 1e-2
+
+
+def test_qlinear_s8_sampled_rows_bit_exact():
+    d = workloads.qlinear_s8(device=DEV)
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    y = qg.mm_qlinear_matmul(*[d[k] for k in keys])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    rows = _rows(16384, 14, 3)
+    h = {k: d[k].cpu().numpy() for k in keys}
+    ref = oracle.qlinear_matmul(h["a"][rows], h["a_scale"][rows], h["a_zero_point"][rows], h["b"], h["b_scale"],
+                                h["b_zero_point"], h["y_scale"], h["y_zero_point"])
+    got = y[rows].cpu().numpy()
+    assert np.array_equal(got, ref), "%d mismatching outputs" % int((got != ref).sum())
+    sat = float(((y == 127) | (y == -128)).float().mean())
+    assert 0.001 < sat < 0.05      # the workload's y_scale saturates about 1% of outputs
+
+
+def test_grouped_bf16_sampled_tokens_and_columns():
+    d = workloads.grouped_bf16(device=DEV)
+    out = qg.mm_grouped_matmul(d["input"], d["weights"], d["group_indices"], d["bias"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    toks = _rows(16384, 6, 4)
+    cols = np.sort(np.random.default_rng(5).choice(14336, size=512, replace=False))
+    gi = d["group_indices"][toks].cpu().numpy()
+    used = sorted(set(gi.ravel().tolist()))
+    remap = {g: j for j, g in enumerate(used)}
+    gi_local = np.vectorize(remap.get)(gi).astype(np.int64)
+    used_t = torch.tensor(used, device=DEV)
+    cols_t = torch.from_numpy(cols).to(DEV)
+    w = to_np(d["weights"][used_t][:, :, cols_t])
+    bias = to_np(d["bias"][used_t][:, cols_t])
+    x = to_np(d["input"][toks])
+    ref = oracle.grouped_matmul(x, w, gi_local, bias)
+    scale = oracle.grouped_abs_scale(x, w, gi_local, bias)
+    got = to_np(out[toks][:, :, cols_t])
+    assert max_rel_err(got, ref, scale) <= 1e-2
