@@ -166,6 +166,34 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights,
                             const mm_tensor* output, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* ---------------------------------------------------------------- GroupedMatMul without allocation
+ * This entry point has no counterpart in the operator pages; it exists for
+ * callers that cannot allocate device memory at call time: code whose device
+ * memory is fixed when it starts (a serving loop or plugin that must not call
+ * cudaMalloc, which can block and synchronise the device, or that runs inside
+ * a host framework owning every allocation).  mm_grouped_matmul needs a
+ * caller-provided workspace; this variant computes the same result with the
+ * same tensor-core kernels but takes its scratch from a fixed array of
+ * mm_grouped_matmul_noalloc_max_scratch() bytes (16 MiB) that the library
+ * holds in device memory on every GPU where it is loaded, until the process
+ * exits.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   Arguments, layout and result: as mm_grouped_matmul, without the workspace.
+ *   Limits: bf16/f16 operands whose layout the tensor-core kernels take
+ *   (otherwise MM_ERR_UNSUPPORTED; f32/f64 callers can use mm_grouped_matmul,
+ *   whose CUDA-core path needs no workspace), and a problem whose scratch
+ *   (mm_grouped_matmul_workspace_size() under the tensor-core policy: the
+ *   routing tables plus M*S rows of K elements) fits the array; larger
+ *   problems return MM_ERR_WORKSPACE.
+ *   The first call on a device looks up the array's device address (a CUDA
+ *   runtime query, no allocation); make that first call before any stream
+ *   capture.  Every call on a device shares the one array and each call resets
+ *   what it needs, so calls whose GPU work overlaps (different streams, or
+ *   other host threads) race on it and must be ordered by the caller. */
+size_t mm_grouped_matmul_noalloc_max_scratch(void);
+mm_status mm_grouped_matmul_noalloc(const mm_tensor* input, const mm_tensor* weights,
+                                    const mm_tensor* group_indices, const mm_tensor* bias /* NULL = absent */,
+                                    const mm_tensor* output, void* stream);
+
 /* ---------------------------------------------------------------- device status
  * Synchronises `stream`, then returns and clears the device-side status of the
  * current device: MM_OK, MM_ERR_INDEX_RANGE or MM_ERR_TIMEOUT (the first set,

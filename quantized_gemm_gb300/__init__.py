@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "MMError", "mm_matmul", "mm_gemm", "mm_qlinear_matmul", "mm_grouped_matmul",
     "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_version", "library_path",
-    "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size",
+    "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
 ]
 
@@ -76,6 +76,8 @@ def _lib():
             "mm_grouped_matmul_workspace_size": ([T, T, T, ctypes.POINTER(SZ)], I32),
             "mm_grouped_matmul": ([T, T, T, T, T, P, SZ, P], I32),
             "mm_get_device_status": ([P], I32),
+            "mm_grouped_matmul_noalloc_max_scratch": ([], SZ),
+            "mm_grouped_matmul_noalloc": ([T, T, T, T, T, P], I32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -216,6 +218,22 @@ def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream
     _check(lib.mm_grouped_matmul(_ref(dx), _ref(dw), _ref(dg), _ref(_desc(bias)), _ref(_desc(y)),
                                  None if ws is None else ws.data_ptr(), wsb, _stream(input, stream)),
            "mm_grouped_matmul")
+    return y
+
+
+def mm_grouped_matmul_noalloc(input, weights, group_indices, bias=None, out=None, stream=None):
+    """GroupedMatMul for callers that cannot allocate device memory per call.
+
+    Same result as mm_grouped_matmul, computed with scratch taken from a fixed
+    array the library keeps on each device (no workspace argument, no
+    allocation by the library).  ``out`` must be given by such callers; when
+    it is None this binding allocates it with torch for convenience.
+    """
+    y = torch.empty((input.shape[0], group_indices.shape[1], weights.shape[2]), dtype=input.dtype,
+                    device=input.device) if out is None else out
+    _check(_lib().mm_grouped_matmul_noalloc(_ref(_desc(input)), _ref(_desc(weights)), _ref(_desc(group_indices)),
+                                            _ref(_desc(bias)), _ref(_desc(y)), _stream(input, stream)),
+           "mm_grouped_matmul_noalloc")
     return y
 
 

@@ -491,6 +491,60 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights, co
   return finish(launch_simt_grouped(g, status, st), MM_PATH_SIMT);
 }
 
+// ------------------------------------------------------------------ GroupedMatMul without allocation
+//
+// Scratch for mm_grouped_matmul_noalloc: a fixed array in device memory that
+// exists on every device where this library is loaded, from load until the
+// process exits.  Host code may not use the symbol itself as a pointer (on the
+// host it only names a stand-in object); the device address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device (NULL on failure).
+void* noalloc_scratch_ptr() {
+  static std::mutex mu;
+  static void* ptrs[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mm_grouped_matmul_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+mm_status mm_grouped_matmul_noalloc(const mm_tensor* input, const mm_tensor* weights,
+                                    const mm_tensor* group_indices, const mm_tensor* bias,
+                                    const mm_tensor* output, void* stream) {
+  GroupedArgs g;
+  mm_status s = plan_grouped(input, weights, group_indices, bias, &g);
+  if (s != MM_OK) return s;
+  const int64_t oshape[3] = {g.M, g.S, g.N};
+  if ((s = check_output(output, g.dtype, 3, oshape)) != MM_OK) return s;
+  g.out = output->data;
+  if (g.M == 0 || g.S == 0 || g.N == 0) return finish(MM_OK, MM_PATH_NONE);
+  if (!tc_grouped_supported(g)) return MM_ERR_UNSUPPORTED;
+  if (tc_grouped_workspace_bytes(g) > kNoAllocScratchBytes) return MM_ERR_WORKSPACE;
+  unsigned* status = device_status_ptr();
+  void* scratch = noalloc_scratch_ptr();
+  if (!status || !scratch) return MM_ERR_CUDA;
+  return finish(launch_tc_grouped(g, scratch, status, static_cast<cudaStream_t>(stream)), MM_PATH_TENSOR);
+}
+
 // ------------------------------------------------------------------ device status
 
 mm_status mm_get_device_status(void* stream) {
