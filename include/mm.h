@@ -91,6 +91,15 @@ mm_status mm_set_path_policy(int32_t policy);
  * calling host thread (MM_PATH_NONE before any). */
 int32_t mm_last_path(void);
 
+/* Failure detection.  Every wait of the tensor-core kernels' pipeline
+ * (shared-memory stages, TMEM accumulators) gives up after this many
+ * nanoseconds; the kernel then records MM_ERR_TIMEOUT in the device status,
+ * lets its in-flight copies and MMAs land (those final waits keep a fixed 2 s
+ * limit), releases its tensor memory and exits, leaving the CUDA context
+ * usable.  Default 2e9 ns; 0 restores the default.  Applies to calls made
+ * after it returns; meant for tests and diagnosis. */
+mm_status mm_set_wait_limit_ns(uint64_t ns);
+
 /* ---------------------------------------------------------------- MatMul
  * MatMul (onnx-light operator page, ai.onnx MatMul since version 13; summary
  * and Examples): Y = A @ B with numpy.matmul semantics.  A 1-D A is promoted to

@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "MMError", "mm_matmul", "mm_gemm", "mm_qlinear_matmul", "mm_grouped_matmul",
-    "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_version", "library_path",
+    "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_set_wait_limit_ns", "mm_version",
+    "library_path",
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
 ]
@@ -77,6 +78,7 @@ def _lib():
             "mm_grouped_matmul": ([T, T, T, T, T, P, SZ, P], I32),
             "mm_get_device_status": ([P], I32),
             "mm_grouped_matmul_noalloc_max_scratch": ([], SZ),
+            "mm_set_wait_limit_ns": ([ctypes.c_uint64], I32),
             "mm_grouped_matmul_noalloc": ([T, T, T, T, T, P], I32),
         }
         for name, (args, res) in sigs.items():
@@ -163,6 +165,11 @@ def mm_set_path_policy(policy):
 
 def mm_last_path():
     return _lib().mm_last_path()
+
+
+def mm_set_wait_limit_ns(ns):
+    """Limit of each tensor-core pipeline wait, in ns (0 = default 2 s)."""
+    _check(_lib().mm_set_wait_limit_ns(int(ns)), "mm_set_wait_limit_ns")
 
 
 def mm_matmul(A, B, out=None, stream=None):

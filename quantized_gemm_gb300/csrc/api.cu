@@ -200,6 +200,11 @@ mm_status mm_set_path_policy(int32_t policy) {
 
 int32_t mm_last_path(void) { return g_last_path; }
 
+mm_status mm_set_wait_limit_ns(uint64_t ns) {
+  tc_set_wait_limit_ns((unsigned long long)ns);
+  return MM_OK;
+}
+
 // ------------------------------------------------------------------ MatMul
 
 mm_status mm_matmul_output_shape(const mm_tensor* A, const mm_tensor* B, int32_t* out_ndim, int64_t* out_shape) {

@@ -7,6 +7,9 @@
 
 namespace qg {
 
+// Limit of each pipeline wait in the tensor-core kernels (0 = the 2 s default).
+void tc_set_wait_limit_ns(unsigned long long ns);
+
 bool tc_gemm_supported(const GemmArgs& g);
 mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t stream);
 

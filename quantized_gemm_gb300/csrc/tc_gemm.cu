@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -153,7 +154,7 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
 done:
   // Let every issued copy land before the CTA can exit.
   for (int s = 0; s < kStages; ++s)
-    if (pending & (1u << s)) mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.timeout_ns);
+    if (pending & (1u << s)) mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -192,7 +193,7 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
   }
 done:
   tc_commit(drain);
-  mbar_wait_teardown(drain, 0, p.timeout_ns);
+  mbar_wait_teardown(drain, 0, p.teardown_ns);
 }
 
 // ------------------------------------------------------------------ epilogue helpers
@@ -521,9 +522,17 @@ uint32_t make_idesc(int f16, int a_mn, int b_mn) {
          | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
+namespace {
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitNs); }
+
 void init_params(TcParams* p) {
   memset(p, 0, sizeof(*p));
-  p->timeout_ns = 2000000000ull;
+  p->timeout_ns = g_wait_limit_ns.load();
+  p->teardown_ns = kDefaultWaitNs;
   p->alpha = 1.f;
   p->kb_per_seg = 1 << 30;
 }

@@ -46,7 +46,8 @@ struct TcParams {
   const int32_t* g_rowlist;
   int G;
   unsigned* status;
-  unsigned long long timeout_ns;
+  unsigned long long timeout_ns;    // limit of each pipeline wait
+  unsigned long long teardown_ns;   // limit of the waits that let in-flight copies and MMAs land
 };
 
 struct OperandPlan {

@@ -55,16 +55,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  // try_wait suspends the thread for a hardware-defined time before it gives
+  // up, so the clock and the abort flag are checked after every failed try.
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        atomicOr(status, 2u);
-        return false;
-      }
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, 2u);
+      return false;
     }
   }
 }
