@@ -447,6 +447,40 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_profile_workload(args):
+    """Only one workload's public-API call, W + K times (for ncu captures)."""
+    import quantized_gemm_gb300 as qg
+    from quantized_gemm_gb300 import build as qbuild
+    qbuild.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    name = args.profile_workload
+    if name == "gemm_bf16":
+        _, _, step = gemm_case(dev)
+    elif name == "matmul_bf16_bcast":
+        d = workloads.matmul_bf16_bcast(device=dev)
+        Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
+        step = lambda: qg.mm_matmul(d["A"], d["B"], out=Y)
+    elif name == "qlinear_s8":
+        d = workloads.qlinear_s8(device=dev)
+        keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+        yq = torch.empty((16384, 4096), dtype=torch.int8, device=dev)
+        ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
+        step = lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws)
+    elif name.startswith("grouped_bf16"):
+        G = int(name.split("_g")[1]) if "_g" in name else 64     # grouped_bf16_g8: fewer groups, same M,K,N
+        d = workloads.grouped_bf16(device=dev, G=G)
+        yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(qg.mm_grouped_matmul_workspace_size(d["input"], d["weights"], d["group_indices"]),
+                         dtype=torch.uint8, device=dev)
+        step = lambda: qg.mm_grouped_matmul(d["input"], d["weights"], d["group_indices"], d["bias"], out=yo,
+                                            workspace=ws)
+    else:
+        raise SystemExit("unknown workload " + name)
+    stream = torch.cuda.current_stream(dev)
+    ms, _ = time_loop(step, args.steps, args.warmup, 1, stream)
+    print(json.dumps({"profile_workload": name, "ms_per_call": ms, "status": qg.mm_get_device_status()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,10 +490,15 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
+    ap.add_argument("--profile-workload", default=None,
+                    help="run only this workload (gemm_bf16, matmul_bf16_bcast, qlinear_s8, grouped_bf16[_gN])")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_init(args.gpus)
+    if args.profile_workload:
+        run_profile_workload(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

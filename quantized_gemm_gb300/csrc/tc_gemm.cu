@@ -54,10 +54,13 @@ constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kBBytes = BN * BK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kEpiWarp0 = 2;                     // warps 2..9 run the epilogue
+constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
 constexpr int kGroupM = 16;                      // raster band height (tiles)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
+constexpr int kQColWords = 3 * 128;              // QLinear per-warp column staging
+constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + kEpiWarps * kQColWords * 4 + 1024;
 
 struct Tile {
   int64_t batch;     // dense: broadcast batch index
@@ -257,12 +260,30 @@ __device__ __forceinline__ float load_q8(const void* base, int64_t off, int is_s
   return is_signed ? (float)(int8_t)u : (float)u;
 }
 
+// The requantisation of requant_f32 (common.cuh), returning the output byte,
+// with two exact shortcuts.  rint: for |q| < 2^22, (q + 1.5*2^23) - 1.5*2^23
+// rounds q to the nearest integer, ties to even, exactly as rintf; any larger
+// |q| (or an infinity or NaN) saturates to the same end of [qmin, qmax] either
+// way.  Byte: t is an integer in [-128, 255], so the low bits of t + 1.5*2^23
+// are t in two's complement.
+__device__ __forceinline__ uint32_t requant_byte(int32_t acc, float sa, float sb, float ys, float yzp, float qmin,
+                                                 float qmax) {
+  constexpr float kMagic = 12582912.0f;
+  const float s = __fmul_rn(sa, sb);
+  const float v = __fmul_rn(__int2float_rn(acc), s);
+  const float q = __fdiv_rn(v, ys);
+  const float r = __fsub_rn(__fadd_rn(q, kMagic), kMagic);
+  const float t = fminf(fmaxf(__fadd_rn(r, yzp), qmin), qmax);
+  return (uint32_t)(__float_as_int(__fadd_rn(t, kMagic)) - 0x4B400000) & 0xFFu;
+}
+
 // ------------------------------------------------------------------ epilogue
 
 template <int MODE>
-__device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort) {
+__device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort,
+                             int32_t* qcol) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quad = warp & 3, half = (warp - 2) >> 2;
+  const int quad = warp & 3, half = (warp - kEpiWarp0) >> 2;
   const int rloc = quad * 32 + lane;
   const uint32_t tlane = (uint32_t)(quad * 32) << 16;
   const int64_t total = total_tiles<MODE>(p);
@@ -280,6 +301,28 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
     const bool row_ok = rloc < ti.rows;
     const int64_t ncol0 = ti.n0 + half * 128;
     if (MODE == kQLinear) {
+      // Column data of this warp's 128 columns (zero point, column sum, scale),
+      // staged once per tile in a warp-private shared-memory slice.
+      {
+        const int64_t zboff = batch_offset(p.bm, p.zb.bstride, ti.batch);
+        const int64_t sboff = batch_offset(p.bm, p.sb.bstride, ti.batch);
+        const int32_t* cs = p.q_cs + (int64_t)ti.b_b * p.N;
+        const int bshift = p.b_signed ? 0 : 128;
+        for (int j = lane; j < 128; j += 32) {
+          const int64_t n = ncol0 + j;
+          int32_t zbv = 0, csv = 0;
+          float sbv = 0.f;
+          if (n < p.N) {
+            zbv = (int32_t)load_q8(p.zb.ptr, zboff + n * p.zb.vs, p.b_signed) - bshift;
+            csv = cs[n];
+            sbv = load_scale(p.sb.ptr, sboff + n * p.sb.vs, p.sb_f16);
+          }
+          qcol[j] = zbv;
+          qcol[128 + j] = csv;
+          qcol[256 + j] = __float_as_int(sbv);
+        }
+        __syncwarp();
+      }
       int32_t acc[4][32];
       for (int s = 0; s < nseg; ++s, ++seg) {
         const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
@@ -293,7 +336,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int32_t v = __float2int_rn(__uint_as_float(r[j]));   // exact: |v| < 2^24
+            const int32_t v = __float2int_rn(__uint_as_float(r[j]));   // exact: |v| <= 2^24
             acc[c][j] = s == 0 ? v : (int32_t)((uint32_t)acc[c][j] + (uint32_t)v);
           }
         }
@@ -304,7 +347,11 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       if (row_ok) {
         const int64_t m = ti.m0 + rloc;
         const float sa = load_scale(p.sa.ptr, batch_offset(p.bm, p.sa.bstride, ti.batch) + m * p.sa.vs, p.sa_f16);
-        const int64_t sboff = batch_offset(p.bm, p.sb.bstride, ti.batch);
+        const uint32_t za = (uint32_t)((int32_t)load_q8(p.za.ptr, batch_offset(p.bm, p.za.bstride, ti.batch) + m * p.za.vs,
+                                                        p.a_signed) - (p.a_signed ? 0 : 128));
+        const uint32_t rs = (uint32_t)p.q_rs[(int64_t)ti.a_b * p.M + m];
+        // acc - zb'*rs - za'*cs + K*za'*zb' = acc - zb'*(rs - K*za') - za'*cs   (mod 2^32)
+        const uint32_t rowterm = rs - (uint32_t)p.K * za;
         uint8_t* yrow = static_cast<uint8_t*>(p.y) + batch_offset(p.bm, p.y_bstride, ti.batch) + m * p.y_rs;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -313,13 +360,17 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
           uint32_t packed[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
+            const int4 zb4 = *reinterpret_cast<const int4*>(qcol + c * 32 + 4 * q);
+            const int4 cs4 = *reinterpret_cast<const int4*>(qcol + 128 + c * 32 + 4 * q);
+            const int4 sb4 = *reinterpret_cast<const int4*>(qcol + 256 + c * 32 + 4 * q);
+            const int32_t zbv[4] = {zb4.x, zb4.y, zb4.z, zb4.w};
+            const int32_t csv[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
+            const int32_t sbv[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
             uint32_t w = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int j = q * 4 + e;
-              const float sb = (n + j < p.N) ? load_scale(p.sb.ptr, sboff + (n + j) * p.sb.vs, p.sb_f16) : 1.f;
-              const float tq = requant_f32(acc[c][j], sa, sb, ys, yz, qmin, qmax);
-              w |= ((uint32_t)(int32_t)tq & 0xFFu) << (8 * e);
+              const uint32_t total = (uint32_t)acc[c][4 * q + e] - (uint32_t)zbv[e] * rowterm - za * (uint32_t)csv[e];
+              w |= requant_byte((int32_t)total, sa, __int_as_float(sbv[e]), ys, yz, qmin, qmax) << (8 * e);
             }
             packed[q] = w;
           }
@@ -328,10 +379,13 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           } else {
-            for (int j = 0; j < 32 && n + j < p.N; ++j) yrow[n + j] = (uint8_t)(packed[j >> 2] >> (8 * (j & 3)));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < p.N) yrow[n + j] = (uint8_t)(packed[j >> 2] >> (8 * (j & 3)));
           }
         }
       }
+      __syncwarp();   // every lane is done with qcol before the next tile restages it
     } else {
       const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
       ++seg;
@@ -414,8 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) run_producer<MODE>(&tmA, &tmB, p, sbase, full0, empty0, abort);
   } else if (warp == 1) {
     if (lane == 0) run_mma<MODE>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
-  } else {
-    run_epilogue<MODE>(p, tmem, accf0, acce0, abort);
+  } else if (warp >= kEpiWarp0) {
+    // QLinear column staging: 3 x 128 words per epilogue warp after the control block.
+    int32_t* qcol = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes) + (warp - kEpiWarp0) * kQColWords;
+    run_epilogue<MODE>(p, tmem, accf0, acce0, abort, qcol);
   }
   tc_fence_before();
   __syncthreads();

@@ -34,11 +34,14 @@ struct TcParams {
   int64_t c_bstride[kMaxBatchDims];
   int64_t c_rs, c_cs, c_gs;                    // c_gs: grouped bias row stride per group
   int c_vec;
-  // QLinear epilogue
-  VecView sa, sb;
+  // QLinear epilogue: zero-point correction from the operand sums, then requantisation
+  VecView sa, sb, za, zb;
   const void* ys;
   const void* yz;
   int sa_f16, sb_f16, ys_f16, y_signed;
+  int a_signed, b_signed;                      // uint8 operands were shifted by -128
+  const int32_t* q_rs;                         // [a matrices, M] row sums of a'
+  const int32_t* q_cs;                         // [b matrices, N] column sums of b'
   // GroupedMatMul routing tables (device, in the workspace)
   const int32_t* g_count;
   const int32_t* g_offset;

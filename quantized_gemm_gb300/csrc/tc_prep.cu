@@ -2,11 +2,12 @@
 // kernels that prepare operands in the caller's workspace, then the launch of
 // the shared tcgen05 GEMM (tc_gemm.cu).
 //
-// QLinearMatMul (QLinear page, summary): acc = sum_k (a - a_zp)(b - b_zp).
+// QLinearMatMul (QLinearMatMul - version 10, summary): acc = sum_k (a - a_zp)(b - b_zp).
 //   GB300 has no int8 tensor-core instruction (tcgen05 kind::i8 does not exist
-//   on sm_103a), so each operand is rewritten once as the exact f16 value of
-//   (x - zero_point), |x - zp| <= 255, into the workspace; the GEMM runs on the
-//   f16 pipe with segment-exact fp32 accumulation and an int32 epilogue.
+//   on sm_103a), so each operand is rewritten once, exactly, in f16 (shifted
+//   into [-128, 127]) together with its row or column sums; the GEMM runs on
+//   the f16 pipe with segment-exact fp32 accumulation and an int32 epilogue
+//   that applies the zero points.
 //
 // GroupedMatMul (GroupedMatMul - 29, summary): rows (m, i) are routed to their
 //   group on the device: a histogram of group_indices, an exclusive scan into
@@ -27,81 +28,156 @@ constexpr int64_t kAlign = 256;
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// ------------------------------------------------------------------ QLinear: operand shift to f16
+// ------------------------------------------------------------------ QLinear: operands to f16 + sums
+//
+// Each operand is rewritten once as x' = x - c (c = 128 for uint8, 0 for
+// int8), so x' lies in [-128, 127] for both types and is exact in f16.  The
+// zero points are not applied here: with za' = za - c_a and zb' = zb - c_b,
+//   sum_k (a - za)(b - zb) = sum_k a'b' - zb' * rs - za' * cs + K * za' * zb'
+// where rs[m] = sum_k a'[m, k] and cs[n] = sum_k b'[k, n]; the GEMM epilogue
+// applies this (int32, wrapping).  Products |a'b'| <= 2^14 let 1024-deep
+// segments accumulate exactly in fp32 (|sum| <= 2^24).
 
 struct ShiftArgs {
   const uint8_t* src;
-  int is_signed;
+  int is_signed;                       // int8 (shift 0) or uint8 (shift 128)
   int nb;
-  int64_t own_shape[kMaxBatchDims];   // operand's own batch shape (1 where broadcast)
+  int64_t own_shape[kMaxBatchDims];    // operand's own batch shape (1 where broadcast)
   int64_t src_bstride[kMaxBatchDims];
   int64_t src_rs, src_cs;
-  const uint8_t* zp;
-  int64_t zp_bstride[kMaxBatchDims];
-  int64_t zp_vs;
-  int zp_per_col;                      // zero point indexed by column (b) instead of row (a)
   int64_t rows, cols, ld, count;       // dst: [count, rows, ld] f16
   __half* dst;
+  int32_t* sums;                       // a: row sums [count, rows]; b: column sums [count, cols]
 };
 
-__device__ __forceinline__ int load_i8(const uint8_t* p, int is_signed) {
-  return is_signed ? (int)(int8_t)*p : (int)*p;
+__device__ __forceinline__ int64_t own_offset(const ShiftArgs& p, int64_t mat) {
+  int64_t off = 0;
+  for (int d = p.nb - 1; d >= 0; --d) {
+    const int64_t i = mat % p.own_shape[d];
+    mat /= p.own_shape[d];
+    off += i * p.src_bstride[d];
+  }
+  return off;
 }
 
-__global__ void __launch_bounds__(256) shift_to_f16_kernel(const ShiftArgs p) {
-  const int64_t cgroups = (p.cols + 7) / 8;
-  const int64_t total = p.count * p.rows * cgroups;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t cg = idx % cgroups;
-    const int64_t rest = idx / cgroups;
-    const int64_t r = rest % p.rows;
-    int64_t mat = rest / p.rows;
-    const int64_t mat_index = mat;
-    int64_t soff = 0, zoff = 0;
-    for (int d = p.nb - 1; d >= 0; --d) {
-      const int64_t i = mat % p.own_shape[d];
-      mat /= p.own_shape[d];
-      soff += i * p.src_bstride[d];
-      zoff += i * p.zp_bstride[d];
-    }
-    const int64_t c0 = cg * 8;
-    const uint8_t* srow = p.src + soff + r * p.src_rs;
-    int zrow = 0;
-    if (!p.zp_per_col) zrow = load_i8(p.zp + zoff + r * p.zp_vs, p.is_signed);
-    uint32_t w[4];
+// 16 shifted values of a row starting at column c0 (zeros beyond `cols`).
+__device__ __forceinline__ void load16_shifted(const ShiftArgs& p, const uint8_t* srow, int64_t c0, int (&x)[16]) {
+  const int shift = p.is_signed ? 0 : 128;
+  if (p.src_cs == 1 && c0 + 16 <= p.cols && ((reinterpret_cast<uintptr_t>(srow + c0) & 15) == 0)) {
+    const uint4 u = *reinterpret_cast<const uint4*>(srow + c0);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      float v[2];
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t c = c0 + e + u;
-        int x = 0;
-        if (c < p.cols) {
-          const int z = p.zp_per_col ? load_i8(p.zp + zoff + c * p.zp_vs, p.is_signed) : zrow;
-          x = load_i8(srow + c * p.src_cs, p.is_signed) - z;   // |x| <= 255: exact in f16
-        }
-        v[u] = (float)x;
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t b = (w[q] >> (8 * e)) & 0xFFu;
+        x[4 * q + e] = p.is_signed ? (int)(int8_t)b : (int)b - shift;
       }
-      __half2 h = __floats2half2_rn(v[0], v[1]);
-      w[e / 2] = *reinterpret_cast<uint32_t*>(&h);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      int v = 0;
+      if (c0 + e < p.cols) {
+        const uint8_t b = srow[(c0 + e) * p.src_cs];
+        v = p.is_signed ? (int)(int8_t)b : (int)b - shift;
+      }
+      x[e] = v;
     }
-    *reinterpret_cast<uint4*>(p.dst + (mat_index * p.rows + r) * p.ld + c0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-mm_status launch_shift(const ShiftArgs& s, cudaStream_t stream) {
-  const int64_t total = s.count * s.rows * ((s.cols + 7) / 8);
-  if (total == 0) return MM_OK;
-  const int64_t blocks = (total + 255) / 256;
-  const int grid = (int)(blocks < 4 * 152 * 8 ? blocks : 4 * 152 * 8);
-  shift_to_f16_kernel<<<grid, 256, 0, stream>>>(s);
-  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+// Stores 16 f16 values at dst (16-byte aligned); the elements at or beyond
+// `valid` are stored only if they fall inside the padded row (ld).
+__device__ __forceinline__ void store16_f16(__half* dst, const int (&x)[16], int64_t c0, int64_t ld) {
+  uint32_t w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    __half2 h = __floats2half2_rn((float)x[2 * e], (float)x[2 * e + 1]);   // exact: |x| <= 128
+    w[e] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  if (c0 + 8 < ld) d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// a: one warp per (matrix, row): converts the row and writes its exact sum.
+__global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t total = p.count * p.rows;
+  for (int64_t wr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wr < total; wr += warps) {
+    const int64_t mat = wr / p.rows, r = wr - mat * p.rows;
+    const uint8_t* srow = p.src + own_offset(p, mat) + r * p.src_rs;
+    __half* drow = p.dst + wr * p.ld;
+    uint32_t sum = 0;   // modulo 2^32, like every term of the int32 accumulator
+    for (int64_t c0 = (int64_t)lane * 16; c0 < p.cols; c0 += 512) {
+      int x[16];
+      load16_shifted(p, srow, c0, x);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sum += (uint32_t)x[e];
+      store16_f16(drow + c0, x, c0, p.ld);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) p.sums[wr] = (int32_t)sum;
+  }
+}
+
+// b: a block converts a strip of 256 columns (16 column groups of 16) over a
+// band of kColRows rows; its 16 row lanes stride through the band, their
+// partial column sums are combined in shared memory, and one atomic add per
+// column and block accumulates the band into the column sums (which start at
+// zero).  Consecutive threads read consecutive 16-byte pieces of a row.
+constexpr int kColRows = 512;
+constexpr int kColGroups = 16;                   // 16-column groups per block
+constexpr int kRowLanes = 16;
+
+__global__ void __launch_bounds__(kColGroups * kRowLanes) shift_cols_kernel(const ShiftArgs p) {
+  __shared__ uint32_t part_s[kRowLanes][kColGroups * 16 + 1];
+  const int cgl = threadIdx.x % kColGroups, lane_r = threadIdx.x / kColGroups;
+  const int64_t cgroups = (p.cols + 15) / 16;
+  const int64_t cblocks = (cgroups + kColGroups - 1) / kColGroups;
+  const int64_t rblocks = (p.rows + kColRows - 1) / kColRows;
+  const int64_t total = p.count * rblocks * cblocks;
+  for (int64_t bidx = blockIdx.x; bidx < total; bidx += gridDim.x) {
+    const int64_t cb = bidx % cblocks;
+    const int64_t rest = bidx / cblocks;
+    const int64_t rb = rest % rblocks, mat = rest / rblocks;
+    const int64_t cg = cb * kColGroups + cgl;
+    const int64_t c0 = cg * 16;
+    uint32_t part[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) part[e] = 0;
+    if (cg < cgroups) {
+      const uint8_t* base = p.src + own_offset(p, mat);
+      const int64_t r1 = min(p.rows, (rb + 1) * kColRows);
+      for (int64_t r = rb * kColRows + lane_r; r < r1; r += kRowLanes) {
+        int x[16];
+        load16_shifted(p, base + r * p.src_rs, c0, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) part[e] += (uint32_t)x[e];
+        store16_f16(p.dst + (mat * p.rows + r) * p.ld + c0, x, c0, p.ld);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) part_s[lane_r][cgl * 16 + e] = part[e];
+    __syncthreads();
+    // thread t sums column t of the strip over the 16 row lanes
+    const int col = threadIdx.x;
+    const int64_t c = cb * kColGroups * 16 + col;
+    if (c < p.cols) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (int l = 0; l < kRowLanes; ++l) sum += part_s[l][col];
+      atomicAdd(reinterpret_cast<unsigned*>(p.sums) + mat * p.cols + c, sum);
+    }
+  }
 }
 
 struct QLayout {
   int64_t a_count, b_count, kp, np;
-  size_t a_bytes, b_bytes;
+  size_t a_bytes, b_bytes, rs_bytes, cs_bytes;
 };
 
 QLayout qlayout(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_count) {
@@ -112,6 +188,8 @@ QLayout qlayout(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_coun
   l.np = round_up(N, 8);
   l.a_bytes = (size_t)round_up(a_count * M * l.kp * 2, kAlign);
   l.b_bytes = (size_t)round_up(b_count * K * l.np * 2, kAlign);
+  l.rs_bytes = (size_t)round_up(a_count * M * 4, kAlign);
+  l.cs_bytes = (size_t)round_up(b_count * N * 4, kAlign);
   return l;
 }
 
@@ -150,7 +228,7 @@ bool plan_qlinear(const QLinearArgs& q, const QLayout& l, void* ws, OperandPlan*
 
 size_t tc_qlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t a_count, int64_t b_count) {
   const QLayout l = qlayout(M, N, K, a_count, b_count);
-  return l.a_bytes + l.b_bytes;
+  return l.a_bytes + l.b_bytes + l.rs_bytes + l.cs_bytes;
 }
 
 bool tc_qlinear_supported(const QLinearArgs& q) {
@@ -163,34 +241,40 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   const QLayout l = qlayout(q.M, q.N, q.K, own_count(q.a_bshape), own_count(q.b_bshape));
   OperandPlan a, b;
   if (!ws || !status || !plan_qlinear(q, l, ws, &a, &b)) return MM_ERR_UNSUPPORTED;
-  __half* a16 = static_cast<__half*>(ws);
-  __half* b16 = reinterpret_cast<__half*>(static_cast<char*>(ws) + l.a_bytes);
+  char* base = static_cast<char*>(ws);
+  __half* a16 = reinterpret_cast<__half*>(base);
+  __half* b16 = reinterpret_cast<__half*>(base + l.a_bytes);
+  int32_t* rs = reinterpret_cast<int32_t*>(base + l.a_bytes + l.b_bytes);
+  int32_t* cs = reinterpret_cast<int32_t*>(base + l.a_bytes + l.b_bytes + l.rs_bytes);
 
-  // 1. a - a_zero_point (per row) and b - b_zero_point (per column) as exact f16.
+  // 1. a' = a - c_a with row sums, b' = b - c_b with column sums, as exact f16.
   ShiftArgs sa;
   memset(&sa, 0, sizeof(sa));
   sa.src = static_cast<const uint8_t*>(q.a.ptr); sa.is_signed = q.a_signed; sa.nb = q.bm.nb;
   sa.src_rs = q.a.rs; sa.src_cs = q.a.cs;
-  sa.zp = static_cast<const uint8_t*>(q.za.ptr); sa.zp_vs = q.za.vs; sa.zp_per_col = 0;
-  sa.rows = q.M; sa.cols = q.K; sa.ld = l.kp; sa.count = l.a_count; sa.dst = a16;
+  sa.rows = q.M; sa.cols = q.K; sa.ld = l.kp; sa.count = l.a_count; sa.dst = a16; sa.sums = rs;
   ShiftArgs sb = sa;
   sb.src = static_cast<const uint8_t*>(q.b.ptr); sb.is_signed = q.b_signed;
   sb.src_rs = q.b.rs; sb.src_cs = q.b.cs;
-  sb.zp = static_cast<const uint8_t*>(q.zb.ptr); sb.zp_vs = q.zb.vs; sb.zp_per_col = 1;
-  sb.rows = q.K; sb.cols = q.N; sb.ld = l.np; sb.count = l.b_count; sb.dst = b16;
+  sb.rows = q.K; sb.cols = q.N; sb.ld = l.np; sb.count = l.b_count; sb.dst = b16; sb.sums = cs;
   for (int d = 0; d < kMaxBatchDims; ++d) {
     sa.own_shape[d] = d < q.bm.nb ? q.a_bshape[d] : 1;
     sa.src_bstride[d] = q.a.bstride[d];
-    sa.zp_bstride[d] = q.za.bstride[d];
     sb.own_shape[d] = d < q.bm.nb ? q.b_bshape[d] : 1;
     sb.src_bstride[d] = q.b.bstride[d];
-    sb.zp_bstride[d] = q.zb.bstride[d];
   }
-  mm_status st = launch_shift(sa, stream);
-  if (st == MM_OK) st = launch_shift(sb, stream);
-  if (st != MM_OK) return st;
+  if (cudaMemsetAsync(cs, 0, (size_t)(l.b_count * q.N * 4), stream) != cudaSuccess) return MM_ERR_CUDA;
+  const int64_t awarps = l.a_count * q.M;
+  const int64_t ablocks = (awarps + 7) / 8;
+  shift_rows_kernel<<<(unsigned)(ablocks < 8 * 152 * 8 ? ablocks : 8 * 152 * 8), 256, 0, stream>>>(sa);
+  const int64_t bblocks =
+      l.b_count * ((q.K + kColRows - 1) / kColRows) * ((((q.N + 15) / 16) + kColGroups - 1) / kColGroups);
+  shift_cols_kernel<<<(unsigned)(bblocks < 16 * 152 * 8 ? bblocks : 16 * 152 * 8), kColGroups * kRowLanes, 0,
+                      stream>>>(sb);
+  if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
 
-  // 2. The f16 GEMM with 256-deep exact segments and the requantising epilogue.
+  // 2. The f16 GEMM with 1024-deep exact segments and the zero-point-correcting,
+  //    requantising epilogue.
   TcParams p;
   init_params(&p);
   p.M = q.M; p.N = q.N; p.K = q.K;
@@ -198,15 +282,17 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   p.nt = (q.N + kTileN - 1) / kTileN;
   p.bm = q.bm;
   p.tiles = p.mt * p.nt * q.bm.count;
-  p.kb_per_seg = 256 / kTileK;
+  p.kb_per_seg = 1024 / kTileK;
   p.idesc = make_idesc(1, a.mn_major, b.mn_major);
   p.y = const_cast<void*>(q.y.ptr);
   for (int d = 0; d < kMaxBatchDims; ++d) p.y_bstride[d] = q.y.bstride[d];
   p.y_rs = q.y.rs;
   p.y_vec = (reinterpret_cast<uintptr_t>(q.y.ptr) % 16 == 0) && (q.y.rs % 16 == 0);
   for (int d = 0; d < q.bm.nb; ++d) p.y_vec = p.y_vec && (q.y.bstride[d] % 16 == 0);
-  p.sa = q.sa; p.sb = q.sb; p.ys = q.ys; p.yz = q.yz;
+  p.sa = q.sa; p.sb = q.sb; p.za = q.za; p.zb = q.zb; p.ys = q.ys; p.yz = q.yz;
   p.sa_f16 = q.sa_f16; p.sb_f16 = q.sb_f16; p.ys_f16 = q.ys_f16; p.y_signed = q.y_signed;
+  p.a_signed = q.a_signed; p.b_signed = q.b_signed;
+  p.q_rs = rs; p.q_cs = cs;
   p.status = status;
   return launch_tc(kQLinear, a, b, p, p.tiles, stream);
 }
