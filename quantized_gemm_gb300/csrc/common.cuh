@@ -35,6 +35,30 @@ struct VecView {                   // per-row / per-column parameter: ptr[boff(b
   int64_t vs;
 };
 
+// Division of a 32-bit unsigned integer by an invariant divisor 1 <= d < 2^31
+// with one multiply-high and a shift (Granlund & Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, unsigned case):
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, and for every n < 2^32
+// n / d = (mulhi(m, n) + n) >> l, the sum taken in 64 bits.
+struct FastDiv {
+  uint32_t d, mul, shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  f.shift = l;
+  f.mul = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = (uint32_t)(((uint64_t)n * f.mul) >> 32);
+  return (uint32_t)(((uint64_t)t + n) >> f.shift);
+}
+
 // Device status word bits (see mm_get_device_status).
 enum : unsigned { kStatusIndexRange = 1u, kStatusTimeout = 2u };
 

@@ -1,7 +1,7 @@
 // tcgen05 tensor-core GEMM for sm_103a (GB300), shared by the MatMul, Gemm,
 // QLinearMatMul and GroupedMatMul fast paths.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 576 threads, 320 for QLinear):
 //   warp 0      TMA producer: one thread streams A and B tiles (BK = 64) into a
 //               4-stage shared-memory ring, 128-byte swizzled, completing on
 //               per-stage mbarriers (full[s]); it waits on empty[s] before
@@ -11,9 +11,10 @@
 //               256-column TMEM accumulators and commits: empty[s] when a
 //               stage has been consumed, acc_full[b] when an accumulation
 //               segment is complete.
-//   warps 2-9   epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
-//               owns TMEM lanes 32*(w%4).. and one 128-column half), release
-//               the buffer (acc_empty[b]) and write the output.
+//   warps 2-    epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
+//               owns TMEM lanes 32*(w%4).. and one column slice: 16 warps of 64
+//               columns for the float modes, 8 warps of 128 for QLinear),
+//               release the buffer (acc_empty[b]) and write the output.
 // Two TMEM accumulators let the epilogue of one segment overlap the MMAs of
 // the next.  Every mbarrier wait is bounded; a wait that runs out sets the
 // timeout bit of the device status word and the CTA winds down cleanly.
@@ -53,17 +54,29 @@ constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kBBytes = BN * BK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
-constexpr int kEpiWarps = 8;
-constexpr int kEpiWarp0 = 2;                     // warps 2..9 run the epilogue
-constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
-constexpr int kGroupM = 16;                      // raster band height (tiles)
+constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
+constexpr int kGroupM = 16;                      // raster band height (tiles), a power of two
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
 constexpr int kQColWords = 3 * 128;              // QLinear per-warp column staging
-constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + kEpiWarps * kQColWords * 4 + 1024;
+constexpr int kStageWords = 32 * 16;             // float per-warp output staging: 32 rows x 64 bytes
+
+// Per-mode shape of the CTA.  The float epilogues (MatMul/Gemm, GroupedMatMul)
+// use 16 warps of 64 columns each, so that a tile's epilogue has enough warps
+// to hide its latency when K is small; QLinearMatMul keeps 8 warps of 128
+// columns, whose int32 running sums need the registers.
+template <int MODE>
+struct Cfg {
+  static constexpr int kEpiWarps = MODE == kQLinear ? 8 : 16;
+  static constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
+  static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
+  static constexpr int kWarpWords = MODE == kQLinear ? kQColWords : kStageWords;
+  static constexpr int kSmem = kStages * kStageBytes + kCtrlBytes + kEpiWarps * kWarpWords * 4 + 1024;
+  static_assert(kSmem <= 232448, "shared memory per block");
+};
 
 struct Tile {
-  int64_t batch;     // dense: broadcast batch index
+  uint32_t batch;    // dense: broadcast batch index
   int64_t m0, n0;    // first output row / column of the tile
   int32_t a_row;     // TMA coordinate of the first A row
   int32_t a_b, b_b;  // TMA batch coordinates
@@ -71,45 +84,62 @@ struct Tile {
   int32_t g;         // grouped: group
 };
 
+// Offset of broadcast batch index b for per-dimension strides `bstride`,
+// decomposing b with the precomputed divisors.
+__device__ __forceinline__ int64_t batch_off(const TcParams& p, const int64_t* bstride, uint32_t b) {
+  int64_t off = 0;
+  for (int d = p.bm.nb - 1; d >= 0; --d) {
+    const uint32_t q = fast_div(b, p.fd_bshape[d]);
+    off += (int64_t)(b - q * p.fd_bshape[d].d) * bstride[d];
+    b = q;
+  }
+  return off;
+}
+
+// Tile t of the persistent schedule.  `g_hint` carries the group found for the
+// previous tile of the same CTA (tiles only move forward), so the grouped
+// lookup is a short forward scan.
 template <int MODE>
-__device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti) {
+__device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti, int& g_hint) {
   if (t >= total) return false;
   if (MODE == kGrouped) {
-    int lo = 0, hi = p.G;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (p.g_tile_start[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int64_t local = t - p.g_tile_start[lo];
-    const int cnt = p.g_count[lo];
-    const int64_t mtg = (cnt + BM - 1) / BM;
-    const int64_t ntile = local / mtg, mtile = local - ntile * mtg;
+    int g = g_hint;
+    while (g + 1 < p.G && __ldg(p.g_tile_start + g + 1) <= t) ++g;
+    g_hint = g;
+    const uint32_t local = (uint32_t)(t - __ldg(p.g_tile_start + g));
+    const int cnt = __ldg(p.g_count + g);
+    const uint32_t mtg = (uint32_t)((cnt + BM - 1) / BM);
+    const uint32_t ntile = local / mtg, mtile = local - ntile * mtg;
     ti.batch = 0;
-    ti.g = lo;
-    ti.m0 = mtile * BM;
-    ti.n0 = ntile * BN;
-    ti.a_row = p.g_offset[lo] + (int32_t)(mtile * BM);
+    ti.g = g;
+    ti.m0 = (int64_t)mtile * BM;
+    ti.n0 = (int64_t)ntile * BN;
+    ti.a_row = __ldg(p.g_offset + g) + (int32_t)(mtile * BM);
     ti.a_b = 0;
-    ti.b_b = lo;
-    ti.rows = (int32_t)min((int64_t)BM, (int64_t)cnt - mtile * BM);
+    ti.b_b = g;
+    ti.rows = min(BM, cnt - (int)(mtile * BM));
     return true;
   }
-  const int64_t per_batch = p.mt * p.nt;
-  const int64_t b = t / per_batch;
-  const int64_t r = t - b * per_batch;
-  const int64_t band = (int64_t)kGroupM * p.nt;
-  const int64_t gband = r / band;
-  const int64_t w = r - gband * band;
-  const int64_t h = min((int64_t)kGroupM, p.mt - gband * kGroupM);
-  const int64_t mtile = gband * kGroupM + w % h;
-  const int64_t ntile = w / h;
+  const uint32_t tt = (uint32_t)t;
+  const uint32_t b = fast_div(tt, p.fd_per_batch);
+  const uint32_t r = tt - b * p.fd_per_batch.d;
+  const uint32_t gband = fast_div(r, p.fd_band);
+  const uint32_t w = r - gband * p.fd_band.d;
+  uint32_t mtile, ntile;
+  if (gband != p.last_band) {              // full bands are kGroupM (a power of two) tiles high
+    mtile = gband * kGroupM + (w & (kGroupM - 1));
+    ntile = w / kGroupM;
+  } else {
+    ntile = fast_div(w, p.fd_last_h);
+    mtile = gband * kGroupM + (w - ntile * p.fd_last_h.d);
+  }
   ti.batch = b;
   ti.g = 0;
-  ti.m0 = mtile * BM;
-  ti.n0 = ntile * BN;
+  ti.m0 = (int64_t)mtile * BM;
+  ti.n0 = (int64_t)ntile * BN;
   ti.a_row = (int32_t)ti.m0;
-  ti.a_b = (int32_t)batch_offset(p.bm, p.a_bc, b);
-  ti.b_b = (int32_t)batch_offset(p.bm, p.b_bc, b);
+  ti.a_b = (int32_t)batch_off(p, p.a_bc, b);
+  ti.b_b = (int32_t)batch_off(p, p.b_bc, b);
   ti.rows = (int32_t)min((int64_t)BM, p.M - ti.m0);
   return true;
 }
@@ -130,7 +160,8 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
   uint32_t stage = 0, phase = 0;
   uint32_t pending = 0, pend_parity = 0;   // bit s: a load into stage s was issued (and its parity)
   Tile ti;
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+  int gh = 0;
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.status, p.timeout_ns)) goto done;
       const uint32_t full = full0 + 8 * stage;
@@ -168,7 +199,8 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
   const int64_t total = total_tiles<MODE>(p);
   uint32_t stage = 0, phase = 0, seg = 0;
   Tile ti;
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+  int gh = 0;
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
     for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_seg) {
       const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
       if (!mbar_wait(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns)) goto done;
@@ -235,23 +267,6 @@ __device__ __forceinline__ void add_c32(const TcParams& p, const uint16_t* crow,
   }
 }
 
-__device__ __forceinline__ void store32_16(const TcParams& p, uint16_t* yrow, int64_t n, const float (&v)[32]) {
-  if (p.y_vec && n + 32 <= p.N) {
-    uint4* dst = reinterpret_cast<uint4*>(yrow + n);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      dst[q] = make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16), pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
-                          pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16), pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16));
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n + j < p.N) {
-        const uint32_t w = pack2(v[j], 0.f, p.out_f16);
-        yrow[n + j] = (uint16_t)(w & 0xFFFF);
-      }
-  }
-}
-
 __device__ __forceinline__ float load_scale(const void* base, int64_t off, int is_f16) {
   return is_f16 ? __half2float(static_cast<const __half*>(base)[off]) : static_cast<const float*>(base)[off];
 }
@@ -281,9 +296,14 @@ __device__ __forceinline__ uint32_t requant_byte(int32_t acc, float sa, float sb
 
 template <int MODE>
 __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort,
-                             int32_t* qcol) {
+                             uint32_t* stage) {
+  // Warp-private shared memory: QLinear column data (kQColWords) or the
+  // output staging rows (kStageWords).
+  int32_t* qcol = reinterpret_cast<int32_t*>(stage);
+  uint32_t* stg = stage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quad = warp & 3, half = (warp - kEpiWarp0) >> 2;
+  const int quad = warp & 3, slice = (warp - kEpiWarp0) >> 2;
+  constexpr int kCols = Cfg<MODE>::kCols;
   const int rloc = quad * 32 + lane;
   const uint32_t tlane = (uint32_t)(quad * 32) << 16;
   const int64_t total = total_tiles<MODE>(p);
@@ -297,15 +317,16 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
     qmin = p.y_signed ? -128.f : 0.f;
     qmax = p.y_signed ? 127.f : 255.f;
   }
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti); t += gridDim.x) {
+  int gh = 0;
+  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
     const bool row_ok = rloc < ti.rows;
-    const int64_t ncol0 = ti.n0 + half * 128;
+    const int64_t ncol0 = ti.n0 + slice * kCols;
     if (MODE == kQLinear) {
       // Column data of this warp's 128 columns (zero point, column sum, scale),
       // staged once per tile in a warp-private shared-memory slice.
       {
-        const int64_t zboff = batch_offset(p.bm, p.zb.bstride, ti.batch);
-        const int64_t sboff = batch_offset(p.bm, p.sb.bstride, ti.batch);
+        const int64_t zboff = batch_off(p, p.zb.bstride, ti.batch);
+        const int64_t sboff = batch_off(p, p.sb.bstride, ti.batch);
         const int32_t* cs = p.q_cs + (int64_t)ti.b_b * p.N;
         const int bshift = p.b_signed ? 0 : 128;
         for (int j = lane; j < 128; j += 32) {
@@ -328,7 +349,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
         tc_fence_after();
-        const uint32_t taddr = tmem + tlane + buf * BN + half * 128;
+        const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -346,13 +367,13 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       }
       if (row_ok) {
         const int64_t m = ti.m0 + rloc;
-        const float sa = load_scale(p.sa.ptr, batch_offset(p.bm, p.sa.bstride, ti.batch) + m * p.sa.vs, p.sa_f16);
-        const uint32_t za = (uint32_t)((int32_t)load_q8(p.za.ptr, batch_offset(p.bm, p.za.bstride, ti.batch) + m * p.za.vs,
+        const float sa = load_scale(p.sa.ptr, batch_off(p, p.sa.bstride, ti.batch) + m * p.sa.vs, p.sa_f16);
+        const uint32_t za = (uint32_t)((int32_t)load_q8(p.za.ptr, batch_off(p, p.za.bstride, ti.batch) + m * p.za.vs,
                                                         p.a_signed) - (p.a_signed ? 0 : 128));
         const uint32_t rs = (uint32_t)p.q_rs[(int64_t)ti.a_b * p.M + m];
         // acc - zb'*rs - za'*cs + K*za'*zb' = acc - zb'*(rs - K*za') - za'*cs   (mod 2^32)
         const uint32_t rowterm = rs - (uint32_t)p.K * za;
-        uint8_t* yrow = static_cast<uint8_t*>(p.y) + batch_offset(p.bm, p.y_bstride, ti.batch) + m * p.y_rs;
+        uint8_t* yrow = static_cast<uint8_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t n = ncol0 + c * 32;
@@ -391,35 +412,64 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       ++seg;
       if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
       tc_fence_after();
-      const uint32_t taddr = tmem + tlane + buf * BN + half * 128;
-      uint32_t r[4][32];
+      const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
+      uint32_t r[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, r[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(taddr + c * 32, r[c]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * buf);
-      if (!row_ok) continue;
+      // This thread's output row (kept even when the row is past the tile's
+      // valid rows: it is then only shuffled around, never dereferenced).
       uint16_t* yrow;
       const uint16_t* crow = nullptr;
       if (MODE == kGrouped) {
-        const int64_t orow = p.g_rowlist[ti.a_row + rloc];
+        const int64_t orow = row_ok ? p.g_rowlist[ti.a_row + rloc] : 0;
         yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
-        if (p.c) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
+        if (p.c && row_ok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
       } else {
         const int64_t m = ti.m0 + rloc;
-        yrow = static_cast<uint16_t*>(p.y) + batch_offset(p.bm, p.y_bstride, ti.batch) + m * p.y_rs;
-        if (p.c) crow = static_cast<const uint16_t*>(p.c) + batch_offset(p.bm, p.c_bstride, ti.batch) + m * p.c_rs;
+        yrow = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
+        if (p.c && row_ok)
+          crow = static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs;
       }
+      // Each 32-column chunk (64 bytes of each of the warp's 32 rows) is staged
+      // through the warp's shared-memory slice (16-byte pieces XOR-swizzled by
+      // row pair, so both the row-wise writes and the column-wise reads are
+      // bank-conflict free) and written back so that each warp store covers 8
+      // rows x 64 bytes of whole 32-byte sectors.
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int64_t n = ncol0 + c * 32;
+      for (int h = 0; h < 2; ++h) {
+        const int64_t n = ncol0 + 32 * h;
         if (n >= p.N) break;
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[c][j]);
+        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
         if (crow) add_c32(p, crow, n, v);
-        store32_16(p, yrow, n, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1], p.out_f16);
+        if (p.y_vec && n + 32 <= p.N) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(stg + lane * 16 + ((q ^ ((lane >> 1) & 3)) * 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (lane >> 2), pc = lane & 3;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
+            uint16_t* dst = reinterpret_cast<uint16_t*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(yrow), rr));
+            if (quad * 32 + rr < ti.rows) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
+          }
+          __syncwarp();
+        } else if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+        }
       }
     }
   }
@@ -428,7 +478,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
 // ------------------------------------------------------------------ kernel
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -449,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, kEpiWarps);
+      mbar_init(acce0 + 8 * b, Cfg<MODE>::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -469,9 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) run_mma<MODE>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
   } else if (warp >= kEpiWarp0) {
-    // QLinear column staging: 3 x 128 words per epilogue warp after the control block.
-    int32_t* qcol = reinterpret_cast<int32_t*>(ctrl + kCtrlBytes) + (warp - kEpiWarp0) * kQColWords;
-    run_epilogue<MODE>(p, tmem, accf0, acce0, abort, qcol);
+    uint32_t* stage = reinterpret_cast<uint32_t*>(ctrl + kCtrlBytes) +
+                      (warp - kEpiWarp0) * Cfg<MODE>::kWarpWords;
+    run_epilogue<MODE>(p, tmem, accf0, acce0, abort, stage);
   }
   tc_fence_before();
   __syncthreads();
@@ -599,22 +649,41 @@ mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcPara
   p.b_mn = b.mn_major;
   for (int d = 0; d < kMaxBatchDims; ++d) { p.a_bc[d] = a.bc[d]; p.b_bc[d] = b.bc[d]; }
   p.num_kb = (int)((p.K + BK - 1) / BK);
+  if (mode != kGrouped) {
+    if (p.tiles >= (1ll << 31) || p.mt * p.nt >= (1ll << 31)) return MM_ERR_UNSUPPORTED;
+    const uint32_t per_batch = (uint32_t)(p.mt * p.nt);
+    const uint32_t bands = (uint32_t)((p.mt + kGroupM - 1) / kGroupM);
+    p.fd_per_batch = make_fastdiv(per_batch);
+    p.fd_band = make_fastdiv((uint32_t)(kGroupM * p.nt));
+    p.last_band = bands - 1;
+    p.fd_last_h = make_fastdiv((uint32_t)(p.mt - (int64_t)(bands - 1) * kGroupM));
+  }
+  for (int d = 0; d < kMaxBatchDims; ++d) {
+    if (p.bm.shape[d] >= (1ll << 31)) return MM_ERR_UNSUPPORTED;
+    p.fd_bshape[d] = make_fastdiv((uint32_t)(p.bm.shape[d] > 0 ? p.bm.shape[d] : 1));
+  }
   if (p.kb_per_seg > p.num_kb) p.kb_per_seg = p.num_kb > 0 ? p.num_kb : 1;
   const int sms = sm_count();
   const int grid = (int)(grid_tiles < sms ? (grid_tiles > 0 ? grid_tiles : 1) : sms);
   cudaError_t e = cudaSuccess;
   switch (mode) {
     case kDense:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) tc_gemm_kernel<kDense><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<kDense>::kSmem);
+      if (e == cudaSuccess)
+        tc_gemm_kernel<kDense><<<grid, Cfg<kDense>::kThreads, Cfg<kDense>::kSmem, stream>>>(a.map, b.map, p);
       break;
     case kGrouped:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) tc_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<kGrouped>::kSmem);
+      if (e == cudaSuccess)
+        tc_gemm_kernel<kGrouped><<<grid, Cfg<kGrouped>::kThreads, Cfg<kGrouped>::kSmem, stream>>>(a.map, b.map, p);
       break;
     case kQLinear:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kQLinear>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e == cudaSuccess) tc_gemm_kernel<kQLinear><<<grid, kThreads, kSmemBytes, stream>>>(a.map, b.map, p);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<kQLinear>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<kQLinear>::kSmem);
+      if (e == cudaSuccess)
+        tc_gemm_kernel<kQLinear><<<grid, Cfg<kQLinear>::kThreads, Cfg<kQLinear>::kSmem, stream>>>(a.map, b.map, p);
       break;
     default:
       return MM_ERR_UNSUPPORTED;

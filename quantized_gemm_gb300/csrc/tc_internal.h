@@ -19,6 +19,12 @@ struct TcParams {
   int64_t M, N, K;
   int64_t mt, nt, tiles;                       // tile counts (dense / qlinear)
   BatchMap bm;
+  // 32-bit tile decoding (filled by launch_tc): divisors by the tiles per
+  // batch, per raster band and (last band) the band height, and by each batch
+  // dimension; tile indices are < 2^31.
+  FastDiv fd_per_batch, fd_band, fd_last_h;
+  uint32_t last_band;
+  FastDiv fd_bshape[kMaxBatchDims];
   int64_t a_bc[kMaxBatchDims], b_bc[kMaxBatchDims];   // batch index -> TMA batch coordinate
   int a_mn, b_mn;                              // operand is MN-major in shared memory
   int num_kb, kb_per_seg;                      // k-blocks; k-blocks per accumulation segment
