@@ -50,12 +50,24 @@ using namespace ptx;
 namespace {
 
 constexpr int BM = kTileM, BN = kTileN, BK = kTileK;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;             // 16 KB
-constexpr int kBBytes = BN * BK * 2;             // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
+
+// Shared-memory ring geometry.  One CTA: A 128x64 + B 256x64 per stage (48 KB),
+// 4 stages.  CTA pair (cta_group::2, a 256 x 256 tile per pair): each CTA holds
+// its 128 rows of A and half (128) of the tile's B columns, 32 KB per stage,
+// 6 stages.
+template <bool PAIR>
+struct Geo {
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;     // B columns (rows of B') held by one CTA
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
+  static constexpr int kRingBytes = kStages * kStageBytes;
+};
 constexpr int kGroupM = 16;                      // raster band height (tiles), a power of two
+constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
 constexpr int kQColWords = 3 * 128;              // QLinear per-warp column staging
@@ -65,14 +77,15 @@ constexpr int kStageWords = 32 * 16;             // float per-warp output stagin
 // use 16 warps of 64 columns each, so that a tile's epilogue has enough warps
 // to hide its latency when K is small; QLinearMatMul keeps 8 warps of 128
 // columns, whose int32 running sums need the registers.
-template <int MODE>
+template <int MODE, bool PAIR>
 struct Cfg {
   static constexpr int kEpiWarps = MODE == kQLinear ? 8 : 16;
   static constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
   static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
   static constexpr int kWarpWords = MODE == kQLinear ? kQColWords : kStageWords;
-  static constexpr int kSmem = kStages * kStageBytes + kCtrlBytes + kEpiWarps * kWarpWords * 4 + 1024;
+  static constexpr int kSmem = Geo<PAIR>::kRingBytes + kCtrlBytes + kEpiWarps * kWarpWords * 4 + 1024;
   static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(16 * Geo<PAIR>::kStages + 48 <= kCtrlBytes, "control block");
 };
 
 struct Tile {
@@ -99,7 +112,7 @@ __device__ __forceinline__ int64_t batch_off(const TcParams& p, const int64_t* b
 // Tile t of the persistent schedule.  `g_hint` carries the group found for the
 // previous tile of the same CTA (tiles only move forward), so the grouped
 // lookup is a short forward scan.
-template <int MODE>
+template <int MODE, bool PAIR>
 __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti, int& g_hint) {
   if (t >= total) return false;
   if (MODE == kGrouped) {
@@ -135,12 +148,12 @@ __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t t
   }
   ti.batch = b;
   ti.g = 0;
-  ti.m0 = (int64_t)mtile * BM;
+  ti.m0 = (int64_t)mtile * Geo<PAIR>::kTileRows;
   ti.n0 = (int64_t)ntile * BN;
   ti.a_row = (int32_t)ti.m0;
   ti.a_b = (int32_t)batch_off(p, p.a_bc, b);
   ti.b_b = (int32_t)batch_off(p, p.b_bc, b);
-  ti.rows = (int32_t)min((int64_t)BM, p.M - ti.m0);
+  ti.rows = (int32_t)min((int64_t)Geo<PAIR>::kTileRows, p.M - ti.m0);
   return true;
 }
 
@@ -149,85 +162,133 @@ __device__ __forceinline__ int64_t total_tiles(const TcParams& p) {
   return MODE == kGrouped ? (int64_t)p.g_tile_start[p.G] : p.tiles;
 }
 
+// The persistent schedule: a CTA (or CTA pair) takes tiles first, first + step, ...
+template <bool PAIR>
+__device__ __forceinline__ int64_t first_tile() { return PAIR ? (blockIdx.x >> 1) : blockIdx.x; }
+template <bool PAIR>
+__device__ __forceinline__ int64_t tile_step() { return PAIR ? (gridDim.x >> 1) : gridDim.x; }
+
 // ------------------------------------------------------------------ producer
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const TcParams& p, uint32_t sbase,
                              uint32_t full0, uint32_t empty0, volatile int* abort) {
+  using G = Geo<PAIR>;
   prefetch_tmap(tmA);
   prefetch_tmap(tmB);
   const int64_t total = total_tiles<MODE>(p);
+  // In a pair each CTA loads its own 128 rows of A and 128 columns of B; every
+  // copy completes on the leader CTA's full barrier, which expects both CTAs' bytes.
+  const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
+  const int32_t arow_off = PAIR ? (int32_t)(rank * BM) : 0;
+  const int32_t bcol_off = PAIR ? (int32_t)(rank * G::kBRows) : 0;
   uint32_t stage = 0, phase = 0;
   uint32_t pending = 0, pend_parity = 0;   // bit s: a load into stage s was issued (and its parity)
   Tile ti;
   int gh = 0;
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
+  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.status, p.timeout_ns)) goto done;
       const uint32_t full = full0 + 8 * stage;
-      mbar_arrive_expect_tx(full, kStageBytes);
-      const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
+      const uint32_t sa = sbase + stage * G::kStageBytes, sb = sa + G::kABytes;
       const int32_t k0 = kb * BK;
-      if (!p.a_mn) {
-        tma_load_3d(sa, tmA, k0, ti.a_row, ti.a_b, full);
-      } else {
-        tma_load_3d(sa, tmA, ti.a_row, k0, ti.a_b, full);
-        tma_load_3d(sa + 8192, tmA, ti.a_row + 64, k0, ti.a_b, full);
-      }
-      if (!p.b_mn) {
-        tma_load_3d(sb, tmB, k0, (int32_t)ti.n0, ti.b_b, full);
-      } else {
+      const int32_t ar = ti.a_row + arow_off, bc = (int32_t)ti.n0 + bcol_off;
+      if (PAIR) {
+        const uint32_t bar = mapa_shared(full, 0);
+        if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kStageBytes);
+        if (!p.a_mn) {
+          tma_load_3d_pair(sa, tmA, k0, ar, ti.a_b, bar);
+        } else {
+          tma_load_3d_pair(sa, tmA, ar, k0, ti.a_b, bar);
+          tma_load_3d_pair(sa + 8192, tmA, ar + 64, k0, ti.a_b, bar);
+        }
+        if (!p.b_mn) {
+          tma_load_3d_pair(sb, tmB, k0, bc, ti.b_b, bar);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * 8192, tmB, (int32_t)ti.n0 + 64 * j, k0, ti.b_b, full);
+          for (int j = 0; j < G::kBRows / 64; ++j) tma_load_3d_pair(sb + j * 8192, tmB, bc + 64 * j, k0, ti.b_b, bar);
+        }
+      } else {
+        mbar_arrive_expect_tx(full, G::kStageBytes);
+        if (!p.a_mn) {
+          tma_load_3d(sa, tmA, k0, ar, ti.a_b, full);
+        } else {
+          tma_load_3d(sa, tmA, ar, k0, ti.a_b, full);
+          tma_load_3d(sa + 8192, tmA, ar + 64, k0, ti.a_b, full);
+        }
+        if (!p.b_mn) {
+          tma_load_3d(sb, tmB, k0, bc, ti.b_b, full);
+        } else {
+#pragma unroll
+          for (int j = 0; j < G::kBRows / 64; ++j) tma_load_3d(sb + j * 8192, tmB, bc + 64 * j, k0, ti.b_b, full);
+        }
       }
       pending |= 1u << stage;
       pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
+      if (++stage == G::kStages) { stage = 0; phase ^= 1; }
     }
   }
 done:
-  // Let every issued copy land before the CTA can exit.
-  for (int s = 0; s < kStages; ++s)
-    if (pending & (1u << s)) mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
+  // Let every issued copy land before the CTA can exit.  In a pair the leader's
+  // full barriers count both CTAs' bytes, so the leader waits for both.
+  if (!PAIR || rank == 0)
+    for (int s = 0; s < G::kStages; ++s)
+      if (pending & (1u << s)) {
+        if (PAIR) mbar_wait_teardown_cluster(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
+        else mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
+      }
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
-template <int MODE>
+// In a pair only the leader CTA runs this: one M=256 MMA covers both CTAs' rows
+// (A and B halves read from both CTAs' shared memory at the same offsets), and
+// every commit signals the barrier of that name in both CTAs.
+template <int MODE, bool PAIR>
 __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32_t full0, uint32_t empty0,
                         uint32_t accf0, uint32_t acce0, uint32_t drain, volatile int* abort) {
+  using G = Geo<PAIR>;
   const int64_t total = total_tiles<MODE>(p);
   uint32_t stage = 0, phase = 0, seg = 0;
   Tile ti;
   int gh = 0;
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
+  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
     for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_seg) {
       const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
-      if (!mbar_wait(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns)) goto done;
+      const bool ok = PAIR ? mbar_wait_cluster(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns)
+                           : mbar_wait(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns);
+      if (!ok) goto done;
       tc_fence_after();
       const uint32_t d = tmem + buf * BN;
       const int kb1 = min(kb0 + p.kb_per_seg, p.num_kb);
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns)) goto done;
+        const bool got = PAIR ? mbar_wait_cluster(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns)
+                              : mbar_wait(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+        if (!got) goto done;
         tc_fence_after();
-        const uint32_t sa = sbase + stage * kStageBytes, sb = sa + kABytes;
+        const uint32_t sa = sbase + stage * G::kStageBytes, sb = sa + G::kABytes;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           // K-major: advance 32 bytes inside the 128-byte swizzle row.
           // MN-major: advance two 8-row (1024-byte) swizzle atoms.
           const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
           const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
-          tc_mma_f16(d, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+          if (PAIR) tc_mma_f16_pair(d, ad, bd, p.idesc, acc);
+          else tc_mma_f16(d, ad, bd, p.idesc, acc);
         }
-        tc_commit(empty0 + 8 * stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
+        else tc_commit(empty0 + 8 * stage);
+        if (++stage == G::kStages) { stage = 0; phase ^= 1; }
       }
-      tc_commit(accf0 + 8 * buf);
+      if (PAIR) tc_commit_pair(accf0 + 8 * buf, 0x3);
+      else tc_commit(accf0 + 8 * buf);
       ++seg;
     }
   }
 done:
-  tc_commit(drain);
+  if (PAIR) tc_commit_pair(drain, 0x3);
+  else tc_commit(drain);
   mbar_wait_teardown(drain, 0, p.teardown_ns);
 }
 
@@ -294,7 +355,7 @@ __device__ __forceinline__ uint32_t requant_byte(int32_t acc, float sa, float sb
 
 // ------------------------------------------------------------------ epilogue
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort,
                              uint32_t* stage) {
   // Warp-private shared memory: QLinear column data (kQColWords) or the
@@ -303,7 +364,21 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
   uint32_t* stg = stage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3, slice = (warp - kEpiWarp0) >> 2;
-  constexpr int kCols = Cfg<MODE>::kCols;
+  constexpr int kCols = Cfg<MODE, PAIR>::kCols;
+  // In a pair this CTA's TMEM lanes hold rows rank*128.. of the 256-row tile.
+  const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
+  const int64_t row_off = (int64_t)rank * BM;
+  // acc_empty lives in the leader CTA; every epilogue warp of the pair arrives there.
+  auto release = [&](uint32_t buf) {
+    if (lane == 0) {
+      if (PAIR) mbar_arrive_cluster(mapa_shared(acce0 + 8 * buf, 0));
+      else mbar_arrive(acce0 + 8 * buf);
+    }
+  };
+  auto wait_full = [&](uint32_t buf, uint32_t aph) {
+    return PAIR ? mbar_wait_cluster(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns)
+                : mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns);
+  };
   const int rloc = quad * 32 + lane;
   const uint32_t tlane = (uint32_t)(quad * 32) << 16;
   const int64_t total = total_tiles<MODE>(p);
@@ -318,8 +393,9 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
     qmax = p.y_signed ? 127.f : 255.f;
   }
   int gh = 0;
-  for (int64_t t = blockIdx.x; get_tile<MODE>(p, t, total, ti, gh); t += gridDim.x) {
-    const bool row_ok = rloc < ti.rows;
+  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+    const int rows_cta = PAIR ? max(0, min(BM, ti.rows - (int)row_off)) : ti.rows;
+    const bool row_ok = rloc < rows_cta;
     const int64_t ncol0 = ti.n0 + slice * kCols;
     if (MODE == kQLinear) {
       // Column data of this warp's 128 columns (zero point, column sum, scale),
@@ -347,7 +423,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       int32_t acc[4][32];
       for (int s = 0; s < nseg; ++s, ++seg) {
         const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
+        if (!__all_sync(0xffffffffu, wait_full(buf, aph))) return;
         tc_fence_after();
         const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
 #pragma unroll
@@ -363,10 +439,10 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+        release(buf);
       }
       if (row_ok) {
-        const int64_t m = ti.m0 + rloc;
+        const int64_t m = ti.m0 + row_off + rloc;
         const float sa = load_scale(p.sa.ptr, batch_off(p, p.sa.bstride, ti.batch) + m * p.sa.vs, p.sa_f16);
         const uint32_t za = (uint32_t)((int32_t)load_q8(p.za.ptr, batch_off(p, p.za.bstride, ti.batch) + m * p.za.vs,
                                                         p.a_signed) - (p.a_signed ? 0 : 128));
@@ -410,7 +486,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
     } else {
       const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
       ++seg;
-      if (!__all_sync(0xffffffffu, mbar_wait(accf0 + 8 * buf, aph, abort, p.status, p.timeout_ns))) return;
+      if (!__all_sync(0xffffffffu, wait_full(buf, aph))) return;
       tc_fence_after();
       const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
       uint32_t r[2][32];
@@ -419,7 +495,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+      release(buf);
       // This thread's output row (kept even when the row is past the tile's
       // valid rows: it is then only shuffled around, never dereferenced).
       uint16_t* yrow;
@@ -429,7 +505,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
         if (p.c && row_ok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
       } else {
-        const int64_t m = ti.m0 + rloc;
+        const int64_t m = ti.m0 + row_off + rloc;
         yrow = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
         if (p.c && row_ok)
           crow = static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs;
@@ -462,7 +538,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
             const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
             uint16_t* dst = reinterpret_cast<uint16_t*>(
                 __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(yrow), rr));
-            if (quad * 32 + rr < ti.rows) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
+            if (quad * 32 + rr < rows_cta) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
           }
           __syncwarp();
         } else if (row_ok) {
@@ -477,58 +553,76 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
 
 // ------------------------------------------------------------------ kernel
 
-template <int MODE>
-__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
+template <int MODE, bool PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
+  using G = Geo<PAIR>;
+  constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* ctrl = smem_raw + (sbase - raw) + kStages * kStageBytes;
-  const uint32_t cbase = sbase + kStages * kStageBytes;
-  const uint32_t full0 = cbase, empty0 = cbase + 8 * kStages, accf0 = cbase + 16 * kStages;
+  uint8_t* ctrl = smem_raw + (sbase - raw) + G::kRingBytes;
+  const uint32_t cbase = sbase + G::kRingBytes;
+  const uint32_t full0 = cbase, empty0 = cbase + 8 * S, accf0 = cbase + 16 * S;
   const uint32_t acce0 = accf0 + 16, drain = acce0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 16 * kStages + 40);
-  volatile int* abort = reinterpret_cast<volatile int*>(ctrl + 16 * kStages + 44);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 16 * S + 40);
+  volatile int* abort = reinterpret_cast<volatile int*>(ctrl + 16 * S + 44);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, Cfg<MODE>::kEpiWarps);
+      mbar_init(acce0 + 8 * b, (PAIR ? 2 : 1) * Cfg<MODE, PAIR>::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
   }
+  // A pair's barriers must be initialised in both CTAs before either CTA
+  // signals the other's.
+  if (PAIR) cluster_sync();
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<MODE>(&tmA, &tmB, p, sbase, full0, empty0, abort);
+    if (lane == 0) run_producer<MODE, PAIR>(&tmA, &tmB, p, sbase, full0, empty0, abort);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<MODE>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
+    if (lane == 0) {
+      if (rank == 0) run_mma<MODE, PAIR>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
+      else mbar_wait_teardown(drain, 0, p.teardown_ns);   // the leader's last commit reaches this CTA too
+    }
   } else if (warp >= kEpiWarp0) {
     uint32_t* stage = reinterpret_cast<uint32_t*>(ctrl + kCtrlBytes) +
-                      (warp - kEpiWarp0) * Cfg<MODE>::kWarpWords;
-    run_epilogue<MODE>(p, tmem, accf0, acce0, abort, stage);
+                      (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
+    run_epilogue<MODE, PAIR>(p, tmem, accf0, acce0, abort, stage);
   }
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair may leave (or free tensor memory) while the other
+  // can still signal its barriers or its MMAs can still touch its memory.
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -620,12 +714,13 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
   return r == CUDA_SUCCESS;
 }
 
-uint32_t make_idesc(int f16, int a_mn, int b_mn) {
+uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair) {
+  const uint32_t m = pair ? 2 * BM : BM;        // a pair's MMA covers both CTAs' rows
   return (1u << 4)                              // D: fp32
          | ((f16 ? 0u : 1u) << 7)               // A: f16 (0) / bf16 (1)
          | ((f16 ? 0u : 1u) << 10)              // B: f16 (0) / bf16 (1)
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
-         | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         | ((uint32_t)(BN >> 3) << 17) | ((m >> 4) << 24);
 }
 
 namespace {
@@ -643,13 +738,87 @@ void init_params(TcParams* p) {
   p->kb_per_seg = 1 << 30;
 }
 
-mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcParams& p, int64_t grid_tiles,
+namespace {
+
+// Clusters of 2 CTAs (one CTA per SM) that can be resident at once for a
+// kernel, queried once per device (0 if none).
+template <int MODE>
+int max_pair_clusters() {
+  static int cache[128];
+  static bool done[128];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) return 0;
+  if (!done[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+    cfg.blockDim = dim3(Cfg<MODE, true>::kThreads);
+    cfg.dynamicSmemBytes = Cfg<MODE, true>::kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<MODE, true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[dev] = n;
+    done[dev] = true;
+  }
+  return cache[dev];
+}
+
+template <int MODE, bool PAIR>
+mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const TcParams& p, int64_t work,
+                        cudaStream_t stream) {
+  constexpr int kSmem = Cfg<MODE, PAIR>::kSmem, kThreadsM = Cfg<MODE, PAIR>::kThreads;
+  if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+      cudaSuccess)
+    return MM_ERR_CUDA;
+  if (!PAIR) {
+    const int sms = sm_count();
+    const int grid = (int)(work < sms ? (work > 0 ? work : 1) : sms);
+    tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, p);
+    return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+  }
+  // One persistent pair per resident cluster slot: a pair that could not be
+  // resident would only start after the others finish.
+  const int slots = max_pair_clusters<MODE>();
+  if (slots <= 0) return MM_ERR_UNSUPPORTED;
+  const int clusters = (int)(work < slots ? (work > 0 ? work : 1) : slots);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(kThreadsM);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, p) == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+}  // namespace
+
+mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan& b, TcParams& p,
                     cudaStream_t stream) {
   p.a_mn = a.mn_major;
   p.b_mn = b.mn_major;
   for (int d = 0; d < kMaxBatchDims; ++d) { p.a_bc[d] = a.bc[d]; p.b_bc[d] = b.bc[d]; }
   p.num_kb = (int)((p.K + BK - 1) / BK);
+  int64_t work = 0;
   if (mode != kGrouped) {
+    const int64_t rows = pair ? 2 * BM : BM;
+    p.mt = (p.M + rows - 1) / rows;
+    p.nt = (p.N + BN - 1) / BN;
+    p.tiles = p.mt * p.nt * p.bm.count;
     if (p.tiles >= (1ll << 31) || p.mt * p.nt >= (1ll << 31)) return MM_ERR_UNSUPPORTED;
     const uint32_t per_batch = (uint32_t)(p.mt * p.nt);
     const uint32_t bands = (uint32_t)((p.mt + kGroupM - 1) / kGroupM);
@@ -657,40 +826,33 @@ mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcPara
     p.fd_band = make_fastdiv((uint32_t)(kGroupM * p.nt));
     p.last_band = bands - 1;
     p.fd_last_h = make_fastdiv((uint32_t)(p.mt - (int64_t)(bands - 1) * kGroupM));
+    work = p.tiles;
+  } else {
+    work = sm_count();          // the tile count is known only on the device
   }
   for (int d = 0; d < kMaxBatchDims; ++d) {
     if (p.bm.shape[d] >= (1ll << 31)) return MM_ERR_UNSUPPORTED;
     p.fd_bshape[d] = make_fastdiv((uint32_t)(p.bm.shape[d] > 0 ? p.bm.shape[d] : 1));
   }
   if (p.kb_per_seg > p.num_kb) p.kb_per_seg = p.num_kb > 0 ? p.num_kb : 1;
-  const int sms = sm_count();
-  const int grid = (int)(grid_tiles < sms ? (grid_tiles > 0 ? grid_tiles : 1) : sms);
-  cudaError_t e = cudaSuccess;
   switch (mode) {
     case kDense:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<kDense>::kSmem);
-      if (e == cudaSuccess)
-        tc_gemm_kernel<kDense><<<grid, Cfg<kDense>::kThreads, Cfg<kDense>::kSmem, stream>>>(a.map, b.map, p);
-      break;
+      return pair ? launch_kernel<kDense, true>(a, b, p, work, stream)
+                  : launch_kernel<kDense, false>(a, b, p, work, stream);
     case kGrouped:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<kGrouped>::kSmem);
-      if (e == cudaSuccess)
-        tc_gemm_kernel<kGrouped><<<grid, Cfg<kGrouped>::kThreads, Cfg<kGrouped>::kSmem, stream>>>(a.map, b.map, p);
-      break;
+      return launch_kernel<kGrouped, false>(a, b, p, work, stream);
     case kQLinear:
-      e = cudaFuncSetAttribute(tc_gemm_kernel<kQLinear>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<kQLinear>::kSmem);
-      if (e == cudaSuccess)
-        tc_gemm_kernel<kQLinear><<<grid, Cfg<kQLinear>::kThreads, Cfg<kQLinear>::kSmem, stream>>>(a.map, b.map, p);
-      break;
+      return pair ? launch_kernel<kQLinear, true>(a, b, p, work, stream)
+                  : launch_kernel<kQLinear, false>(a, b, p, work, stream);
     default:
       return MM_ERR_UNSUPPORTED;
   }
-  if (e != cudaSuccess) return MM_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
+
+// CTA pairs halve the operand bytes each SM must take in per MMA cycle, which
+// is what bounds long-K products; short-K (output-bound) products run better
+// on single CTAs, whose smaller tiles keep more epilogues in flight.
+bool use_pair(int64_t M, int64_t K) { return M > BM && K >= kPairMinK; }
 
 int sm_count_public() { return sm_count(); }
 
@@ -698,12 +860,12 @@ int sm_count_public() { return sm_count(); }
 
 namespace {
 
-bool plan_dense(const GemmArgs& g, OperandPlan* a, OperandPlan* b) {
+bool plan_dense(const GemmArgs& g, bool pair, OperandPlan* a, OperandPlan* b) {
   if (g.dtype != MM_BF16 && g.dtype != MM_F16) return false;
   if (g.M < 2 || g.N < 2 || g.K < 1) return false;
   if (g.y.cs != 1) return false;
   if (!plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM, a)) return false;
-  if (!plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, BN, b)) return false;
+  if (!plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, pair ? BN / 2 : BN, b)) return false;
   return true;
 }
 
@@ -711,21 +873,16 @@ bool plan_dense(const GemmArgs& g, OperandPlan* a, OperandPlan* b) {
 
 bool tc_gemm_supported(const GemmArgs& g) {
   OperandPlan a, b;
-  return plan_dense(g, &a, &b);
+  return plan_dense(g, false, &a, &b);
 }
 
 mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t stream) {
-  OperandPlan a, b;
-  if (!plan_dense(g, &a, &b) || !status) return MM_ERR_UNSUPPORTED;
+  if (!status) return MM_ERR_UNSUPPORTED;
   TcParams p;
   init_params(&p);
   p.M = g.M; p.N = g.N; p.K = g.K;
-  p.mt = (g.M + BM - 1) / BM;
-  p.nt = (g.N + BN - 1) / BN;
   p.bm = g.bm;
-  p.tiles = p.mt * p.nt * g.bm.count;
   p.out_f16 = g.dtype == MM_F16;
-  p.idesc = make_idesc(p.out_f16, a.mn_major, b.mn_major);
   p.y = const_cast<void*>(g.y.ptr);
   for (int d = 0; d < kMaxBatchDims; ++d) { p.y_bstride[d] = g.y.bstride[d]; p.c_bstride[d] = g.c.bstride[d]; }
   p.y_rs = g.y.rs;
@@ -741,7 +898,17 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
     for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % 8 == 0);
   }
   p.status = status;
-  return launch_tc(kDense, a, b, p, p.tiles, stream);
+  // CTA pairs (256-row tiles) for long-K products with more than one row tile;
+  // one CTA per tile otherwise, or if no pair can be placed.
+  for (int attempt = use_pair(g.M, g.K) ? 0 : 1; attempt < 2; ++attempt) {
+    const bool pair = attempt == 0;
+    OperandPlan a, b;
+    if (!plan_dense(g, pair, &a, &b)) return MM_ERR_UNSUPPORTED;
+    p.idesc = make_idesc(p.out_f16, a.mn_major, b.mn_major, pair);
+    const mm_status st = launch_tc(kDense, pair, a, b, p, stream);
+    if (st != MM_ERR_UNSUPPORTED || !pair) return st;
+  }
+  return MM_ERR_UNSUPPORTED;
 }
 
 }  // namespace qg

@@ -67,10 +67,15 @@ struct OperandPlan {
 
 bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int64_t mn_stride, int64_t k_stride,
                   const BatchMap& bm, const int64_t* bstride, int box_mn, OperandPlan* out);
-uint32_t make_idesc(int f16, int a_mn, int b_mn);
+uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair);
 void init_params(TcParams* p);
-mm_status launch_tc(int mode, const OperandPlan& a, const OperandPlan& b, TcParams& p, int64_t grid_tiles,
+// Fills the tile bookkeeping and launches tc_gemm_kernel: one CTA per SM, or
+// (pair) 2-CTA clusters computing 256-row tiles with cta_group::2 MMAs.
+// Returns MM_ERR_UNSUPPORTED when pairs cannot be placed.
+mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan& b, TcParams& p,
                     cudaStream_t stream);
+// Whether an M x K problem uses CTA pairs.
+bool use_pair(int64_t M, int64_t K);
 int sm_count_public();
 
 }  // namespace qg

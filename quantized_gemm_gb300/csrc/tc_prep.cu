@@ -209,7 +209,7 @@ void dense_batch_strides(const BatchMap& bm, const int64_t* own, int64_t matrix_
   }
 }
 
-bool plan_qlinear(const QLinearArgs& q, const QLayout& l, void* ws, OperandPlan* a, OperandPlan* b) {
+bool plan_qlinear(const QLinearArgs& q, const QLayout& l, void* ws, bool pair, OperandPlan* a, OperandPlan* b) {
   if (q.M < 2 || q.N < 2 || q.K < 1) return false;
   if (q.M > 0x7fffffffLL || q.N > 0x7fffffffLL || q.K > 0x7fffffffLL) return false;
   if (q.y.cs != 1) return false;
@@ -220,7 +220,8 @@ bool plan_qlinear(const QLinearArgs& q, const QLayout& l, void* ws, OperandPlan*
   dense_batch_strides(q.bm, q.a_bshape, q.M * l.kp, abs_);
   dense_batch_strides(q.bm, q.b_bshape, q.K * l.np, bbs);
   if (!plan_operand(base, MM_F16, q.M, q.K, l.kp, 1, q.bm, abs_, kTileM, a)) return false;
-  if (!plan_operand(base + l.a_bytes, MM_F16, q.N, q.K, 1, l.np, q.bm, bbs, kTileN, b)) return false;
+  if (!plan_operand(base + l.a_bytes, MM_F16, q.N, q.K, 1, l.np, q.bm, bbs, pair ? kTileN / 2 : kTileN, b))
+    return false;
   return true;
 }
 
@@ -234,13 +235,13 @@ size_t tc_qlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t a_cou
 bool tc_qlinear_supported(const QLinearArgs& q) {
   const QLayout l = qlayout(q.M, q.N, q.K, own_count(q.a_bshape), own_count(q.b_bshape));
   OperandPlan a, b;
-  return plan_qlinear(q, l, nullptr, &a, &b);
+  return plan_qlinear(q, l, nullptr, false, &a, &b);
 }
 
 mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cudaStream_t stream) {
   const QLayout l = qlayout(q.M, q.N, q.K, own_count(q.a_bshape), own_count(q.b_bshape));
   OperandPlan a, b;
-  if (!ws || !status || !plan_qlinear(q, l, ws, &a, &b)) return MM_ERR_UNSUPPORTED;
+  if (!ws || !status || !plan_qlinear(q, l, ws, false, &a, &b)) return MM_ERR_UNSUPPORTED;
   char* base = static_cast<char*>(ws);
   __half* a16 = reinterpret_cast<__half*>(base);
   __half* b16 = reinterpret_cast<__half*>(base + l.a_bytes);
@@ -278,12 +279,8 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   TcParams p;
   init_params(&p);
   p.M = q.M; p.N = q.N; p.K = q.K;
-  p.mt = (q.M + kTileM - 1) / kTileM;
-  p.nt = (q.N + kTileN - 1) / kTileN;
   p.bm = q.bm;
-  p.tiles = p.mt * p.nt * q.bm.count;
   p.kb_per_seg = 1024 / kTileK;
-  p.idesc = make_idesc(1, a.mn_major, b.mn_major);
   p.y = const_cast<void*>(q.y.ptr);
   for (int d = 0; d < kMaxBatchDims; ++d) p.y_bstride[d] = q.y.bstride[d];
   p.y_rs = q.y.rs;
@@ -294,7 +291,16 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   p.a_signed = q.a_signed; p.b_signed = q.b_signed;
   p.q_rs = rs; p.q_cs = cs;
   p.status = status;
-  return launch_tc(kQLinear, a, b, p, p.tiles, stream);
+  // Single CTAs: this product is bound by its epilogue (exact int32 segment
+  // sums and requantisation), which CTA pairs do not shorten.
+  for (int attempt = 1; attempt < 2; ++attempt) {
+    const bool pair = attempt == 0;
+    if (!plan_qlinear(q, l, ws, pair, &a, &b)) return MM_ERR_UNSUPPORTED;
+    p.idesc = make_idesc(1, a.mn_major, b.mn_major, pair);
+    const mm_status st = launch_tc(kQLinear, pair, a, b, p, stream);
+    if (st != MM_ERR_UNSUPPORTED || !pair) return st;
+  }
+  return MM_ERR_UNSUPPORTED;
 }
 
 // ------------------------------------------------------------------ GroupedMatMul: routing
@@ -485,7 +491,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   init_params(&p);
   p.M = rows; p.N = g.N; p.K = g.K;
   p.nt = nt;
-  p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major);
+  p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major, false);
   p.out_f16 = g.dtype == MM_F16;
   p.y = g.out;
   p.y_rs = g.N;
@@ -501,7 +507,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.G = (int)g.G;
   p.status = status;
   // The tile count is known only on the device: one persistent CTA per SM.
-  return launch_tc(kGrouped, a, b, p, sm_count_public(), stream);
+  return launch_tc(kGrouped, false, a, b, p, stream);
 }
 
 }  // namespace qg
