@@ -205,14 +205,22 @@ def time_loop(step, steps, warmup, world, stream, flush=None, sampler=None):
 KERNEL_SOURCES = ("common.cuh", "tc_internal.h", "tc_ptx.cuh", "tc_gemm.cu")
 
 
+def _code_only(text):
+    """C++ source with comments and blank space removed (string literals in the
+    kernel sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash():
-    """Hash of the tensor-core GEMM's sources: a stored ncu traffic figure is
-    valid only while this hash is unchanged."""
+    """Hash of the tensor-core GEMM's code (comments and spacing ignored): a
+    stored ncu traffic figure is valid only while this hash is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_gemm_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update((f + "\n" + _code_only(fh.read())).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,37 +1,47 @@
 // tcgen05 tensor-core GEMM for sm_103a (GB300), shared by the MatMul, Gemm,
 // QLinearMatMul and GroupedMatMul fast paths.
 //
-// Structure (one persistent CTA per SM, 576 threads, 320 for QLinear):
+// Structure (one persistent CTA per SM; 576 threads, 320 for QLinear):
 //   warp 0      TMA producer: one thread streams A and B tiles (BK = 64) into a
-//               4-stage shared-memory ring, 128-byte swizzled, completing on
-//               per-stage mbarriers (full[s]); it waits on empty[s] before
-//               reusing a stage.
+//               shared-memory ring, 128-byte swizzled, completing on per-stage
+//               mbarriers (full[s]); it waits on empty[s] before reusing a stage.
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (M=128, N=256, K=16, fp32 accumulation) into one of two
-//               256-column TMEM accumulators and commits: empty[s] when a
-//               stage has been consumed, acc_full[b] when an accumulation
-//               segment is complete.
+//               (K=16, fp32 accumulation) into one of two 256-column TMEM
+//               accumulators and commits: empty[s] when a stage has been
+//               consumed, acc_full[b] when an accumulation segment is complete.
 //   warps 2-    epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
 //               owns TMEM lanes 32*(w%4).. and one column slice: 16 warps of 64
 //               columns for the float modes, 8 warps of 128 for QLinear),
-//               release the buffer (acc_empty[b]) and write the output.
+//               release the buffer (acc_empty[b]) and write the output through
+//               a swizzled shared-memory stage so that every warp store covers
+//               whole 32-byte sectors.
 // Two TMEM accumulators let the epilogue of one segment overlap the MMAs of
 // the next.  Every mbarrier wait is bounded; a wait that runs out sets the
 // timeout bit of the device status word and the CTA winds down cleanly.
 //
+// Single CTAs compute 128 x 256 tiles with tcgen05.mma.cta_group::1 (4-stage
+// ring of 48 KB).  For long-K dense products two CTAs of a cluster compute one
+// 256 x 256 tile with tcgen05.mma.cta_group::2: each loads its 128 rows of A
+// and half of the tile's B columns (6-stage ring of 32 KB), the even CTA
+// issues the MMAs for both, and commits are multicast to the pair.  Each SM
+// then takes in 64 bytes of operands per MMA cycle instead of 96.
+//
+// Tiles are numbered in a grouped raster (bands of 16 row tiles, for L2 reuse)
+// and decoded with 32-bit multiply-shift division by precomputed divisors.
+//
 // Modes (template parameter):
-//   kDense    MatMul / Gemm: tiles over (batch, M/128, N/256) in a grouped
-//             raster for L2 reuse; epilogue y = alpha*acc + beta*C[bcast],
-//             rounded once to bf16/f16.
+//   kDense    MatMul / Gemm: tiles over (batch, M, N); epilogue
+//             y = alpha*acc + beta*C[bcast], rounded once to bf16/f16.
 //   kGrouped  GroupedMatMul: A rows are the routed (group-ordered) copy of the
 //             input rows, B is weights[g]; tiles come from the device-built
 //             per-group tile table; epilogue adds bias[g] and scatters each
 //             row to output[m, i, :].
-//   kQLinear  QLinearMatMul: operands are the zero-point-shifted int8/uint8
-//             values held exactly in f16 (|x| <= 255).  Products are exact in
-//             fp32 and a 256-deep partial sum is below 2^24, so each 256-deep
-//             segment accumulates exactly in fp32; the epilogue converts each
-//             segment to int32 and adds with wrap-around, then requantises.
+//   kQLinear  QLinearMatMul: operands are int8/uint8 values moved into
+//             [-128, 127] (uint8 minus 128) and held exactly in f16.  Products
+//             are at most 2^14 in magnitude, so each 1024-deep segment sums
+//             exactly in the fp32 accumulator; the epilogue converts each
+//             segment to int32, adds with wrap-around, applies the zero points
+//             from the operands' row and column sums, then requantises.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

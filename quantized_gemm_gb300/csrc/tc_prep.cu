@@ -293,14 +293,8 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   p.status = status;
   // Single CTAs: this product is bound by its epilogue (exact int32 segment
   // sums and requantisation), which CTA pairs do not shorten.
-  for (int attempt = 1; attempt < 2; ++attempt) {
-    const bool pair = attempt == 0;
-    if (!plan_qlinear(q, l, ws, pair, &a, &b)) return MM_ERR_UNSUPPORTED;
-    p.idesc = make_idesc(1, a.mn_major, b.mn_major, pair);
-    const mm_status st = launch_tc(kQLinear, pair, a, b, p, stream);
-    if (st != MM_ERR_UNSUPPORTED || !pair) return st;
-  }
-  return MM_ERR_UNSUPPORTED;
+  p.idesc = make_idesc(1, a.mn_major, b.mn_major, false);
+  return launch_tc(kQLinear, false, a, b, p, stream);
 }
 
 // ------------------------------------------------------------------ GroupedMatMul: routing
