@@ -251,7 +251,7 @@ def gemm_case(dev, M=8192, N=8192, K=8192):
 
 
 def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
-    """The four other workloads: one call of the public API per step."""
+    """The four other workloads and their type variants: one call of the public API per step."""
     import quantized_gemm_gb300 as qg
     out = {}
     bf16_peak = peaks["bf16_tflops"]
@@ -286,38 +286,62 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     del d, Y
     torch.cuda.empty_cache()
 
-    # 4. int8 QLinearMatMul 16384 x 4096 x 4096 (runs on the f16 tensor pipe).
-    d = workloads.qlinear_s8(device=dev)
-    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
-    yq = torch.empty((16384, 4096), dtype=torch.int8, device=dev)
-    ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
-    ms, _ = time_loop(lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws), 20, 3, world,
-                      stream)
-    ops = 2 * 16384 * 4096 * 4096
-    tops = ops / ms / 1e9
-    sat = float(((yq == 127) | (yq == -128)).float().mean().item())
-    out["qlinear_s8"] = {"value": tops, "unit": "TOP/s", "ms_per_call": ms, "bound": "tensor",
-                         "pipe": "f16 (no int8 tensor-core instruction on sm_103a)", "peak_tflops": bf16_peak,
-                         "frac": tops / bf16_peak, "kernels_per_call": 3, "saturated_fraction": sat,
-                         "l2": "inputs+workspace larger than L2"}
-    del d, yq, ws
-    torch.cuda.empty_cache()
+    # 4. int8 QLinearMatMul 16384 x 4096 x 4096 (runs on the f16 tensor pipe),
+    #    then the same product with uint8 / mixed operands, float16 scales and
+    #    batch-indexed quantisation parameters.
+    out["qlinear_s8"] = bench_qlinear(workloads.qlinear_s8(device=dev), world, stream, bf16_peak)
+    for name, kw in sorted(workloads.QLINEAR_VARIANTS.items()):
+        out[name] = bench_qlinear(workloads.qlinear(device=dev, **kw), world, stream, bf16_peak)
 
-    # 5. bf16 GroupedMatMul M=16384, S=2, G=64, K=4096, N=14336.
-    d = workloads.grouped_bf16(device=dev)
-    yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(qg.mm_grouped_matmul_workspace_size(d["input"], d["weights"], d["group_indices"]),
-                     dtype=torch.uint8, device=dev)
-    ms, _ = time_loop(lambda: qg.mm_grouped_matmul(d["input"], d["weights"], d["group_indices"], d["bias"],
-                                                   out=yo, workspace=ws), 10, 3, world, stream)
-    flops = 2 * 16384 * 2 * 4096 * 14336
-    tf = flops / ms / 1e9
-    out["grouped_bf16"] = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor",
-                           "peak_tflops": bf16_peak, "frac": tf / bf16_peak, "kernels_per_call": 4,
-                           "l2": "weights (7.5 GB) larger than L2"}
-    del d, yo, ws
-    torch.cuda.empty_cache()
+    # 5. GroupedMatMul M=16384, S=2, G=64, K=4096, N=14336: bf16 with int32
+    #    indices, then float16 with int64 indices.
+    out["grouped_bf16"] = bench_grouped(workloads.grouped_bf16(device=dev), world, stream, bf16_peak)
+    out["grouped_f16_i64"] = bench_grouped(
+        workloads.grouped_bf16(device=dev, dtype=torch.float16, index_dtype=torch.int64), world, stream, bf16_peak)
     return out
+
+
+def bench_qlinear(d, world, stream, peak):
+    import quantized_gemm_gb300 as qg
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    a, b = d["a"], d["b"]
+    ydims = tuple(a.shape[:-1]) + (b.shape[-1],)
+    y = torch.empty(ydims, dtype=d["y_zero_point"].dtype, device=a.device)
+    ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(a, b), dtype=torch.uint8, device=a.device)
+    ms, _ = time_loop(lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=y, workspace=ws), 20, 3, world,
+                      stream)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    ops = 2 * y.numel() * a.shape[-1]
+    tops = ops / ms / 1e9
+    info = torch.iinfo(y.dtype)
+    sat = float(((y == info.max) | (y == info.min)).float().mean().item())
+    res = {"value": tops, "unit": "TOP/s", "ms_per_call": ms, "bound": "tensor",
+           "pipe": "f16 (no int8 tensor-core instruction on sm_103a)", "peak_tflops": peak, "frac": tops / peak,
+           "kernels_per_call": 3, "saturated_fraction": sat, "l2": "inputs+workspace larger than L2",
+           "types": "a %s, b %s, y %s, scales %s" % (a.dtype, b.dtype, y.dtype, d["a_scale"].dtype),
+           "shape": "a %s, b %s" % (list(a.shape), list(b.shape))}
+    del d, y, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_grouped(d, world, stream, peak):
+    import quantized_gemm_gb300 as qg
+    x, w, gi = d["input"], d["weights"], d["group_indices"]
+    M, K = x.shape
+    S, N = gi.shape[1], w.shape[2]
+    yo = torch.empty((M, S, N), dtype=x.dtype, device=x.device)
+    ws = torch.empty(qg.mm_grouped_matmul_workspace_size(x, w, gi), dtype=torch.uint8, device=x.device)
+    ms, _ = time_loop(lambda: qg.mm_grouped_matmul(x, w, gi, d["bias"], out=yo, workspace=ws), 10, 3, world,
+                      stream)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    tf = 2 * M * S * K * N / ms / 1e9
+    res = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor", "peak_tflops": peak,
+           "frac": tf / peak, "kernels_per_call": 4, "l2": "weights (7.5 GB) larger than L2",
+           "types": "%s, indices %s" % (x.dtype, gi.dtype)}
+    del d, x, w, gi, yo, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline_gemm(d, rows):
@@ -507,10 +531,10 @@ def run_profile_workload(args):
         d = workloads.matmul_bf16_bcast(device=dev)
         Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
         step = lambda: qg.mm_matmul(d["A"], d["B"], out=Y)
-    elif name == "qlinear_s8":
-        d = workloads.qlinear_s8(device=dev)
+    elif name == "qlinear_s8" or name in workloads.QLINEAR_VARIANTS:
+        d = workloads.qlinear(device=dev, **workloads.QLINEAR_VARIANTS.get(name, {}))
         keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
-        yq = torch.empty((16384, 4096), dtype=torch.int8, device=dev)
+        yq = torch.empty(tuple(d["a"].shape[:-1]) + (d["b"].shape[-1],), dtype=d["y_zero_point"].dtype, device=dev)
         ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
         step = lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws)
     elif name.startswith("grouped_bf16"):
@@ -538,7 +562,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--profile-workload", default=None,
-                    help="run only this workload (gemm_bf16, matmul_bf16_bcast, qlinear_s8, grouped_bf16[_gN])")
+                    help="run only this workload (gemm_bf16, matmul_bf16_bcast, qlinear_s8 or a QLinear variant, "
+                         "grouped_bf16[_gN])")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -176,14 +176,15 @@ def test_qlinear_tensor_f16_scales_and_batch():
 
 
 def _swamping_case(K, rows=256, cols=256):
-    """Shifted operands whose running sums reach +-3.9e6 and then cancel.
+    """Large operand values whose products rise to +-3.9e6 and then cancel.
 
     uint8 a with a_zero_point 128 and uint8 b with b_zero_point 0.  In every
     256-deep block of k: 120 terms of (+127)*255 = +32385, 16 terms of
     s_r * j (s_r in {-1, 0, 1} per row, j = 0..15), 120 terms of
     (-128)*253 = -32384.  Each block sums to 120 + 120 * s_r in {0, 120, 240},
-    so with unit scales the uint8 output is the exact accumulator: any bit lost
-    while the running sum is near 2^22 changes the result.
+    so with unit scales the uint8 output is the exact accumulator: a bit lost
+    in any partial sum, however the kernel splits the zero points off, changes
+    the result.
     """
     a = torch.empty((rows, K), dtype=torch.uint8)
     b = torch.empty((K, cols), dtype=torch.uint8)
@@ -212,6 +213,66 @@ def test_qlinear_tensor_accumulation_is_exact(K):
         y = qg.mm_qlinear_matmul(*[d[k] for k in keys]).cpu()
     want = torch.tensor([(0, 120, 240)[r % 3] for r in range(256)], dtype=torch.uint8)[:, None].expand(256, 256)
     assert torch.equal(y, want)
+
+
+def _extreme_case(K, types, rows=256, cols=256, seed=0):
+    """Operands at the bottom of the 8-bit range, cancelled by the zero points.
+
+    a = za + u and b = zb + v with u, v in {0, 1}: int8 operands with zero point
+    -128, or uint8 operands with zero point 0.  The true accumulator is
+    sum_k u*v (about 100, at most 255), written exactly to a uint8 output with
+    unit scales.  Moved into [-128, 127] (int8 as is, uint8 minus 128) both
+    operands are u - 128 and v - 128, so products are 16384 - 128(u + v) + u*v
+    and any 1024 of them sum to nearly 2^24: every bit of every partial sum
+    the kernel forms reaches the output.
+    """
+    g = np.random.default_rng(seed)
+    pv = 200.0 / K
+    u = (g.random((rows, K)) < 0.5).astype(np.int16)
+    v = (g.random((K, cols)) < pv).astype(np.int16)
+    want = (u.astype(np.int64) @ v.astype(np.int64))
+    assert want.max() <= 255
+
+    def operand(x, t):
+        zp = -128 if t == torch.int8 else 0
+        np_t = np.int8 if t == torch.int8 else np.uint8
+        return torch.from_numpy((x + zp).astype(np_t)).to(DEV), torch.tensor(zp, dtype=t, device=DEV)
+
+    a, za = operand(u, types[0])
+    b, zb = operand(v, types[1])
+    one = torch.tensor(1.0, device=DEV)
+    d = {"a": a, "a_scale": one, "a_zero_point": za, "b": b, "b_scale": one, "b_zero_point": zb,
+         "y_scale": one, "y_zero_point": torch.tensor(0, dtype=torch.uint8, device=DEV)}
+    return d, torch.from_numpy(want.astype(np.uint8))
+
+
+@pytest.mark.parametrize("types", [(torch.int8, torch.int8), (torch.uint8, torch.uint8),
+                                   (torch.int8, torch.uint8)], ids=["s8s8", "u8u8", "s8u8"])
+@pytest.mark.parametrize("K", [1024, 2048, 4160])
+def test_qlinear_tensor_exact_at_full_range(types, K):
+    d, want = _extreme_case(K, types)
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    with tensor_path():
+        y = qg.mm_qlinear_matmul(*[d[k] for k in keys]).cpu()
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert torch.equal(y, want)
+    _q(d)
+
+
+@pytest.mark.parametrize("ys", [2.0, float(np.nextafter(np.float32(2), np.float32(3))),
+                                float(np.nextafter(np.float32(2), np.float32(1))), 3.0, 0.25, 0.0625],
+                         ids=["tie", "above_tie", "below_tie", "third", "quarter", "sixteenth"])
+def test_qlinear_tensor_rounding_near_half_integers(ys):
+    """Quotients on, or one ulp beside, half-integers: the requantisation must
+    round exactly as the correctly rounded division followed by rint does."""
+    g = np.random.default_rng(7)
+    a = torch.from_numpy(g.integers(-1, 2, (256, 256)).astype(np.int8)).to(DEV)
+    b = torch.from_numpy(g.integers(-1, 2, (256, 256)).astype(np.int8)).to(DEV)
+    z8 = torch.tensor(0, dtype=torch.int8, device=DEV)
+    d = {"a": a, "a_scale": torch.tensor(0.5, device=DEV), "a_zero_point": z8,
+         "b": b, "b_scale": torch.tensor(0.25, device=DEV), "b_zero_point": z8,
+         "y_scale": torch.tensor(ys * 0.125, dtype=torch.float32, device=DEV), "y_zero_point": z8}
+    _q(d)
 
 
 def test_f16_mma_keeps_integer_sums_exact():

@@ -80,13 +80,46 @@ def test_qlinear_s8_sampled_rows_bit_exact():
     assert 0.001 < sat < 0.05      # the workload's y_scale saturates about 1% of outputs
 
 
+@pytest.mark.parametrize("name", sorted(workloads.QLINEAR_VARIANTS))
+def test_qlinear_variants_sampled_rows_bit_exact(name):
+    """uint8 and mixed operands, float16 scales, batch-indexed parameters at full size."""
+    d = workloads.qlinear(device=DEV, **workloads.QLINEAR_VARIANTS[name])
+    keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
+    y = qg.mm_qlinear_matmul(*[d[k] for k in keys])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    h = {k: d[k].cpu().numpy() for k in keys}
+    yh = y.cpu().numpy()
+    batched = h["a"].ndim == 3
+    for bi in range(h["a"].shape[0] if batched else 1):
+        sel = (lambda x: x[bi]) if batched else (lambda x: x)
+        rows = _rows(sel(h["a"]).shape[0], 8, 10 + bi)
+        ref = oracle.qlinear_matmul(sel(h["a"])[rows], sel(h["a_scale"])[rows], sel(h["a_zero_point"])[rows],
+                                    sel(h["b"]), sel(h["b_scale"]), sel(h["b_zero_point"]), h["y_scale"],
+                                    h["y_zero_point"])
+        got = sel(yh)[rows]
+        assert np.array_equal(got, ref), "%d mismatching outputs" % int((got != ref).sum())
+    info = np.iinfo(yh.dtype)
+    sat = float(((yh == info.max) | (yh == info.min)).mean())
+    assert 0.001 < sat < 0.05
+
+
+def test_grouped_f16_int64_indices_sampled():
+    d = workloads.grouped_bf16(device=DEV, dtype=torch.float16, index_dtype=torch.int64)
+    _grouped_check(d, seed=6)
+
+
 def test_grouped_bf16_sampled_tokens_and_columns():
     d = workloads.grouped_bf16(device=DEV)
+    _grouped_check(d, seed=4)
+
+
+def _grouped_check(d, seed):
     out = qg.mm_grouped_matmul(d["input"], d["weights"], d["group_indices"], d["bias"])
     assert qg.mm_last_path() == qg.MM_PATH_TENSOR
     assert qg.mm_get_device_status() == "MM_OK"
-    toks = _rows(16384, 6, 4)
-    cols = np.sort(np.random.default_rng(5).choice(14336, size=512, replace=False))
+    toks = _rows(16384, 6, seed)
+    cols = np.sort(np.random.default_rng(seed + 1).choice(14336, size=512, replace=False))
     gi = d["group_indices"][toks].cpu().numpy()
     used = sorted(set(gi.ravel().tolist()))
     remap = {g: j for j, g in enumerate(used)}

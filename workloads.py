@@ -28,6 +28,10 @@ Workloads (shapes and distributions as specified for the benchmark):
                        group_indices int32 [16384,2]: two distinct groups per
                        token drawn without replacement from a Zipf(s=1.1)
                        popularity p_g ~ (g+1)^-1.1 over G=64.
+
+Variants of 4 and 5 at the same sizes (``QLINEAR_VARIANTS``; ``grouped_bf16``
+with ``dtype`` float16 and int64 indices) cover the other operand types,
+float16 scales and batch-indexed quantisation parameters.
 """
 
 import json
@@ -113,23 +117,59 @@ def qlinear_yscale():
 
 
 def qlinear_s8(device="cpu", seed=0, M=16384, N=4096, K=4096, y_scale=None):
+    return qlinear(device, seed, M, N, K, y_scale=y_scale)
+
+
+def qlinear(device="cpu", seed=0, M=16384, N=4096, K=4096, y_scale=None, a_u8=False, b_u8=False, y_u8=False,
+            scale_dtype=torch.float32, batch=None):
+    """The int8 QLinearMatMul workload and its variants.
+
+    A uint8 operand is the int8 draw plus 128, with its zero points plus 128,
+    so x - zero_point (and with it every accumulator) has the same distribution
+    as in the int8 workload; a uint8 output takes y_zero_point -9 + 128.  With
+    ``scale_dtype`` float16 every scale is rounded to float16.  With ``batch``
+    B, a is [B, M/B, K] (the int8 draw reshaped) with per-row parameters
+    [B, M/B, 1], and b [B, K, N] has per-column parameters [B, 1, N]: each batch
+    index has its own b and its own scales and zero points.
+    """
+    nb = 1 if batch is None else batch
     d = {
         "a": uniform_int((M, K), -128, 127, torch.int8, "cpu", seed),
         "a_scale": uniform((M, 1), 0.003, 0.01, "cpu", seed + 1),
         "a_zero_point": uniform_int((M, 1), -20, 20, torch.int8, "cpu", seed + 2),
-        "b": uniform_int((K, N), -128, 127, torch.int8, "cpu", seed + 3),
-        "b_scale": uniform((1, N), 0.003, 0.01, "cpu", seed + 4),
-        "b_zero_point": uniform_int((1, N), -20, 20, torch.int8, "cpu", seed + 5),
+        "b": uniform_int((nb, K, N), -128, 127, torch.int8, "cpu", seed + 3),
+        "b_scale": uniform((nb, 1, N), 0.003, 0.01, "cpu", seed + 4),
+        "b_zero_point": uniform_int((nb, 1, N), -20, 20, torch.int8, "cpu", seed + 5),
         "y_scale": torch.tensor(qlinear_yscale() if y_scale is None else y_scale, dtype=torch.float32),
         "y_zero_point": torch.tensor(-9, dtype=torch.int8),
     }
-    return {k: v.to(device) for k, v in d.items()}
+    if batch is None:
+        for k in ("b", "b_scale", "b_zero_point"):
+            d[k] = d[k][0]
+    else:
+        for k in ("a", "a_scale", "a_zero_point"):
+            d[k] = d[k].reshape((batch, M // batch) + tuple(d[k].shape[1:]))
+    for k, flag in (("a", a_u8), ("a_zero_point", a_u8), ("b", b_u8), ("b_zero_point", b_u8),
+                    ("y_zero_point", y_u8)):
+        if flag:
+            d[k] = (d[k].to(torch.int16) + 128).to(torch.uint8)
+    for k in ("a_scale", "b_scale", "y_scale"):
+        d[k] = d[k].to(scale_dtype)
+    return {k: v.contiguous().to(device) for k, v in d.items()}
 
 
-def grouped_bf16(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2):
+QLINEAR_VARIANTS = {
+    "qlinear_u8": dict(a_u8=True, b_u8=True, y_u8=True),
+    "qlinear_u8s8_f16scales": dict(a_u8=True, y_u8=False, scale_dtype=torch.float16),
+    "qlinear_s8_batched4": dict(batch=4),
+}
+
+
+def grouped_bf16(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, dtype=torch.bfloat16,
+                 index_dtype=torch.int32):
     return {
-        "input": normal((M, K), device, seed, 1.0, torch.bfloat16),
-        "weights": normal((G, K, N), device, seed + 1, 1.0 / 64, torch.bfloat16),
-        "bias": normal((G, N), device, seed + 2, 0.1, torch.bfloat16),
-        "group_indices": zipf_two_distinct(M, G, S, 1.1, device, seed + 3),
+        "input": normal((M, K), device, seed, 1.0, dtype),
+        "weights": normal((G, K, N), device, seed + 1, 1.0 / 64, dtype),
+        "bias": normal((G, N), device, seed + 2, 0.1, dtype),
+        "group_indices": zipf_two_distinct(M, G, S, 1.1, device, seed + 3, index_dtype),
     }
