@@ -1,7 +1,7 @@
 // tcgen05 tensor-core GEMM for sm_103a (GB300), shared by the MatMul, Gemm,
 // QLinearMatMul and GroupedMatMul fast paths.
 //
-// Structure (one persistent CTA per SM; 576 threads, 320 for QLinear):
+// Structure (one persistent CTA per SM, 576 threads):
 //   warp 0      TMA producer: one thread streams A and B tiles (BK = 64) into a
 //               shared-memory ring, 128-byte swizzled, completing on per-stage
 //               mbarriers (full[s]); it waits on empty[s] before reusing a stage.
@@ -9,9 +9,8 @@
 //               (K=16, fp32 accumulation) into one of two 256-column TMEM
 //               accumulators and commits: empty[s] when a stage has been
 //               consumed, acc_full[b] when an accumulation segment is complete.
-//   warps 2-    epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
-//               owns TMEM lanes 32*(w%4).. and one column slice: 16 warps of 64
-//               columns for the float modes, 8 warps of 128 for QLinear),
+//   warps 2-17  epilogue: wait acc_full[b], tcgen05.ld the accumulator (warp w
+//               owns TMEM lanes 32*(w%4).. and a 64-column slice),
 //               release the buffer (acc_empty[b]) and write the output through
 //               a swizzled shared-memory stage so that every warp store covers
 //               whole 32-byte sectors.
@@ -80,19 +79,19 @@ constexpr int kGroupM = 16;                      // raster band height (tiles), 
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
-constexpr int kQColWords = 3 * 128;              // QLinear per-warp column staging
 constexpr int kStageWords = 32 * 16;             // float per-warp output staging: 32 rows x 64 bytes
 
-// Per-mode shape of the CTA.  The float epilogues (MatMul/Gemm, GroupedMatMul)
-// use 16 warps of 64 columns each, so that a tile's epilogue has enough warps
-// to hide its latency when K is small; QLinearMatMul keeps 8 warps of 128
-// columns, whose int32 running sums need the registers.
+// Shape of the CTA: 16 epilogue warps of 64 columns each, enough warps to hide
+// the epilogue's latency (short-K float products, the QLinear requantisation).
+// With 18 warps ptxas caps a thread at 96 registers (five warps share one SM
+// sub-partition's register file); QLinear keeps its 64 int32 running sums in
+// registers and drains TMEM 16 columns at a time.
 template <int MODE, bool PAIR>
 struct Cfg {
-  static constexpr int kEpiWarps = MODE == kQLinear ? 8 : 16;
+  static constexpr int kEpiWarps = 16;
   static constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
   static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
-  static constexpr int kWarpWords = MODE == kQLinear ? kQColWords : kStageWords;
+  static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : kStageWords;
   static constexpr int kSmem = Geo<PAIR>::kRingBytes + kCtrlBytes + kEpiWarps * kWarpWords * 4 + 1024;
   static_assert(kSmem <= 232448, "shared memory per block");
   static_assert(16 * Geo<PAIR>::kStages + 48 <= kCtrlBytes, "control block");
@@ -126,21 +125,22 @@ template <int MODE, bool PAIR>
 __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti, int& g_hint) {
   if (t >= total) return false;
   if (MODE == kGrouped) {
+    constexpr int TR = Geo<PAIR>::kTileRows;
     int g = g_hint;
     while (g + 1 < p.G && __ldg(p.g_tile_start + g + 1) <= t) ++g;
     g_hint = g;
     const uint32_t local = (uint32_t)(t - __ldg(p.g_tile_start + g));
     const int cnt = __ldg(p.g_count + g);
-    const uint32_t mtg = (uint32_t)((cnt + BM - 1) / BM);
+    const uint32_t mtg = (uint32_t)((cnt + TR - 1) / TR);
     const uint32_t ntile = local / mtg, mtile = local - ntile * mtg;
     ti.batch = 0;
     ti.g = g;
-    ti.m0 = (int64_t)mtile * BM;
+    ti.m0 = (int64_t)mtile * TR;
     ti.n0 = (int64_t)ntile * BN;
-    ti.a_row = __ldg(p.g_offset + g) + (int32_t)(mtile * BM);
+    ti.a_row = __ldg(p.g_offset + g) + (int32_t)(mtile * TR);
     ti.a_b = 0;
     ti.b_b = g;
-    ti.rows = min(BM, cnt - (int)(mtile * BM));
+    ti.rows = min(TR, cnt - (int)(mtile * TR));
     return true;
   }
   const uint32_t tt = (uint32_t)t;
@@ -363,6 +363,28 @@ __device__ __forceinline__ uint32_t requant_byte(int32_t acc, float sa, float sb
   return (uint32_t)(__float_as_int(__fadd_rn(t, kMagic)) - 0x4B400000) & 0xFFu;
 }
 
+// The same byte without a division in the common case.  With rys = RN(1/ys)
+// (ys normal, |ys| < 2^126), qa = RN(v*rys) differs from the correctly rounded
+// quotient qo = RN(v/ys) by less than 2^-21 |qa|: |qa - v/ys| <= ~1.5*2^-23 |qa|
+// and |qo - v/ys| <= 2^-24 |qa|.  So when qa lies more than 2^-20 |qa| from
+// the nearest half-integer, qa and qo lie strictly inside the same interval
+// between half-integers, neither is a tie, and rint(qa) = rint(qo).  When
+// |qa| >= 2^21 the result saturates whatever the rounding.  Otherwise
+// (rarely) *slow is set and the caller recomputes with requant_byte.
+__device__ __forceinline__ uint32_t requant_byte_fast(int32_t acc, float sa, float sb, float rys, bool fast,
+                                                      float yzp, float qmin, float qmax, bool* slow) {
+  constexpr float kMagic = 12582912.0f;
+  const float s = __fmul_rn(sa, sb);
+  const float v = __fmul_rn(__int2float_rn(acc), s);
+  const float qa = __fmul_rn(v, rys);
+  const float r = __fsub_rn(__fadd_rn(qa, kMagic), kMagic);
+  const float half_gap = __fsub_rn(0.5f, fabsf(__fsub_rn(qa, r)));
+  const float aq = fabsf(qa);
+  *slow = !(fast && (aq >= 2097152.0f || half_gap > __fmul_rn(aq, 9.5367431640625e-07f)));
+  const float t = fminf(fmaxf(__fadd_rn(r, yzp), qmin), qmax);
+  return (uint32_t)(__float_as_int(__fadd_rn(t, kMagic)) - 0x4B400000) & 0xFFu;
+}
+
 // ------------------------------------------------------------------ epilogue
 
 template <int MODE, bool PAIR>
@@ -395,9 +417,12 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
   const int nseg = (p.num_kb + p.kb_per_seg - 1) / p.kb_per_seg;
   uint32_t seg = 0;
   Tile ti;
-  float ys = 0.f, yz = 0.f, qmin = 0.f, qmax = 0.f;
+  float ys = 0.f, yz = 0.f, qmin = 0.f, qmax = 0.f, rys = 0.f;
+  bool fast = false;
   if (MODE == kQLinear) {
     ys = load_scale(p.ys, 0, p.ys_f16);
+    rys = __frcp_rn(ys);
+    fast = fabsf(ys) >= 1.17549435e-38f && fabsf(ys) < 8.50705917e+37f;   // 2^-126 <= |ys| < 2^126
     yz = load_q8(p.yz, 0, p.y_signed);
     qmin = p.y_signed ? -128.f : 0.f;
     qmax = p.y_signed ? 127.f : 255.f;
@@ -408,14 +433,14 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
     const bool row_ok = rloc < rows_cta;
     const int64_t ncol0 = ti.n0 + slice * kCols;
     if (MODE == kQLinear) {
-      // Column data of this warp's 128 columns (zero point, column sum, scale),
-      // staged once per tile in a warp-private shared-memory slice.
+      // Column data of this warp's kCols columns (zero point, column sum,
+      // scale), staged once per tile in a warp-private shared-memory slice.
       {
         const int64_t zboff = batch_off(p, p.zb.bstride, ti.batch);
         const int64_t sboff = batch_off(p, p.sb.bstride, ti.batch);
         const int32_t* cs = p.q_cs + (int64_t)ti.b_b * p.N;
         const int bshift = p.b_signed ? 0 : 128;
-        for (int j = lane; j < 128; j += 32) {
+        for (int j = lane; j < kCols; j += 32) {
           const int64_t n = ncol0 + j;
           int32_t zbv = 0, csv = 0;
           float sbv = 0.f;
@@ -425,26 +450,28 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
             sbv = load_scale(p.sb.ptr, sboff + n * p.sb.vs, p.sb_f16);
           }
           qcol[j] = zbv;
-          qcol[128 + j] = csv;
-          qcol[256 + j] = __float_as_int(sbv);
+          qcol[kCols + j] = csv;
+          qcol[2 * kCols + j] = __float_as_int(sbv);
         }
         __syncwarp();
       }
-      int32_t acc[4][32];
+      constexpr int kChunks = kCols / 32;
+      int32_t acc[kChunks][32];
       for (int s = 0; s < nseg; ++s, ++seg) {
         const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
         if (!__all_sync(0xffffffffu, wait_full(buf, aph))) return;
         tc_fence_after();
         const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
+        for (int h = 0; h < 2 * kChunks; ++h) {     // 16 columns at a time: few live registers
+          uint32_t r[16];
+          tmem_ld16(taddr + h * 16, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const int32_t v = __float2int_rn(__uint_as_float(r[j]));   // exact: |v| <= 2^24
-            acc[c][j] = s == 0 ? v : (int32_t)((uint32_t)acc[c][j] + (uint32_t)v);
+            int32_t& a = acc[h >> 1][(h & 1) * 16 + j];
+            a = s == 0 ? v : (int32_t)((uint32_t)a + (uint32_t)v);
           }
         }
         tc_fence_before();
@@ -461,23 +488,33 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         const uint32_t rowterm = rs - (uint32_t)p.K * za;
         uint8_t* yrow = static_cast<uint8_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kChunks; ++c) {
           const int64_t n = ncol0 + c * 32;
           if (n >= p.N) break;
           uint32_t packed[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const int4 zb4 = *reinterpret_cast<const int4*>(qcol + c * 32 + 4 * q);
-            const int4 cs4 = *reinterpret_cast<const int4*>(qcol + 128 + c * 32 + 4 * q);
-            const int4 sb4 = *reinterpret_cast<const int4*>(qcol + 256 + c * 32 + 4 * q);
+            const int4 cs4 = *reinterpret_cast<const int4*>(qcol + kCols + c * 32 + 4 * q);
+            const int4 sb4 = *reinterpret_cast<const int4*>(qcol + 2 * kCols + c * 32 + 4 * q);
             const int32_t zbv[4] = {zb4.x, zb4.y, zb4.z, zb4.w};
             const int32_t csv[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
             const int32_t sbv[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
             uint32_t w = 0;
+            bool any_slow = false;
+            int32_t tot[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint32_t total = (uint32_t)acc[c][4 * q + e] - (uint32_t)zbv[e] * rowterm - za * (uint32_t)csv[e];
-              w |= requant_byte((int32_t)total, sa, __int_as_float(sbv[e]), ys, yz, qmin, qmax) << (8 * e);
+              tot[e] = (int32_t)((uint32_t)acc[c][4 * q + e] - (uint32_t)zbv[e] * rowterm - za * (uint32_t)csv[e]);
+              bool sl;
+              w |= requant_byte_fast(tot[e], sa, __int_as_float(sbv[e]), rys, fast, yz, qmin, qmax, &sl) << (8 * e);
+              any_slow |= sl;
+            }
+            if (any_slow) {   // near a rounding boundary (or an unusual y_scale): divide
+              w = 0;
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w |= requant_byte(tot[e], sa, __int_as_float(sbv[e]), ys, yz, qmin, qmax) << (8 * e);
             }
             packed[q] = w;
           }
@@ -511,7 +548,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       uint16_t* yrow;
       const uint16_t* crow = nullptr;
       if (MODE == kGrouped) {
-        const int64_t orow = row_ok ? p.g_rowlist[ti.a_row + rloc] : 0;
+        const int64_t orow = row_ok ? p.g_rowlist[ti.a_row + row_off + rloc] : 0;
         yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
         if (p.c && row_ok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
       } else {
@@ -772,7 +809,9 @@ int max_pair_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<MODE, true>, &cfg) != cudaSuccess) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<MODE, true>::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<MODE, true>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -850,7 +889,8 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
       return pair ? launch_kernel<kDense, true>(a, b, p, work, stream)
                   : launch_kernel<kDense, false>(a, b, p, work, stream);
     case kGrouped:
-      return launch_kernel<kGrouped, false>(a, b, p, work, stream);
+      return pair ? launch_kernel<kGrouped, true>(a, b, p, work, stream)
+                  : launch_kernel<kGrouped, false>(a, b, p, work, stream);
     case kQLinear:
       return pair ? launch_kernel<kQLinear, true>(a, b, p, work, stream)
                   : launch_kernel<kQLinear, false>(a, b, p, work, stream);
@@ -863,6 +903,12 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
 // is what bounds long-K products; short-K (output-bound) products run better
 // on single CTAs, whose smaller tiles keep more epilogues in flight.
 bool use_pair(int64_t M, int64_t K) { return M > BM && K >= kPairMinK; }
+
+// Grouped products pay for pairs with more padding (each group's last tile is
+// 256 rows instead of 128); they win when groups average at least 256 rows.
+bool use_grouped_pair(int64_t rows, int64_t G, int64_t K) {
+  return K >= kPairMinK && rows >= 2 * BM * G && max_pair_clusters<kGrouped>() > 0;
+}
 
 int sm_count_public() { return sm_count(); }
 

@@ -76,6 +76,7 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
                     cudaStream_t stream);
 // Whether an M x K problem uses CTA pairs.
 bool use_pair(int64_t M, int64_t K);
+bool use_grouped_pair(int64_t rows, int64_t G, int64_t K);
 int sm_count_public();
 
 }  // namespace qg

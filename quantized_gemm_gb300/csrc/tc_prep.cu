@@ -338,7 +338,7 @@ __global__ void route_count_kernel(const void* gi, int ind64, int64_t gi_ms, int
 
 // One block: offset[g] = sum_{h<g} count[h]; tile_start[g] = sum_{h<g} ceil(count[h]/128) * nt.
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, int64_t G, int64_t nt,
-                                                          int32_t* offset, int32_t* tile_start) {
+                                                          int tile_rows, int32_t* offset, int32_t* tile_start) {
   __shared__ int64_t part_rows[1024], part_tiles[1024];
   const int t = threadIdx.x, T = blockDim.x;
   const int64_t per = (G + T - 1) / T;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, 
   int64_t rows = 0, tiles = 0;
   for (int64_t g = lo; g < hi; ++g) {
     rows += count[g];
-    tiles += (count[g] + kTileM - 1) / kTileM * nt;
+    tiles += (count[g] + tile_rows - 1) / tile_rows * nt;
   }
   part_rows[t] = rows;
   part_tiles[t] = tiles;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, 
     offset[g] = (int32_t)rows;
     tile_start[g] = (int32_t)tiles;
     rows += count[g];
-    tiles += (count[g] + kTileM - 1) / kTileM * nt;
+    tiles += (count[g] + tile_rows - 1) / tile_rows * nt;
   }
   if (hi == G && lo < hi) {
     offset[G] = (int32_t)rows;
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(128) route_scatter_kernel(const GroupedArgs g,
   }
 }
 
-bool plan_grouped_b(const GroupedArgs& g, OperandPlan* b) {
+bool plan_grouped_b(const GroupedArgs& g, bool pair, OperandPlan* b) {
   BatchMap bm;
   memset(&bm, 0, sizeof(bm));
   bm.nb = 1;
@@ -423,7 +423,7 @@ bool plan_grouped_b(const GroupedArgs& g, OperandPlan* b) {
   bm.count = g.G;
   for (int d = 1; d < kMaxBatchDims; ++d) bm.shape[d] = 1;
   int64_t bs[kMaxBatchDims] = {g.w_gs, 0, 0, 0, 0, 0};
-  if (!plan_operand(g.w, g.dtype, g.N, g.K, g.w_ns, g.w_ks, bm, bs, kTileN, b)) return false;
+  if (!plan_operand(g.w, g.dtype, g.N, g.K, g.w_ns, g.w_ks, bm, bs, pair ? kTileN / 2 : kTileN, b)) return false;
   // Tile coordinates address weights[g] directly as batch coordinate g.
   return g.G <= 1 || b->bc[0] == 1;
 }
@@ -442,12 +442,15 @@ bool tc_grouped_supported(const GroupedArgs& g) {
   const int64_t nt = (g.N + kTileN - 1) / kTileN;
   if ((g.M * g.S / kTileM + g.G + 1) * nt > 0x7fffffffLL) return false;
   OperandPlan b;
-  return plan_grouped_b(g, &b);
+  return plan_grouped_b(g, false, &b);
 }
 
 mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cudaStream_t stream) {
   OperandPlan a, b;
-  if (!ws || !status || !plan_grouped_b(g, &b)) return MM_ERR_UNSUPPORTED;
+  // CTA pairs (256-row tiles) when groups are large enough; the routing scan
+  // counts tiles of the same height.
+  const bool pair = use_grouped_pair(g.M * g.S, g.G, g.K);
+  if (!ws || !status || !plan_grouped_b(g, pair, &b)) return MM_ERR_UNSUPPORTED;
   const GLayout l = glayout(g.M, g.S, g.G, g.K, 2);
   char* base = static_cast<char*>(ws);
   int32_t* count = reinterpret_cast<int32_t*>(base + l.off_count);
@@ -471,7 +474,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   const int64_t cb = (rows + 255) / 256;
   route_count_kernel<<<(unsigned)(cb < 4096 ? cb : 4096), 256, 0, stream>>>(g.gi, g.ind64, g.gi_ms, g.gi_ss, g.M,
                                                                           g.S, g.G, count, status);
-  route_scan_kernel<<<1, 1024, 0, stream>>>(count, g.G, nt, offset, tile_start);
+  route_scan_kernel<<<1, 1024, 0, stream>>>(count, g.G, nt, pair ? 2 * kTileM : kTileM, offset, tile_start);
   const unsigned sgrid = (unsigned)(rows < 65536 ? rows : 65536);
   if (g.dtype == MM_BF16)
     route_scatter_kernel<__nv_bfloat16><<<sgrid, 128, 0, stream>>>(g, offset, cursor, rowlist,
@@ -485,7 +488,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   init_params(&p);
   p.M = rows; p.N = g.N; p.K = g.K;
   p.nt = nt;
-  p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major, false);
+  p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major, pair);
   p.out_f16 = g.dtype == MM_F16;
   p.y = g.out;
   p.y_rs = g.N;
@@ -500,8 +503,8 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.g_count = count; p.g_offset = offset; p.g_tile_start = tile_start; p.g_rowlist = rowlist;
   p.G = (int)g.G;
   p.status = status;
-  // The tile count is known only on the device: one persistent CTA per SM.
-  return launch_tc(kGrouped, false, a, b, p, stream);
+  // The tile count is known only on the device: one persistent CTA (pair) per SM (pair).
+  return launch_tc(kGrouped, pair, a, b, p, stream);
 }
 
 }  // namespace qg
