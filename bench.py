@@ -298,6 +298,8 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     out["grouped_bf16"] = bench_grouped(workloads.grouped_bf16(device=dev), world, stream, bf16_peak)
     out["grouped_f16_i64"] = bench_grouped(
         workloads.grouped_bf16(device=dev, dtype=torch.float16, index_dtype=torch.int64), world, stream, bf16_peak)
+    # The same sizes with 8 groups (4096 rows each on average): CTA-pair tiles.
+    out["grouped_bf16_g8"] = bench_grouped(workloads.grouped_bf16(device=dev, G=8), world, stream, bf16_peak)
     return out
 
 

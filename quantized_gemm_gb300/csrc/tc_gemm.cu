@@ -828,30 +828,32 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const TcPara
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MM_ERR_CUDA;
-  if (!PAIR) {
+  if constexpr (!PAIR) {
     const int sms = sm_count();
     const int grid = (int)(work < sms ? (work > 0 ? work : 1) : sms);
     tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, p);
     return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+  } else {
+    // One persistent pair per resident cluster slot: a pair that could not be
+    // resident would only start after the others finish.
+    const int slots = max_pair_clusters<MODE>();
+    if (slots <= 0) return MM_ERR_UNSUPPORTED;
+    const int clusters = (int)(work < slots ? (work > 0 ? work : 1) : slots);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3(kThreadsM);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, p) == cudaSuccess ? MM_OK
+                                                                                               : MM_ERR_CUDA;
   }
-  // One persistent pair per resident cluster slot: a pair that could not be
-  // resident would only start after the others finish.
-  const int slots = max_pair_clusters<MODE>();
-  if (slots <= 0) return MM_ERR_UNSUPPORTED;
-  const int clusters = (int)(work < slots ? (work > 0 ? work : 1) : slots);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(2 * clusters));
-  cfg.blockDim = dim3(kThreadsM);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, p) == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
 }  // namespace
@@ -891,9 +893,8 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
     case kGrouped:
       return pair ? launch_kernel<kGrouped, true>(a, b, p, work, stream)
                   : launch_kernel<kGrouped, false>(a, b, p, work, stream);
-    case kQLinear:
-      return pair ? launch_kernel<kQLinear, true>(a, b, p, work, stream)
-                  : launch_kernel<kQLinear, false>(a, b, p, work, stream);
+    case kQLinear:   // single CTAs only: the product is bound by its epilogue
+      return pair ? MM_ERR_UNSUPPORTED : launch_kernel<kQLinear, false>(a, b, p, work, stream);
     default:
       return MM_ERR_UNSUPPORTED;
   }
@@ -905,9 +906,11 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
 bool use_pair(int64_t M, int64_t K) { return M > BM && K >= kPairMinK; }
 
 // Grouped products pay for pairs with more padding (each group's last tile is
-// 256 rows instead of 128); they win when groups average at least 256 rows.
+// 256 rows instead of 128).  Measured on 16384 x 2 routed rows, K = 4096,
+// N = 14336: pairs are 5% faster with 8 groups (4096 rows each on average)
+// and 1.5% slower with 64 groups (512 rows), so they need 1024 rows a group.
 bool use_grouped_pair(int64_t rows, int64_t G, int64_t K) {
-  return K >= kPairMinK && rows >= 2 * BM * G && max_pair_clusters<kGrouped>() > 0;
+  return K >= kPairMinK && rows >= 8 * BM * G && max_pair_clusters<kGrouped>() > 0;
 }
 
 int sm_count_public() { return sm_count(); }

@@ -332,14 +332,14 @@ def test_grouped_tensor(dtype, ind, with_bias):
 @pytest.mark.parametrize("dtype", HALF, ids=str)
 @pytest.mark.parametrize("with_bias", [False, True])
 def test_grouped_tensor_cta_pairs(dtype, with_bias):
-    # K >= 1024 and groups of 366 rows on average: the planner runs 256-row
-    # CTA-pair tiles.  Group sizes are not multiples of 256 (two are below
-    # 128, one is empty), K = 1096 leaves a partial k-block, N = 520 a
-    # partial column tile.
-    M, K, N, G, S = 1100, 1096, 520, 6, 2
+    # K >= 1024 and groups of 1100 rows on average: the planner runs 256-row
+    # CTA-pair tiles.  Group sizes are not multiples of 256 (one is below 128,
+    # one is empty), K = 1096 leaves a partial k-block, N = 520 a partial
+    # column tile.
+    M, K, N, G, S = 2200, 1096, 520, 4, 2
     x = rand_tensor((M, K), dtype, 31, DEV)
     w = rand_tensor((G, K, N), dtype, 32, DEV)
-    p = np.array([0.45, 0.25, 0.0, 0.2, 0.05, 0.05])
+    p = np.array([0.63, 0.345, 0.0, 0.025])
     gi = torch.from_numpy(np.random.default_rng(33).choice(G, size=(M, S), p=p)).to(torch.int32).to(DEV)
     bias = rand_tensor((G, N), dtype, 34, DEV) if with_bias else None
     _grouped(x, w, gi, bias)
@@ -347,7 +347,7 @@ def test_grouped_tensor_cta_pairs(dtype, with_bias):
 
 
 def test_grouped_tensor_cta_pairs_invalid_indices():
-    M, K, N, G = 1100, 1024, 256, 4
+    M, K, N, G = 2200, 1024, 256, 2
     x = rand_tensor((M, K), torch.bfloat16, 35, DEV)
     w = rand_tensor((G, K, N), torch.bfloat16, 36, DEV)
     gi = torch.from_numpy(np.random.default_rng(37).integers(-1, G + 1, size=(M, 2))).to(torch.int64).to(DEV)

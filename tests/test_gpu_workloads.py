@@ -109,6 +109,12 @@ def test_grouped_f16_int64_indices_sampled():
     _grouped_check(d, seed=6)
 
 
+def test_grouped_bf16_8_groups_sampled():
+    """Eight groups of 4096 routed rows on average: the CTA-pair tiles."""
+    d = workloads.grouped_bf16(device=DEV, G=8)
+    _grouped_check(d, seed=8)
+
+
 def test_grouped_bf16_sampled_tokens_and_columns():
     d = workloads.grouped_bf16(device=DEV)
     _grouped_check(d, seed=4)
