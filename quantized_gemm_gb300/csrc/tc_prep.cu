@@ -60,34 +60,44 @@ __device__ __forceinline__ int64_t own_offset(const ShiftArgs& p, int64_t mat) {
   return off;
 }
 
-// 16 shifted values of a row starting at column c0 (zeros beyond `cols`).
-__device__ __forceinline__ void load16_shifted(const ShiftArgs& p, const uint8_t* srow, int64_t c0, int (&x)[16]) {
-  const int shift = p.is_signed ? 0 : 128;
-  if (p.src_cs == 1 && c0 + 16 <= p.cols && ((reinterpret_cast<uintptr_t>(srow + c0) & 15) == 0)) {
-    const uint4 u = *reinterpret_cast<const uint4*>(srow + c0);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// Loads are issued kBatch at a time before any is used: the f16 stores could
+// alias the uint8 source as far as the compiler knows, so without this each
+// 16-byte load would wait for the previous chunk's store (one DRAM round trip
+// per chunk).
+constexpr int kBatch = 4;
+
+// Whether the 16 bytes of a row at column c0 can be read as one aligned vector.
+__device__ __forceinline__ bool vec16_ok(const ShiftArgs& p, const uint8_t* srow, int64_t c0) {
+  return p.src_cs == 1 && c0 + 16 <= p.cols && ((reinterpret_cast<uintptr_t>(srow + c0) & 15) == 0);
+}
+
+// x = the 16 bytes of u moved into [-128, 127] (int8 as is, uint8 minus 128).
+__device__ __forceinline__ void decode16(const uint4& u, int is_signed, int (&x)[16]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < 4; ++q)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t b = (w[q] >> (8 * e)) & 0xFFu;
-        x[4 * q + e] = p.is_signed ? (int)(int8_t)b : (int)b - shift;
-      }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      int v = 0;
-      if (c0 + e < p.cols) {
-        const uint8_t b = srow[(c0 + e) * p.src_cs];
-        v = p.is_signed ? (int)(int8_t)b : (int)b - shift;
-      }
-      x[e] = v;
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t b = (w[q] >> (8 * e)) & 0xFFu;
+      x[4 * q + e] = is_signed ? (int)(int8_t)b : (int)b - 128;
     }
+}
+
+// The same for a piece that is not a full aligned vector (zeros beyond `cols`).
+__device__ __forceinline__ void load16_scalar(const ShiftArgs& p, const uint8_t* srow, int64_t c0, int (&x)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    int v = 0;
+    if (c0 + e < p.cols) {
+      const uint8_t b = __ldg(srow + (c0 + e) * p.src_cs);
+      v = p.is_signed ? (int)(int8_t)b : (int)b - 128;
+    }
+    x[e] = v;
   }
 }
 
-// Stores 16 f16 values at dst (16-byte aligned); the elements at or beyond
-// `valid` are stored only if they fall inside the padded row (ld).
+// Stores 16 f16 values at dst (16-byte aligned); the second half only if it
+// starts inside the padded row (ld).
 __device__ __forceinline__ void store16_f16(__half* dst, const int (&x)[16], int64_t c0, int64_t ld) {
   uint32_t w[8];
 #pragma unroll
@@ -110,12 +120,24 @@ __global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
     const uint8_t* srow = p.src + own_offset(p, mat) + r * p.src_rs;
     __half* drow = p.dst + wr * p.ld;
     uint32_t sum = 0;   // modulo 2^32, like every term of the int32 accumulator
-    for (int64_t c0 = (int64_t)lane * 16; c0 < p.cols; c0 += 512) {
-      int x[16];
-      load16_shifted(p, srow, c0, x);
+    for (int64_t cb = (int64_t)lane * 16; cb < p.cols; cb += 512 * kBatch) {
+      uint4 raw[kBatch];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) sum += (uint32_t)x[e];
-      store16_f16(drow + c0, x, c0, p.ld);
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t c0 = cb + 512 * u;
+        raw[u] = vec16_ok(p, srow, c0) ? __ldg(reinterpret_cast<const uint4*>(srow + c0)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t c0 = cb + 512 * u;
+        if (c0 >= p.cols) break;
+        int x[16];
+        if (vec16_ok(p, srow, c0)) decode16(raw[u], p.is_signed, x);
+        else load16_scalar(p, srow, c0, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sum += (uint32_t)x[e];
+        store16_f16(drow + c0, x, c0, p.ld);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -128,7 +150,7 @@ __global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
 // partial column sums are combined in shared memory, and one atomic add per
 // column and block accumulates the band into the column sums (which start at
 // zero).  Consecutive threads read consecutive 16-byte pieces of a row.
-constexpr int kColRows = 512;
+constexpr int kColRows = 128;
 constexpr int kColGroups = 16;                   // 16-column groups per block
 constexpr int kRowLanes = 16;
 
@@ -151,12 +173,27 @@ __global__ void __launch_bounds__(kColGroups * kRowLanes) shift_cols_kernel(cons
     if (cg < cgroups) {
       const uint8_t* base = p.src + own_offset(p, mat);
       const int64_t r1 = min(p.rows, (rb + 1) * kColRows);
-      for (int64_t r = rb * kColRows + lane_r; r < r1; r += kRowLanes) {
-        int x[16];
-        load16_shifted(p, base + r * p.src_rs, c0, x);
+      for (int64_t rbase = rb * kColRows + lane_r; rbase < r1; rbase += kRowLanes * kBatch) {
+        uint4 raw[kBatch];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) part[e] += (uint32_t)x[e];
-        store16_f16(p.dst + (mat * p.rows + r) * p.ld + c0, x, c0, p.ld);
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t r = rbase + kRowLanes * u;
+          const uint8_t* srow = base + r * p.src_rs;
+          raw[u] = (r < r1 && vec16_ok(p, srow, c0)) ? __ldg(reinterpret_cast<const uint4*>(srow + c0))
+                                                     : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t r = rbase + kRowLanes * u;
+          if (r >= r1) break;
+          const uint8_t* srow = base + r * p.src_rs;
+          int x[16];
+          if (vec16_ok(p, srow, c0)) decode16(raw[u], p.is_signed, x);
+          else load16_scalar(p, srow, c0, x);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) part[e] += (uint32_t)x[e];
+          store16_f16(p.dst + (mat * p.rows + r) * p.ld + c0, x, c0, p.ld);
+        }
       }
     }
     __syncthreads();
