@@ -23,6 +23,8 @@ Each module cites the page and section it follows:
 * ``gemm``            -- Gemm (onnx-light, ai.onnx since version 13)
 * ``qlinear_matmul``  -- QLinearMatMul - version 10 (onnx-light)
 * ``grouped_matmul``  -- GroupedMatMul - 29 (onnx.ai)
+* ``dequantize_linear`` -- GroupedMatMul - 29, Summary: weight-only quantized
+  experts (DequantizeLinear of the weights, then GroupedMatMul)
 
 Parity status: every function here is pinned by tests in
 ``tests/test_oracle_pins.py`` (printed worked examples, brute force on tiny
@@ -34,10 +36,13 @@ from .matmul import matmul, matmul_output_shape, matmul_abs_scale
 from .gemm import gemm, gemm_output_shape, gemm_abs_scale
 from .qlinear_matmul import qlinear_matmul, requantize
 from .grouped_matmul import grouped_matmul, grouped_abs_scale
+from .dequantize_linear import (dequantize_linear, grouped_matmul_qweights, grouped_qweights_abs_scale,
+                                round_to, round_to_bf16)
 
 __all__ = [
     "matmul", "matmul_output_shape", "matmul_abs_scale",
     "gemm", "gemm_output_shape", "gemm_abs_scale",
     "qlinear_matmul", "requantize",
     "grouped_matmul", "grouped_abs_scale",
+    "dequantize_linear", "grouped_matmul_qweights", "grouped_qweights_abs_scale", "round_to", "round_to_bf16",
 ]

@@ -495,3 +495,103 @@ def test_grouped_brute_force():
                 for k in range(K):
                     s += float(x[m, k]) * float(w[g, k, n])
                 assert got[m, i, n] == s
+
+
+# ------------------------------------------------------------------ weight-only quantized experts
+# ("GroupedMatMul - 29", Summary: DequantizeLinear of the weights, then GroupedMatMul)
+
+def test_dequantize_worked_values():
+    # (q - zp) * scale by hand: (-128 - 3) * 0.5 = -65.5, (127 + 1) * 1.5 = 192,
+    # (5 - 3) * 0.5 = 1, (-5 + 1) * 1.5 = -6; all exact in bfloat16.
+    q = np.array([[[-128, 127], [5, -5]]], dtype=np.int8)
+    zp = np.array([[[3, -1]]], dtype=np.int8)
+    scale = np.array([[[0.5, 1.5]]])
+    got = oracle.dequantize_linear(q, scale, zp, None, "bf16")
+    assert got.tolist() == [[[-65.5, 192.0], [1.0, -6.0]]]
+    # uint8 with the default zero point 0
+    qu = np.array([[[0, 255]]], dtype=np.uint8)
+    assert oracle.dequantize_linear(qu, np.array([[[2.0, 0.25]]]), None, 1, "f16").tolist() == [[[0.0, 63.75]]]
+
+
+def test_dequantize_rounds_once_to_the_scale_type():
+    # 255 * 1.5 = 382.5: bfloat16 spacing is 2 in [256, 512), so 382; exact in float16.
+    q = np.array([[[127]]], dtype=np.int8)
+    zp = np.array([[[-128]]], dtype=np.int8)
+    s = np.array([[[1.5]]])
+    assert oracle.dequantize_linear(q, s, zp, None, "bf16").item() == 382.0
+    assert oracle.dequantize_linear(q, s, zp, None, "f16").item() == 382.5
+    # ties go to the even neighbour: 174 * 1.5 = 261 -> 260, 178 * 1.5 = 267 -> 268
+    for diff, want in ((174, 260.0), (178, 268.0), (-174, -260.0)):
+        qq = np.array([[[diff - 128 if diff > 0 else diff + 127]]], dtype=np.int8)
+        zz = np.array([[[-128 if diff > 0 else 127]]], dtype=np.int8)
+        assert oracle.dequantize_linear(qq, s, zz, None, "bf16").item() == want
+
+
+def test_bf16_rounding_matches_torch_conversion():
+    # The bfloat16 rounding written out in the oracle against torch's float32 ->
+    # bfloat16 conversion (round to nearest even), over every (q - zp) in
+    # [-255, 255] and a set of bfloat16 scales.
+    torch = pytest.importorskip("torch")
+    diffs = np.arange(-255, 256, dtype=np.float64)
+    scales = torch.tensor(np.random.default_rng(40).uniform(-3, 3, 64), dtype=torch.float32).to(torch.bfloat16)
+    scales = scales.double().numpy()
+    prod = np.multiply.outer(diffs, scales)            # exact in float32 (<= 17 significant bits)
+    ours = oracle.round_to_bf16(prod)
+    ref = torch.from_numpy(prod.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_dequantize_blocks_brute_force():
+    rng = np.random.default_rng(41)
+    G, K, N, block = 2, 7, 3, 3                        # Kb = 3, last block partial
+    q = rng.integers(-128, 128, size=(G, K, N)).astype(np.int8)
+    zp = rng.integers(-20, 21, size=(G, 3, N)).astype(np.int8)
+    scale = rng.integers(1, 9, size=(G, 3, N)) / 8.0   # exact, products exact in every type
+    got = oracle.dequantize_linear(q, scale, zp, block, "f32")
+    for g in range(G):
+        for k in range(K):
+            for n in range(N):
+                b = k // block
+                assert got[g, k, n] == (int(q[g, k, n]) - int(zp[g, b, n])) * float(scale[g, b, n])
+
+
+def test_grouped_qweights_reduces_to_grouped_matmul():
+    # block = K, unit scales and zero points 0: the weights are the integers themselves.
+    rng = np.random.default_rng(42)
+    M, K, N, G, S = 6, 5, 4, 3, 2
+    x = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    q = rng.integers(-128, 128, size=(G, K, N)).astype(np.int8)
+    gi = rng.integers(0, G, size=(M, S)).astype(np.int32)
+    bias = rng.integers(-4, 5, size=(G, N)).astype(np.float32)
+    got = oracle.grouped_matmul_qweights(x, q, np.ones((G, 1, N)), None, K, gi, bias, "bf16")
+    assert np.array_equal(got, oracle.grouped_matmul(x, q.astype(np.float32), gi, bias))
+    # a per-column scale of 2**-3 scales every output of that column (bias excluded)
+    s = np.ones((G, 1, N))
+    s[:, :, 1] = 0.125
+    got2 = oracle.grouped_matmul_qweights(x, q, s, None, K, gi, None, "bf16")
+    ref2 = oracle.grouped_matmul(x, q.astype(np.float32), gi, None)
+    assert np.array_equal(got2[:, :, 1], ref2[:, :, 1] * 0.125)
+    assert np.array_equal(got2[:, :, 0], ref2[:, :, 0])
+
+
+def test_grouped_qweights_uses_each_groups_parameters():
+    # two groups with the same quantized weights but different zero points:
+    # outputs differ by (zp1 - zp0) * scale * sum(x) for every column
+    x = np.array([[1.0, 2.0, 3.0]])
+    q = np.zeros((2, 3, 2), dtype=np.int8)
+    zp = np.array([[[1, 1]], [[4, 4]]], dtype=np.int8)
+    s = np.full((2, 1, 2), 0.5)
+    gi = np.array([[0, 1]], dtype=np.int64)
+    out = oracle.grouped_matmul_qweights(x, q, s, zp, None, gi, None, "f16")
+    assert out[0, 0].tolist() == [-3.0, -3.0]          # (0 - 1) * 0.5 * 6
+    assert out[0, 1].tolist() == [-12.0, -12.0]        # (0 - 4) * 0.5 * 6
+
+
+def test_dequantize_rejects_bad_shapes():
+    q = np.zeros((1, 4, 2), dtype=np.int8)
+    with pytest.raises(ValueError):
+        oracle.dequantize_linear(q, np.ones((1, 1, 2)), None, 2, "bf16")      # needs [1, 2, 2]
+    with pytest.raises(TypeError):
+        oracle.dequantize_linear(q, np.ones((1, 1, 2)), np.zeros((1, 1, 2), dtype=np.uint8), None, "bf16")
+    with pytest.raises(TypeError):
+        oracle.dequantize_linear(q.astype(np.int16), np.ones((1, 1, 2)), None, None, "bf16")
