@@ -175,6 +175,40 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights,
                             const mm_tensor* output, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* ---------------------------------------------------------------- GroupedMatMul, weight-only quantized experts
+ * GroupedMatMul - 29 (onnx.ai operator page), Summary, last paragraph: experts
+ * whose weights are stored quantized are expressed as DequantizeLinear of the
+ * weights followed by GroupedMatMul, and a runtime may fuse the two so that
+ * the dequantized [G, K, N] weights are never formed.  This entry point is
+ * that fusion:
+ *   W[g,k,n] = T((weights_q[g,k,n] - w_zero_point[g,k/B,n]) * w_scale[g,k/B,n])
+ *   output[m,i,:] = input[m,:] @ W[g,:,:] (+ bias[g,:]),  g = group_indices[m,i],
+ * with B = block_size (0 means K: one scale per group and output column).
+ * The pages name DequantizeLinear without defining it; this is the reading
+ * used: the difference is an exact integer and the product is rounded once to
+ * T (nearest, ties to even), so W is exactly what a separate dequantization to
+ * T would store; the product with W then accumulates as in mm_grouped_matmul.
+ *   input [M,K] (T = bf16, f16, f32 or f64); weights_q [G,K,N] MM_I8 or MM_U8;
+ *   w_scale [G, ceil(K/B), N] of type T; w_zero_point NULL (zero) or of the
+ *   type of weights_q and the shape of w_scale; group_indices [M,S] MM_I32 or
+ *   MM_I64; bias NULL or [G,N] of type T; output dense [M,S,N] of type T.
+ *   block_size < 0 returns MM_ERR_INVALID_ARG.  Invalid group indices as for
+ *   mm_grouped_matmul (zero rows, MM_ERR_INDEX_RANGE in the device status).
+ * The tensor-core path (bf16/f16; weights, scales and zero points with a
+ * unit-stride N dimension and 16-byte aligned rows; B a multiple of 64 or
+ * B >= K) keeps the weights int8 in memory: each k-block is loaded as int8
+ * and converted in shared memory just before the tensor cores read it.
+ * Workspace: mm_grouped_matmul_qweights_workspace_size() bytes. */
+mm_status mm_grouped_matmul_qweights_workspace_size(const mm_tensor* input, const mm_tensor* weights_q,
+                                                    const mm_tensor* w_scale, const mm_tensor* w_zero_point,
+                                                    int64_t block_size, const mm_tensor* group_indices,
+                                                    size_t* bytes);
+mm_status mm_grouped_matmul_qweights(const mm_tensor* input, const mm_tensor* weights_q, const mm_tensor* w_scale,
+                                     const mm_tensor* w_zero_point /* NULL = 0 */, int64_t block_size,
+                                     const mm_tensor* group_indices, const mm_tensor* bias /* NULL = absent */,
+                                     const mm_tensor* output, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* ---------------------------------------------------------------- GroupedMatMul without allocation
  * This entry point has no counterpart in the operator pages; it exists for
  * callers that cannot allocate device memory at call time: code whose device

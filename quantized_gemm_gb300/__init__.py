@@ -19,6 +19,7 @@ __all__ = [
     "mm_get_device_status", "mm_set_path_policy", "mm_last_path", "mm_set_wait_limit_ns", "mm_version",
     "library_path",
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
+    "mm_grouped_matmul_qweights", "mm_grouped_matmul_qweights_workspace_size",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
 ]
 
@@ -80,6 +81,8 @@ def _lib():
             "mm_grouped_matmul_noalloc_max_scratch": ([], SZ),
             "mm_set_wait_limit_ns": ([ctypes.c_uint64], I32),
             "mm_grouped_matmul_noalloc": ([T, T, T, T, T, P], I32),
+            "mm_grouped_matmul_qweights_workspace_size": ([T, T, T, T, I64, T, ctypes.POINTER(SZ)], I32),
+            "mm_grouped_matmul_qweights": ([T, T, T, T, I64, T, T, T, P, SZ, P], I32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -225,6 +228,33 @@ def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream
     _check(lib.mm_grouped_matmul(_ref(dx), _ref(dw), _ref(dg), _ref(_desc(bias)), _ref(_desc(y)),
                                  None if ws is None else ws.data_ptr(), wsb, _stream(input, stream)),
            "mm_grouped_matmul")
+    return y
+
+
+def mm_grouped_matmul_qweights_workspace_size(input, weights_q, w_scale, w_zero_point, block_size, group_indices):
+    nbytes = ctypes.c_size_t()
+    _check(_lib().mm_grouped_matmul_qweights_workspace_size(
+        _ref(_desc(input)), _ref(_desc(weights_q)), _ref(_desc(w_scale)), _ref(_desc(w_zero_point)),
+        int(block_size), _ref(_desc(group_indices)), ctypes.byref(nbytes)), "mm_grouped_matmul_qweights_workspace_size")
+    return nbytes.value
+
+
+def mm_grouped_matmul_qweights(input, weights_q, w_scale, w_zero_point, block_size, group_indices, bias=None,
+                               out=None, stream=None, workspace=None):
+    """GroupedMatMul of int8/uint8 experts: input[m] @ W[g] (+ bias[g]) with
+    W = DequantizeLinear(weights_q, w_scale, w_zero_point) in blocks of
+    ``block_size`` rows of K (0: one scale per group and column), fused."""
+    lib = _lib()
+    M, S, N = input.shape[0], group_indices.shape[1], weights_q.shape[2]
+    y = torch.empty((M, S, N), dtype=input.dtype, device=input.device) if out is None else out
+    ws, wsb = _workspace(mm_grouped_matmul_qweights_workspace_size(input, weights_q, w_scale, w_zero_point,
+                                                                   block_size, group_indices),
+                         input.device, workspace)
+    _check(lib.mm_grouped_matmul_qweights(_ref(_desc(input)), _ref(_desc(weights_q)), _ref(_desc(w_scale)),
+                                          _ref(_desc(w_zero_point)), int(block_size), _ref(_desc(group_indices)),
+                                          _ref(_desc(bias)), _ref(_desc(y)), None if ws is None else ws.data_ptr(),
+                                          wsb, _stream(input, stream)),
+           "mm_grouped_matmul_qweights")
     return y
 
 

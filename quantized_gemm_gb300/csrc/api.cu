@@ -496,6 +496,101 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights, co
   return finish(launch_simt_grouped(g, status, st), MM_PATH_SIMT);
 }
 
+// ------------------------------------------------------------------ GroupedMatMul, weight-only quantized experts
+
+namespace {
+
+mm_status plan_grouped_q(const mm_tensor* input, const mm_tensor* weights_q, const mm_tensor* w_scale,
+                         const mm_tensor* w_zero_point, int64_t block_size, const mm_tensor* gi,
+                         const mm_tensor* bias, GroupedArgs* g) {
+  mm_status s;
+  if ((s = check_tensor(input)) != MM_OK || (s = check_tensor(weights_q)) != MM_OK ||
+      (s = check_tensor(w_scale)) != MM_OK || (s = check_tensor(gi)) != MM_OK)
+    return s;
+  if (w_zero_point && (s = check_tensor(w_zero_point)) != MM_OK) return s;
+  if (bias && (s = check_tensor(bias)) != MM_OK) return s;
+  if (block_size < 0) return MM_ERR_INVALID_ARG;
+  const int dt = input->dtype;
+  if (dt != MM_BF16 && dt != MM_F16 && dt != MM_F32 && dt != MM_F64) return MM_ERR_DTYPE;
+  if (weights_q->dtype != MM_I8 && weights_q->dtype != MM_U8) return MM_ERR_DTYPE;
+  if (w_scale->dtype != dt || (bias && bias->dtype != dt)) return MM_ERR_DTYPE;
+  if (w_zero_point && w_zero_point->dtype != weights_q->dtype) return MM_ERR_DTYPE;
+  if (gi->dtype != MM_I32 && gi->dtype != MM_I64) return MM_ERR_DTYPE;
+  if (input->ndim != 2 || weights_q->ndim != 3 || gi->ndim != 2 || w_scale->ndim != 3) return MM_ERR_SHAPE;
+  const int64_t G = weights_q->shape[0], K = weights_q->shape[1], N = weights_q->shape[2];
+  if (K != input->shape[1] || gi->shape[0] != input->shape[0]) return MM_ERR_SHAPE;
+  const int64_t block = block_size == 0 ? (K > 0 ? K : 1) : block_size;
+  const int64_t kb = (K + block - 1) / block;
+  if (w_scale->shape[0] != G || w_scale->shape[1] != kb || w_scale->shape[2] != N) return MM_ERR_SHAPE;
+  if (w_zero_point) {
+    if (w_zero_point->ndim != 3) return MM_ERR_SHAPE;
+    for (int d = 0; d < 3; ++d)
+      if (w_zero_point->shape[d] != w_scale->shape[d]) return MM_ERR_SHAPE;
+  }
+  if (bias && (bias->ndim != 2 || bias->shape[0] != G || bias->shape[1] != N)) return MM_ERR_SHAPE;
+  memset(g, 0, sizeof(*g));
+  g->dtype = dt;
+  g->ind64 = gi->dtype == MM_I64;
+  g->M = input->shape[0]; g->K = K; g->G = G; g->N = N; g->S = gi->shape[1];
+  g->x = input->data; g->x_rs = input->strides[0]; g->x_cs = input->strides[1];
+  g->w = weights_q->data;
+  g->w_gs = weights_q->strides[0]; g->w_ks = weights_q->strides[1]; g->w_ns = weights_q->strides[2];
+  g->gi = gi->data; g->gi_ms = gi->strides[0]; g->gi_ss = gi->strides[1];
+  if (bias) { g->bias = bias->data; g->bias_gs = bias->strides[0]; g->bias_ns = bias->strides[1]; }
+  g->wq = weights_q->dtype == MM_I8 ? 1 : 2;
+  g->wsc = w_scale->data;
+  g->wsc_gs = w_scale->strides[0]; g->wsc_bs = w_scale->strides[1]; g->wsc_ns = w_scale->strides[2];
+  if (w_zero_point) {
+    g->wzp = w_zero_point->data;
+    g->wzp_gs = w_zero_point->strides[0]; g->wzp_bs = w_zero_point->strides[1]; g->wzp_ns = w_zero_point->strides[2];
+  }
+  g->qblock = block;
+  return MM_OK;
+}
+
+}  // namespace
+
+mm_status mm_grouped_matmul_qweights_workspace_size(const mm_tensor* input, const mm_tensor* weights_q,
+                                                    const mm_tensor* w_scale, const mm_tensor* w_zero_point,
+                                                    int64_t block_size, const mm_tensor* group_indices,
+                                                    size_t* bytes) {
+  if (!bytes) return MM_ERR_INVALID_ARG;
+  GroupedArgs g;
+  mm_status s = plan_grouped_q(input, weights_q, w_scale, w_zero_point, block_size, group_indices, nullptr, &g);
+  if (s != MM_OK) return s;
+  const int pol = g_policy.load();
+  const bool want_tc = pol != MM_PATH_SIMT &&
+                       (pol == MM_PATH_TENSOR || tensor_pays(g.M * g.S, g.N, g.K, 1));
+  *bytes = (want_tc && tc_grouped_supported(g)) ? tc_grouped_workspace_bytes(g) : 0;
+  return MM_OK;
+}
+
+mm_status mm_grouped_matmul_qweights(const mm_tensor* input, const mm_tensor* weights_q, const mm_tensor* w_scale,
+                                     const mm_tensor* w_zero_point, int64_t block_size,
+                                     const mm_tensor* group_indices, const mm_tensor* bias,
+                                     const mm_tensor* output, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  GroupedArgs g;
+  mm_status s = plan_grouped_q(input, weights_q, w_scale, w_zero_point, block_size, group_indices, bias, &g);
+  if (s != MM_OK) return s;
+  const int64_t oshape[3] = {g.M, g.S, g.N};
+  if ((s = check_output(output, g.dtype, 3, oshape)) != MM_OK) return s;
+  g.out = output->data;
+  if (g.M == 0 || g.S == 0 || g.N == 0) return finish(MM_OK, MM_PATH_NONE);
+  unsigned* status = device_status_ptr();
+  if (!status) return MM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int path = choose(tc_grouped_supported(g), tensor_pays(g.M * g.S, g.N, g.K, 1));
+  if (path < 0) return MM_ERR_UNSUPPORTED;
+  if (path == MM_PATH_TENSOR) {
+    const size_t need = tc_grouped_workspace_bytes(g);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+      return MM_ERR_WORKSPACE;
+    return finish(launch_tc_grouped(g, workspace, status, st), MM_PATH_TENSOR);
+  }
+  return finish(launch_simt_grouped(g, status, st), MM_PATH_SIMT);
+}
+
 // ------------------------------------------------------------------ GroupedMatMul without allocation
 //
 // Scratch for mm_grouped_matmul_noalloc: a fixed array in device memory that

@@ -45,6 +45,13 @@ struct GroupedArgs {
   const void* gi;  int64_t gi_ms, gi_ss;
   const void* bias; int64_t bias_gs, bias_ns;   // bias null = absent
   void* out;                 // dense [M, S, N]
+  // Weight-only quantized experts: w holds int8 (wq == 1) or uint8 (wq == 2)
+  // values and the weights are W = T((w - zero_point) * scale), scale and
+  // zero point [G, Kb, N] indexed by (g, k / qblock, n).  wq == 0: w is T.
+  int wq;
+  const void* wsc; int64_t wsc_gs, wsc_bs, wsc_ns;   // scale, type T
+  const void* wzp; int64_t wzp_gs, wzp_bs, wzp_ns;   // zero point (null = 0), type of w
+  int64_t qblock;
 };
 
 mm_status launch_simt_gemm(const GemmArgs& args, cudaStream_t stream);

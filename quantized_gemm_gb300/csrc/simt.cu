@@ -248,7 +248,28 @@ __global__ void __launch_bounds__(kThreads) simt_qlinear_kernel(const QLinearArg
 
 // ------------------------------------------------------------------ GroupedMatMul
 
+// Weight (g, k, n) of weight-only quantized experts: T((q - zp) * scale), the
+// difference exact, the product exact in the accumulator type for a bf16 or
+// f16 scale (at most 9 + 11 significant bits) and rounded once for f32/f64;
+// then rounded once to T (GroupedMatMul - 29, Summary: DequantizeLinear of
+// the weights).
 template <typename T>
+__device__ __forceinline__ typename Arith<T>::acc dequant_weight(const GroupedArgs& p, int64_t g, int64_t k,
+                                                                 int64_t n) {
+  using Acc = typename Arith<T>::acc;
+  const int64_t kq = k / p.qblock;
+  const uint8_t qb = static_cast<const uint8_t*>(p.w)[g * p.w_gs + k * p.w_ks + n * p.w_ns];
+  int d = p.wq == 1 ? (int)(int8_t)qb : (int)qb;
+  if (p.wzp) {
+    const uint8_t zb = static_cast<const uint8_t*>(p.wzp)[g * p.wzp_gs + kq * p.wzp_bs + n * p.wzp_ns];
+    d -= p.wq == 1 ? (int)(int8_t)zb : (int)zb;
+  }
+  const Acc sc = Arith<T>::load(static_cast<const T*>(p.wsc) + g * p.wsc_gs + kq * p.wsc_bs + n * p.wsc_ns);
+  const T w = Arith<T>::store((Acc)d * sc);
+  return Arith<T>::load(&w);
+}
+
+template <typename T, bool QW>
 __global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArgs p, unsigned* status) {
   using Acc = typename Arith<T>::acc;
   constexpr int kChunk = 1024;
@@ -276,8 +297,12 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArg
       for (int k = threadIdx.x; k < kc; k += kThreads) xs[k] = Arith<T>::load(X + m * p.x_rs + (k0 + k) * p.x_cs);
       __syncthreads();
       if (n < p.N) {
-        const T* wcol = W + g * p.w_gs + n * p.w_ns + k0 * p.w_ks;
-        for (int k = 0; k < kc; ++k) acc = mac<Acc>(acc, xs[k], Arith<T>::load(wcol + k * p.w_ks));
+        if (QW) {
+          for (int k = 0; k < kc; ++k) acc = mac<Acc>(acc, xs[k], dequant_weight<T>(p, g, k0 + k, n));
+        } else {
+          const T* wcol = W + g * p.w_gs + n * p.w_ns + k0 * p.w_ks;
+          for (int k = 0; k < kc; ++k) acc = mac<Acc>(acc, xs[k], Arith<T>::load(wcol + k * p.w_ks));
+        }
       }
     }
     if (n < p.N) {
@@ -285,6 +310,12 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArg
       Out[r * p.N + n] = Arith<T>::store(acc);
     }
   }
+}
+
+template <typename T>
+void launch_grouped(const GroupedArgs& p, unsigned* status, dim3 grid, cudaStream_t stream) {
+  if (p.wq) simt_grouped_kernel<T, true><<<grid, kThreads, 0, stream>>>(p, status);
+  else simt_grouped_kernel<T, false><<<grid, kThreads, 0, stream>>>(p, status);
 }
 
 dim3 tile_grid(int64_t M, int64_t N, int64_t batch) {
@@ -326,10 +357,10 @@ mm_status launch_simt_grouped(const GroupedArgs& p, unsigned* status, cudaStream
   if (nb > 0x7fffffff) return MM_ERR_UNSUPPORTED;
   const dim3 grid((unsigned)nb, (unsigned)(rows < 65535 ? rows : 65535));
   switch (p.dtype) {
-    case MM_BF16: simt_grouped_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p, status); break;
-    case MM_F16: simt_grouped_kernel<__half><<<grid, kThreads, 0, stream>>>(p, status); break;
-    case MM_F32: simt_grouped_kernel<float><<<grid, kThreads, 0, stream>>>(p, status); break;
-    case MM_F64: simt_grouped_kernel<double><<<grid, kThreads, 0, stream>>>(p, status); break;
+    case MM_BF16: launch_grouped<__nv_bfloat16>(p, status, grid, stream); break;
+    case MM_F16: launch_grouped<__half>(p, status, grid, stream); break;
+    case MM_F32: launch_grouped<float>(p, status, grid, stream); break;
+    case MM_F64: launch_grouped<double>(p, status, grid, stream); break;
     default: return MM_ERR_DTYPE;
   }
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;

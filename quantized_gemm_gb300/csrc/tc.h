@@ -19,6 +19,8 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* workspace, unsigned* sta
 
 bool tc_grouped_supported(const GroupedArgs& g);
 size_t tc_grouped_workspace_bytes(const GroupedArgs& g);
+// GroupedArgs with wq != 0 take the fused-dequantisation kernel (CTA pairs):
+// the weights stay int8/uint8 in memory and are dequantised in shared memory.
 mm_status launch_tc_grouped(const GroupedArgs& g, void* workspace, unsigned* status, cudaStream_t stream);
 
 }  // namespace qg

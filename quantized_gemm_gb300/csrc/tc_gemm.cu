@@ -65,17 +65,26 @@ constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
 // 4 stages.  CTA pair (cta_group::2, a 256 x 256 tile per pair): each CTA holds
 // its 128 rows of A and half (128) of the tile's B columns, 32 KB per stage,
 // 6 stages.
-template <bool PAIR>
+template <int MODE, bool PAIR>
 struct Geo {
   static constexpr int kBRows = PAIR ? BN / 2 : BN;     // B columns (rows of B') held by one CTA
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = PAIR ? 6 : 4;
+  // kGroupedQ gives one stage's worth of shared memory to its int8 staging ring.
+  static constexpr int kStages = PAIR ? (MODE == kGroupedQ ? 5 : 6) : 4;
   static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
 constexpr int kGroupM = 16;                      // raster band height (tiles), a power of two
+// kGroupedQ staging ring (per CTA and stage): the int8 weight tile (64 k x 128
+// n), the k-block's scale row (128 x 16-bit) and zero-point row (128 bytes).
+constexpr int kQStages = 4;
+constexpr int kQTileBytes = 64 * 128, kQScaleOff = kQTileBytes, kQZeroOff = kQScaleOff + 256;
+constexpr int kQStageBytes = 9216;
+constexpr int kConvWarps = 4;                    // kGroupedQ converter warps (one per SM sub-partition)
+
+__host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedQ; }
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
@@ -85,16 +94,25 @@ constexpr int kStageWords = 32 * 16;             // float per-warp output stagin
 // the epilogue's latency (short-K float products, the QLinear requantisation).
 // With 18 warps ptxas caps a thread at 96 registers (five warps share one SM
 // sub-partition's register file); QLinear keeps its 64 int32 running sums in
-// registers and drains TMEM 16 columns at a time.
+// registers and drains TMEM 16 columns at a time.  kGroupedQ runs 8 epilogue
+// warps of 128 columns plus 4 converter warps (14 warps: 128 registers).
 template <int MODE, bool PAIR>
 struct Cfg {
-  static constexpr int kEpiWarps = 16;
-  static constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
+  static constexpr int kEpiWarps = MODE == kGroupedQ ? 8 : 16;
+  static constexpr int kConv = MODE == kGroupedQ ? kConvWarps : 0;
+  static constexpr int kConvWarp0 = kEpiWarp0 + kEpiWarps;
+  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps + kConv) * 32;
   static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
   static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : kStageWords;
-  static constexpr int kSmem = Geo<PAIR>::kRingBytes + kCtrlBytes + kEpiWarps * kWarpWords * 4 + 1024;
+  static constexpr int kEpiBytes = kEpiWarps * kWarpWords * 4;
+  // kGroupedQ staging ring, after the epilogue's slices (1024-byte aligned)
+  static constexpr int kQOff = (Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes + 1023) / 1024 * 1024;
+  static constexpr int kSmem = (MODE == kGroupedQ ? kQOff + kQStages * kQStageBytes
+                                                  : Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes) +
+                               1024;
   static_assert(kSmem <= 232448, "shared memory per block");
-  static_assert(16 * Geo<PAIR>::kStages + 48 <= kCtrlBytes, "control block");
+  static_assert(16 * Geo<MODE, PAIR>::kStages + 48 + 16 * kQStages <= kCtrlBytes, "control block");
+  static_assert(MODE != kGroupedQ || PAIR, "the fused dequantisation runs on CTA pairs");
 };
 
 struct Tile {
@@ -124,8 +142,8 @@ __device__ __forceinline__ int64_t batch_off(const TcParams& p, const int64_t* b
 template <int MODE, bool PAIR>
 __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t total, Tile& ti, int& g_hint) {
   if (t >= total) return false;
-  if (MODE == kGrouped) {
-    constexpr int TR = Geo<PAIR>::kTileRows;
+  if (is_grouped(MODE)) {
+    constexpr int TR = Geo<MODE, PAIR>::kTileRows;
     int g = g_hint;
     while (g + 1 < p.G && __ldg(p.g_tile_start + g + 1) <= t) ++g;
     g_hint = g;
@@ -158,18 +176,18 @@ __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t t
   }
   ti.batch = b;
   ti.g = 0;
-  ti.m0 = (int64_t)mtile * Geo<PAIR>::kTileRows;
+  ti.m0 = (int64_t)mtile * Geo<MODE, PAIR>::kTileRows;
   ti.n0 = (int64_t)ntile * BN;
   ti.a_row = (int32_t)ti.m0;
   ti.a_b = (int32_t)batch_off(p, p.a_bc, b);
   ti.b_b = (int32_t)batch_off(p, p.b_bc, b);
-  ti.rows = (int32_t)min((int64_t)Geo<PAIR>::kTileRows, p.M - ti.m0);
+  ti.rows = (int32_t)min((int64_t)Geo<MODE, PAIR>::kTileRows, p.M - ti.m0);
   return true;
 }
 
 template <int MODE>
 __device__ __forceinline__ int64_t total_tiles(const TcParams& p) {
-  return MODE == kGrouped ? (int64_t)p.g_tile_start[p.G] : p.tiles;
+  return is_grouped(MODE) ? (int64_t)p.g_tile_start[p.G] : p.tiles;
 }
 
 // The persistent schedule: a CTA (or CTA pair) takes tiles first, first + step, ...
@@ -181,11 +199,17 @@ __device__ __forceinline__ int64_t tile_step() { return PAIR ? (gridDim.x >> 1) 
 // ------------------------------------------------------------------ producer
 
 template <int MODE, bool PAIR>
-__device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const TcParams& p, uint32_t sbase,
-                             uint32_t full0, uint32_t empty0, volatile int* abort) {
-  using G = Geo<PAIR>;
+__device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmS,
+                             const CUtensorMap* tmZ, const TcParams& p, uint32_t sbase, uint32_t full0,
+                             uint32_t empty0, uint32_t qbase, uint32_t qfull0, uint32_t qempty0,
+                             volatile int* abort) {
+  using G = Geo<MODE, PAIR>;
   prefetch_tmap(tmA);
   prefetch_tmap(tmB);
+  if (MODE == kGroupedQ) {
+    prefetch_tmap(tmS);
+    if (p.wzp_present) prefetch_tmap(tmZ);
+  }
   const int64_t total = total_tiles<MODE>(p);
   // In a pair each CTA loads its own 128 rows of A and 128 columns of B; every
   // copy completes on the leader CTA's full barrier, which expects both CTAs' bytes.
@@ -194,6 +218,7 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
   const int32_t bcol_off = PAIR ? (int32_t)(rank * G::kBRows) : 0;
   uint32_t stage = 0, phase = 0;
   uint32_t pending = 0, pend_parity = 0;   // bit s: a load into stage s was issued (and its parity)
+  uint32_t qstage = 0, qphase = 0, qpending = 0, qpend_parity = 0;   // the same for the staging ring
   Tile ti;
   int gh = 0;
   for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
@@ -203,7 +228,22 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
       const uint32_t sa = sbase + stage * G::kStageBytes, sb = sa + G::kABytes;
       const int32_t k0 = kb * BK;
       const int32_t ar = ti.a_row + arow_off, bc = (int32_t)ti.n0 + bcol_off;
-      if (PAIR) {
+      if (MODE == kGroupedQ) {
+        // A as usual; the B half arrives as int8 (plus its scale and zero-point
+        // rows) in the staging ring, and the converter warps write it to sb.
+        if (!mbar_wait(qempty0 + 8 * qstage, qphase ^ 1, abort, p.status, p.timeout_ns)) goto done;
+        const uint32_t qfull = qfull0 + 8 * qstage, qs = qbase + qstage * kQStageBytes;
+        if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kABytes);
+        tma_load_3d_pair(sa, tmA, k0, ar, ti.a_b, mapa_shared(full, 0));
+        const int32_t kq = kb / p.kb_per_q;
+        mbar_arrive_expect_tx(qfull, kQTileBytes + 256 + (p.wzp_present ? 128 : 0));
+        tma_load_3d(qs, tmB, bc, k0, ti.b_b, qfull);
+        tma_load_3d(qs + kQScaleOff, tmS, bc, kq, ti.b_b, qfull);
+        if (p.wzp_present) tma_load_3d(qs + kQZeroOff, tmZ, bc, kq, ti.b_b, qfull);
+        qpending |= 1u << qstage;
+        qpend_parity = (qpend_parity & ~(1u << qstage)) | (qphase << qstage);
+        if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
+      } else if (PAIR) {
         const uint32_t bar = mapa_shared(full, 0);
         if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kStageBytes);
         if (!p.a_mn) {
@@ -240,13 +280,23 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
   }
 done:
   // Let every issued copy land before the CTA can exit.  In a pair the leader's
-  // full barriers count both CTAs' bytes, so the leader waits for both.
+  // full barriers count both CTAs' bytes, so the leader waits for both.  The
+  // waits share one deadline (after an abort, a kGroupedQ full barrier may
+  // also lack the converters' arrivals and only the deadline ends its wait).
+  const uint64_t t_end = globaltimer() + p.teardown_ns;
+  auto left = [&]() -> uint64_t {
+    const uint64_t now = globaltimer();
+    return now < t_end ? t_end - now : 0;
+  };
   if (!PAIR || rank == 0)
     for (int s = 0; s < G::kStages; ++s)
       if (pending & (1u << s)) {
-        if (PAIR) mbar_wait_teardown_cluster(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
-        else mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, p.teardown_ns);
+        if (PAIR) mbar_wait_teardown_cluster(full0 + 8 * s, (pend_parity >> s) & 1u, left());
+        else mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, left());
       }
+  if (MODE == kGroupedQ)
+    for (int s = 0; s < kQStages; ++s)
+      if (qpending & (1u << s)) mbar_wait_teardown(qfull0 + 8 * s, (qpend_parity >> s) & 1u, left());
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -257,7 +307,7 @@ done:
 template <int MODE, bool PAIR>
 __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32_t full0, uint32_t empty0,
                         uint32_t accf0, uint32_t acce0, uint32_t drain, volatile int* abort) {
-  using G = Geo<PAIR>;
+  using G = Geo<MODE, PAIR>;
   const int64_t total = total_tiles<MODE>(p);
   uint32_t stage = 0, phase = 0, seg = 0;
   Tile ti;
@@ -383,6 +433,82 @@ __device__ __forceinline__ uint32_t requant_byte_fast(int32_t acc, float sa, flo
   *slow = !(fast && (aq >= 2097152.0f || half_gap > __fmul_rn(aq, 9.5367431640625e-07f)));
   const float t = fminf(fmaxf(__fadd_rn(r, yzp), qmin), qmax);
   return (uint32_t)(__float_as_int(__fadd_rn(t, kMagic)) - 0x4B400000) & 0xFFu;
+}
+
+// ------------------------------------------------------------------ dequantising converters (kGroupedQ)
+
+// Four warps (128 threads) per CTA turn each k-block's int8/uint8 weight tile
+// (64 k x this CTA's 128 columns, in the staging ring) into the MMA's B
+// operand: W = T((q - zp) * scale), rounded once to bf16/f16, written in the
+// MN-major 128-byte-swizzled layout a TMA load would give (two 64-column
+// sub-tiles; the 16-byte chunk c of row k sits at chunk c ^ (k % 8)).  Thread t
+// owns columns 8*(t%16) .. +7 and rows t/16 + 8*i.  The difference q - zp is
+// formed exactly in fp32: the byte placed in the low mantissa of 2^23 (after
+// adding 128 to int8 values) minus 2^23 + 128 + zp.  Its product with a bf16
+// or f16 scale has at most 9 + 11 significant bits, so it is exact too and the
+// final conversion is the only rounding.  Each warp then makes its writes
+// visible to the tensor cores, frees the staging slot and arrives on the
+// leader CTA's stage barrier, which the MMA waits on.
+template <int MODE, bool PAIR>
+__device__ void run_convert(const TcParams& p, uint32_t sbase, uint32_t full0, uint32_t qbase, uint32_t qfull0,
+                            uint32_t qempty0, volatile int* abort) {
+  using G = Geo<MODE, PAIR>;
+  const int ct = (int)threadIdx.x - Cfg<MODE, PAIR>::kConvWarp0 * 32;
+  const int lane = threadIdx.x & 31;
+  const int cc = ct & 15, k_first = ct >> 4;
+  const int sub = cc >> 3, c = cc & 7;
+  const uint32_t flip = p.w_signed ? 0x80808080u : 0u;
+  const float zbias = 8388608.f + (p.w_signed ? 128.f : 0.f);
+  const int64_t total = total_tiles<MODE>(p);
+  uint32_t stage = 0, qstage = 0, qphase = 0;
+  Tile ti;
+  int gh = 0;
+  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      if (!__all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qstage, qphase, abort, p.status, p.timeout_ns))) return;
+      const uint32_t qs = qbase + qstage * kQStageBytes;
+      const uint4 sraw = lds128(qs + kQScaleOff + cc * 16);
+      const uint2 zraw = p.wzp_present ? lds64(qs + kQZeroOff + cc * 8) : make_uint2(0u, 0u);
+      float sc[8], cz[8];
+      {
+        const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
+        const uint32_t zw[2] = {zraw.x, zraw.y};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t h = (sw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+          sc[e] = p.out_f16 ? __half2float(__ushort_as_half((unsigned short)h)) : __uint_as_float(h << 16);
+          const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+          cz[e] = zbias + (float)(p.w_signed ? (int)(int8_t)zb : (int)zb);
+        }
+      }
+      const uint32_t bsm = sbase + stage * G::kStageBytes + G::kABytes + sub * 8192;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = k_first + 8 * i;
+        uint2 q = lds64(qs + k * 128 + cc * 8);
+        q.x ^= flip;
+        q.y ^= flip;
+        uint32_t w[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const uint32_t src = e2 < 2 ? q.x : q.y;
+          const int b0 = (e2 & 1) * 2;
+          const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
+          const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
+          w[e2] = pack2(__fmul_rn(f0, sc[2 * e2]), __fmul_rn(f1, sc[2 * e2 + 1]), p.out_f16);
+        }
+        sts128(bsm + k * 128 + ((c ^ (k & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+      }
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(qempty0 + 8 * qstage);
+        mbar_arrive_cluster(mapa_shared(full0 + 8 * stage, 0));
+      }
+      if (++stage == G::kStages) stage = 0;
+      if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -535,19 +661,12 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       ++seg;
       if (!__all_sync(0xffffffffu, wait_full(buf, aph))) return;
       tc_fence_after();
-      const uint32_t taddr = tmem + tlane + buf * BN + slice * kCols;
-      uint32_t r[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld32(taddr + c * 32, r[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      release(buf);
+      const uint32_t taddr0 = tmem + tlane + buf * BN + slice * kCols;
       // This thread's output row (kept even when the row is past the tile's
       // valid rows: it is then only shuffled around, never dereferenced).
       uint16_t* yrow;
       const uint16_t* crow = nullptr;
-      if (MODE == kGrouped) {
+      if (is_grouped(MODE)) {
         const int64_t orow = row_ok ? p.g_rowlist[ti.a_row + row_off + rloc] : 0;
         yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
         if (p.c && row_ok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
@@ -557,41 +676,56 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         if (p.c && row_ok)
           crow = static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs;
       }
-      // Each 32-column chunk (64 bytes of each of the warp's 32 rows) is staged
-      // through the warp's shared-memory slice (16-byte pieces XOR-swizzled by
-      // row pair, so both the row-wise writes and the column-wise reads are
-      // bank-conflict free) and written back so that each warp store covers 8
-      // rows x 64 bytes of whole 32-byte sectors.
+      // The warp's columns, 64 at a time (two tcgen05.ld of 32); the
+      // accumulator is released once its last columns are in registers.
+#pragma unroll 1
+      for (int q64 = 0; q64 < kCols / 64; ++q64) {
+        const uint32_t taddr = taddr0 + q64 * 64;
+        uint32_t r[2][32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t n = ncol0 + 32 * h;
-        if (n >= p.N) break;
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
-        if (crow) add_c32(p, crow, n, v);
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1], p.out_f16);
-        if (p.y_vec && n + 32 <= p.N) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(stg + lane * 16 + ((q ^ ((lane >> 1) & 3)) * 4)) =
-                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        for (int c = 0; c < 2; ++c) tmem_ld32(taddr + c * 32, r[c]);
+        tmem_ld_wait();
+        if (q64 == kCols / 64 - 1) {
+          tc_fence_before();
           __syncwarp();
+          release(buf);
+        }
+        // Each 32-column chunk (64 bytes of each of the warp's 32 rows) is staged
+        // through the warp's shared-memory slice (16-byte pieces XOR-swizzled by
+        // row pair, so both the row-wise writes and the column-wise reads are
+        // bank-conflict free) and written back so that each warp store covers 8
+        // rows x 64 bytes of whole 32-byte sectors.
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = i * 8 + (lane >> 2), pc = lane & 3;
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
-            uint16_t* dst = reinterpret_cast<uint16_t*>(
-                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(yrow), rr));
-            if (quad * 32 + rr < rows_cta) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
+        for (int h = 0; h < 2; ++h) {
+          const int64_t n = ncol0 + q64 * 64 + 32 * h;
+          if (n >= p.N) break;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
+          if (crow) add_c32(p, crow, n, v);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1], p.out_f16);
+          if (p.y_vec && n + 32 <= p.N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(stg + lane * 16 + ((q ^ ((lane >> 1) & 3)) * 4)) =
+                  make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = i * 8 + (lane >> 2), pc = lane & 3;
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
+              uint16_t* dst = reinterpret_cast<uint16_t*>(
+                  __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(yrow), rr));
+              if (quad * 32 + rr < rows_cta) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
+            }
+            __syncwarp();
+          } else if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
           }
-          __syncwarp();
-        } else if (row_ok) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
         }
       }
     }
@@ -603,8 +737,9 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                    const TcParams p) {
-  using G = Geo<PAIR>;
+  using G = Geo<MODE, PAIR>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -615,13 +750,22 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   const uint32_t acce0 = accf0 + 16, drain = acce0 + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 16 * S + 40);
   volatile int* abort = reinterpret_cast<volatile int*>(ctrl + 16 * S + 44);
+  const uint32_t qfull0 = cbase + 16 * S + 48, qempty0 = qfull0 + 8 * kQStages;   // kGroupedQ only
+  const uint32_t qbase = sbase + Cfg<MODE, PAIR>::kQOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // kGroupedQ: a stage is full once the leader's producer has armed it (A
+    // bytes of both CTAs) and the converter warps of both CTAs have arrived.
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, MODE == kGroupedQ ? 1 + 2 * kConvWarps : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    if (MODE == kGroupedQ)
+      for (int s = 0; s < kQStages; ++s) {
+        mbar_init(qfull0 + 8 * s, 1);
+        mbar_init(qempty0 + 8 * s, kConvWarps);
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
       mbar_init(acce0 + 8 * b, (PAIR ? 2 : 1) * Cfg<MODE, PAIR>::kEpiWarps);
@@ -649,16 +793,19 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<MODE, PAIR>(&tmA, &tmB, p, sbase, full0, empty0, abort);
+    if (lane == 0)
+      run_producer<MODE, PAIR>(&tmA, &tmB, &tmS, &tmZ, p, sbase, full0, empty0, qbase, qfull0, qempty0, abort);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) run_mma<MODE, PAIR>(p, sbase, tmem, full0, empty0, accf0, acce0, drain, abort);
       else mbar_wait_teardown(drain, 0, p.teardown_ns);   // the leader's last commit reaches this CTA too
     }
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp < Cfg<MODE, PAIR>::kConvWarp0) {
     uint32_t* stage = reinterpret_cast<uint32_t*>(ctrl + kCtrlBytes) +
                       (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
     run_epilogue<MODE, PAIR>(p, tmem, accf0, acce0, abort, stage);
+  } else if (MODE == kGroupedQ) {
+    run_convert<MODE, PAIR>(p, sbase, full0, qbase, qfull0, qempty0, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -761,6 +908,26 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
   return r == CUDA_SUCCESS;
 }
 
+bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int64_t d2, int64_t s1, int64_t s2,
+                   int box0, int box1, OperandPlan* out) {
+  auto encode = encode_fn();
+  if (!encode || !ptr || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+  if (d0 < 1 || d1 < 1 || d2 < 1 || d0 > 0x7fffffffLL || d1 > 0x7fffffffLL || d2 > 0x7fffffffLL) return false;
+  if (s1 <= 0 || s2 <= 0 || (s1 & 15) || (s2 & 15) || s1 >= (1ll << 40) || s2 >= (1ll << 40)) return false;
+  if ((box0 * elem_bytes) % 16 || box0 > 256 || box1 > 256) return false;
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  if (elem_bytes != 1 && elem_bytes != 2) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  const cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
+  const cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  out->mn_major = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) out->bc[d] = 0;
+  return encode(&out->map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair) {
   const uint32_t m = pair ? 2 * BM : BM;        // a pair's MMA covers both CTAs' rows
   return (1u << 4)                              // D: fp32
@@ -822,8 +989,8 @@ int max_pair_clusters() {
 }
 
 template <int MODE, bool PAIR>
-mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const TcParams& p, int64_t work,
-                        cudaStream_t stream) {
+mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtensorMap& ms, const CUtensorMap& mz,
+                        const TcParams& p, int64_t work, cudaStream_t stream) {
   constexpr int kSmem = Cfg<MODE, PAIR>::kSmem, kThreadsM = Cfg<MODE, PAIR>::kThreads;
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
@@ -831,7 +998,7 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const TcPara
   if constexpr (!PAIR) {
     const int sms = sm_count();
     const int grid = (int)(work < sms ? (work > 0 ? work : 1) : sms);
-    tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, p);
+    tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, ms, mz, p);
     return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
   } else {
     // One persistent pair per resident cluster slot: a pair that could not be
@@ -851,21 +1018,22 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const TcPara
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, p) == cudaSuccess ? MM_OK
-                                                                                               : MM_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, ms, mz, p) == cudaSuccess
+               ? MM_OK
+               : MM_ERR_CUDA;
   }
 }
 
 }  // namespace
 
 mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan& b, TcParams& p,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const OperandPlan* s, const OperandPlan* z) {
   p.a_mn = a.mn_major;
   p.b_mn = b.mn_major;
   for (int d = 0; d < kMaxBatchDims; ++d) { p.a_bc[d] = a.bc[d]; p.b_bc[d] = b.bc[d]; }
   p.num_kb = (int)((p.K + BK - 1) / BK);
   int64_t work = 0;
-  if (mode != kGrouped) {
+  if (!is_grouped(mode)) {
     const int64_t rows = pair ? 2 * BM : BM;
     p.mt = (p.M + rows - 1) / rows;
     p.nt = (p.N + BN - 1) / BN;
@@ -886,15 +1054,23 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
     p.fd_bshape[d] = make_fastdiv((uint32_t)(p.bm.shape[d] > 0 ? p.bm.shape[d] : 1));
   }
   if (p.kb_per_seg > p.num_kb) p.kb_per_seg = p.num_kb > 0 ? p.num_kb : 1;
+  if (p.kb_per_q < 1) p.kb_per_q = 1 << 30;
+  // Only kGroupedQ reads the scale and zero-point maps; other modes get A's map
+  // in those (unused) parameters.
+  const CUtensorMap& ms = s ? s->map : a.map;
+  const CUtensorMap& mz = z ? z->map : (s ? s->map : a.map);
   switch (mode) {
     case kDense:
-      return pair ? launch_kernel<kDense, true>(a, b, p, work, stream)
-                  : launch_kernel<kDense, false>(a, b, p, work, stream);
+      return pair ? launch_kernel<kDense, true>(a, b, ms, mz, p, work, stream)
+                  : launch_kernel<kDense, false>(a, b, ms, mz, p, work, stream);
     case kGrouped:
-      return pair ? launch_kernel<kGrouped, true>(a, b, p, work, stream)
-                  : launch_kernel<kGrouped, false>(a, b, p, work, stream);
+      return pair ? launch_kernel<kGrouped, true>(a, b, ms, mz, p, work, stream)
+                  : launch_kernel<kGrouped, false>(a, b, ms, mz, p, work, stream);
     case kQLinear:   // single CTAs only: the product is bound by its epilogue
-      return pair ? MM_ERR_UNSUPPORTED : launch_kernel<kQLinear, false>(a, b, p, work, stream);
+      return pair ? MM_ERR_UNSUPPORTED : launch_kernel<kQLinear, false>(a, b, ms, mz, p, work, stream);
+    case kGroupedQ:  // CTA pairs only
+      if (!pair || !s) return MM_ERR_UNSUPPORTED;
+      return launch_kernel<kGroupedQ, true>(a, b, ms, mz, p, work, stream);
     default:
       return MM_ERR_UNSUPPORTED;
   }
@@ -909,6 +1085,8 @@ bool use_pair(int64_t M, int64_t K) { return M > BM && K >= kPairMinK; }
 // 256 rows instead of 128).  Measured on 16384 x 2 routed rows, K = 4096,
 // N = 14336: pairs are 5% faster with 8 groups (4096 rows each on average)
 // and 1.5% slower with 64 groups (512 rows), so they need 1024 rows a group.
+bool grouped_q_pairs_available() { return max_pair_clusters<kGroupedQ>() > 0; }
+
 bool use_grouped_pair(int64_t rows, int64_t G, int64_t K) {
   return K >= kPairMinK && rows >= 8 * BM * G && max_pair_clusters<kGrouped>() > 0;
 }

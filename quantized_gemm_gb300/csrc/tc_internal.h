@@ -13,7 +13,9 @@ constexpr int kTileM = 128;   // UMMA M (TMEM lanes)
 constexpr int kTileN = 256;   // UMMA N (TMEM columns per accumulator)
 constexpr int kTileK = 64;    // one 128-byte swizzle row of 16-bit elements
 
-enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2 };
+// kGroupedQ: GroupedMatMul whose weights arrive as int8/uint8 with scales and
+// zero points (DequantizeLinear fused into the mainloop; CTA pairs only).
+enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3 };
 
 struct TcParams {
   int64_t M, N, K;
@@ -54,6 +56,9 @@ struct TcParams {
   const int32_t* g_tile_start;
   const int32_t* g_rowlist;
   int G;
+  // kGroupedQ: weights are int8 (w_signed) or uint8; a scale row (and, when
+  // wzp_present, a zero-point row) applies to kb_per_q consecutive k-blocks.
+  int w_signed, wzp_present, kb_per_q;
   unsigned* status;
   unsigned long long timeout_ns;    // limit of each pipeline wait
   unsigned long long teardown_ns;   // limit of the waits that let in-flight copies and MMAs land
@@ -67,16 +72,23 @@ struct OperandPlan {
 
 bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int64_t mn_stride, int64_t k_stride,
                   const BatchMap& bm, const int64_t* bstride, int box_mn, OperandPlan* out);
+// A plain (unswizzled) 3-D tensor map over elements of elem_bytes bytes:
+// dims d0 (contiguous) x d1 x d2, byte strides s1 and s2, box box0 x box1 x 1.
+bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int64_t d2, int64_t s1, int64_t s2,
+                   int box0, int box1, OperandPlan* out);
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair);
 void init_params(TcParams* p);
 // Fills the tile bookkeeping and launches tc_gemm_kernel: one CTA per SM, or
 // (pair) 2-CTA clusters computing 256-row tiles with cta_group::2 MMAs.
 // Returns MM_ERR_UNSUPPORTED when pairs cannot be placed.
+// kGroupedQ also takes the scale and zero-point maps (s, z).
 mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan& b, TcParams& p,
-                    cudaStream_t stream);
+                    cudaStream_t stream, const OperandPlan* s = nullptr, const OperandPlan* z = nullptr);
 // Whether an M x K problem uses CTA pairs.
 bool use_pair(int64_t M, int64_t K);
 bool use_grouped_pair(int64_t rows, int64_t G, int64_t K);
+// Whether the fused-dequantisation kernel's CTA pairs can be resident.
+bool grouped_q_pairs_available();
 int sm_count_public();
 
 }  // namespace qg

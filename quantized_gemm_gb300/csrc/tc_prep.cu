@@ -465,6 +465,31 @@ bool plan_grouped_b(const GroupedArgs& g, bool pair, OperandPlan* b) {
   return g.G <= 1 || b->bc[0] == 1;
 }
 
+// Byte stride of a dimension of extent `count` for a plain tensor map: the
+// given stride, or (a dimension of extent 1 is never stepped) any valid one.
+int64_t map_stride(int64_t stride_bytes, int64_t count, int64_t fallback) {
+  return count == 1 ? (fallback + 15) / 16 * 16 : stride_bytes;
+}
+
+// Weight-only quantized experts: the int8/uint8 weights (boxes of 128 columns
+// x 64 k) and the scale and zero-point rows (boxes of 128 columns x 1 row) as
+// plain tensor maps indexed (n, k or k-block, g).
+bool plan_grouped_q(const GroupedArgs& g, OperandPlan* b, OperandPlan* sm, OperandPlan* zm) {
+  if (g.wq == 0 || g.w_ns != 1 || g.wsc_ns != 1 || (g.wzp && g.wzp_ns != 1)) return false;
+  if (!(g.qblock >= g.K || g.qblock % kTileK == 0)) return false;
+  const int64_t kb = (g.K + g.qblock - 1) / g.qblock;
+  if (!plan_plain_3d(g.w, 1, g.N, g.K, g.G, map_stride(g.w_ks, g.K, g.N), map_stride(g.w_gs, g.G, g.w_ks * g.K),
+                     128, 64, b))
+    return false;
+  const int64_t sbs = map_stride(g.wsc_bs * 2, kb, g.N * 2);
+  if (!plan_plain_3d(g.wsc, 2, g.N, kb, g.G, sbs, map_stride(g.wsc_gs * 2, g.G, sbs * kb), 128, 1, sm)) return false;
+  if (g.wzp) {
+    const int64_t zbs = map_stride(g.wzp_bs, kb, g.N);
+    if (!plan_plain_3d(g.wzp, 1, g.N, kb, g.G, zbs, map_stride(g.wzp_gs, g.G, zbs * kb), 128, 1, zm)) return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 size_t tc_grouped_workspace_bytes(const GroupedArgs& g) {
@@ -478,16 +503,18 @@ bool tc_grouped_supported(const GroupedArgs& g) {
   // an upper bound on the tile count must fit the int32 tile table
   const int64_t nt = (g.N + kTileN - 1) / kTileN;
   if ((g.M * g.S / kTileM + g.G + 1) * nt > 0x7fffffffLL) return false;
-  OperandPlan b;
+  OperandPlan b, sm, zm;
+  if (g.wq) return plan_grouped_q(g, &b, &sm, &zm) && grouped_q_pairs_available();
   return plan_grouped_b(g, false, &b);
 }
 
 mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cudaStream_t stream) {
-  OperandPlan a, b;
-  // CTA pairs (256-row tiles) when groups are large enough; the routing scan
-  // counts tiles of the same height.
-  const bool pair = use_grouped_pair(g.M * g.S, g.G, g.K);
-  if (!ws || !status || !plan_grouped_b(g, pair, &b)) return MM_ERR_UNSUPPORTED;
+  OperandPlan a, b, sm, zm;
+  // CTA pairs (256-row tiles) when groups are large enough, and always for
+  // quantized weights; the routing scan counts tiles of the same height.
+  const bool pair = g.wq ? true : use_grouped_pair(g.M * g.S, g.G, g.K);
+  if (!ws || !status) return MM_ERR_UNSUPPORTED;
+  if (g.wq ? !plan_grouped_q(g, &b, &sm, &zm) : !plan_grouped_b(g, pair, &b)) return MM_ERR_UNSUPPORTED;
   const GLayout l = glayout(g.M, g.S, g.G, g.K, 2);
   char* base = static_cast<char*>(ws);
   int32_t* count = reinterpret_cast<int32_t*>(base + l.off_count);
@@ -526,6 +553,11 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.M = rows; p.N = g.N; p.K = g.K;
   p.nt = nt;
   p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major, pair);
+  if (g.wq) {
+    p.w_signed = g.wq == 1;
+    p.wzp_present = g.wzp != nullptr;
+    p.kb_per_q = g.qblock >= g.K ? (1 << 30) : (int)(g.qblock / kTileK);
+  }
   p.out_f16 = g.dtype == MM_F16;
   p.y = g.out;
   p.y_rs = g.N;
@@ -541,6 +573,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.G = (int)g.G;
   p.status = status;
   // The tile count is known only on the device: one persistent CTA (pair) per SM (pair).
+  if (g.wq) return launch_tc(kGroupedQ, true, a, b, p, stream, &sm, g.wzp ? &zm : nullptr);
   return launch_tc(kGrouped, pair, a, b, p, stream);
 }
 

@@ -158,3 +158,27 @@ def test_policy_and_status_strings(lib):
     for s in range(9):
         assert lib.mm_status_string(s)
     assert qg.mm_version() == "0.1.0"
+
+
+def test_grouped_qweights_validation(lib):
+    # input bf16 [6,8]; int8 weights [3,8,16]; scales bf16 [3, ceil(8/B), 16]
+    ref = ctypes.byref
+    x, gi, out = T((6, 8), 0), T((6, 2), 4), T((6, 2, 16), 0)
+    wq, s1, z1 = T((3, 8, 16), 8), T((3, 1, 16), 0), T((3, 1, 16), 8)
+    call = lib.mm_grouped_matmul_qweights
+    # block 4 needs scales [3, 2, 16]
+    assert call(ref(x), ref(wq), ref(s1), None, 4, ref(gi), None, ref(out), None, 0, None) == 2
+    # a negative block size
+    assert call(ref(x), ref(wq), ref(s1), None, -1, ref(gi), None, ref(out), None, 0, None) == 1
+    # weights must be 8-bit, the scale of type T, the zero point of the weights' type
+    assert call(ref(x), ref(T((3, 8, 16), 0)), ref(s1), None, 0, ref(gi), None, ref(out), None, 0, None) == 3
+    assert call(ref(x), ref(wq), ref(T((3, 1, 16), 2)), None, 0, ref(gi), None, ref(out), None, 0, None) == 3
+    assert call(ref(x), ref(wq), ref(s1), ref(T((3, 1, 16), 9)), 0, ref(gi), None, ref(out), None, 0, None) == 3
+    # zero point of another shape; K mismatch with the input
+    assert call(ref(x), ref(wq), ref(s1), ref(T((3, 2, 16), 8)), 0, ref(gi), None, ref(out), None, 0, None) == 2
+    assert call(ref(x), ref(T((3, 7, 16), 8)), ref(s1), ref(z1), 0, ref(gi), None, ref(out), None, 0, None) == 2
+    # output of the wrong type
+    assert call(ref(x), ref(wq), ref(s1), ref(z1), 0, ref(gi), None, ref(T((6, 2, 16), 1)), None, 0, None) == 3
+    nbytes = ctypes.c_size_t(123)
+    assert lib.mm_grouped_matmul_qweights_workspace_size(ref(x), ref(wq), ref(s1), None, 3, ref(gi),
+                                                         ref(nbytes)) == 2
