@@ -300,6 +300,11 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
         workloads.grouped_bf16(device=dev, dtype=torch.float16, index_dtype=torch.int64), world, stream, bf16_peak)
     # The same sizes with 8 groups (4096 rows each on average): CTA-pair tiles.
     out["grouped_bf16_g8"] = bench_grouped(workloads.grouped_bf16(device=dev, G=8), world, stream, bf16_peak)
+    # Weight-only int8 experts at the same sizes (dequantization fused into the
+    # mainloop): one scale per group and column, and per 128 rows of K.
+    for block in (0, 128):
+        out["grouped_qweights_b%d" % block] = bench_grouped_q(workloads.grouped_qweights(device=dev, block=block),
+                                                              world, stream, bf16_peak)
     return out
 
 
@@ -342,6 +347,26 @@ def bench_grouped(d, world, stream, peak):
            "frac": tf / peak, "kernels_per_call": 4, "l2": "weights (7.5 GB) larger than L2",
            "types": "%s, indices %s" % (x.dtype, gi.dtype)}
     del d, x, w, gi, yo, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_grouped_q(d, world, stream, peak):
+    import quantized_gemm_gb300 as qg
+    x, wq, gi = d["input"], d["weights_q"], d["group_indices"]
+    M, K = x.shape
+    S, N = gi.shape[1], wq.shape[2]
+    yo = torch.empty((M, S, N), dtype=x.dtype, device=x.device)
+    args = (x, wq, d["w_scale"], d["w_zero_point"], d["block_size"], gi)
+    ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*args), dtype=torch.uint8, device=x.device)
+    ms, _ = time_loop(lambda: qg.mm_grouped_matmul_qweights(*args, d["bias"], out=yo, workspace=ws), 10, 3, world,
+                      stream)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    tf = 2 * M * S * K * N / ms / 1e9
+    res = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor", "peak_tflops": peak,
+           "frac": tf / peak, "kernels_per_call": 4, "l2": "weights (3.8 GB int8) larger than L2",
+           "types": "input %s, weights int8, block %s" % (x.dtype, d["block_size"] or "K")}
+    del d, x, wq, gi, yo, ws
     torch.cuda.empty_cache()
     return res
 
@@ -539,6 +564,13 @@ def run_profile_workload(args):
         yq = torch.empty(tuple(d["a"].shape[:-1]) + (d["b"].shape[-1],), dtype=d["y_zero_point"].dtype, device=dev)
         ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
         step = lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws)
+    elif name.startswith("grouped_qweights"):
+        block = int(name.split("_b")[1]) if "_b" in name else 0   # grouped_qweights_b128: blocks of 128 rows
+        d = workloads.grouped_qweights(device=dev, block=block)
+        yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
+        qargs = (d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"], d["block_size"], d["group_indices"])
+        ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*qargs), dtype=torch.uint8, device=dev)
+        step = lambda: qg.mm_grouped_matmul_qweights(*qargs, d["bias"], out=yo, workspace=ws)
     elif name.startswith("grouped_bf16"):
         G = int(name.split("_g")[1]) if "_g" in name else 64     # grouped_bf16_g8: fewer groups, same M,K,N
         d = workloads.grouped_bf16(device=dev, G=G)

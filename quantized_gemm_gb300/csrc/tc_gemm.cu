@@ -83,6 +83,8 @@ constexpr int kQStages = 4;
 constexpr int kQTileBytes = 64 * 128, kQScaleOff = kQTileBytes, kQZeroOff = kQScaleOff + 256;
 constexpr int kQStageBytes = 9216;
 constexpr int kConvWarps = 4;                    // kGroupedQ converter warps (one per SM sub-partition)
+constexpr int kSignalBytes = 16;                 // per converter warp and k-block (see run_convert)
+constexpr int kSignalOff = 240;                  // 16 spare bytes of the control block: signal source/target
 
 __host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedQ; }
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
@@ -111,7 +113,8 @@ struct Cfg {
                                                   : Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes) +
                                1024;
   static_assert(kSmem <= 232448, "shared memory per block");
-  static_assert(16 * Geo<MODE, PAIR>::kStages + 48 + 16 * kQStages <= kCtrlBytes, "control block");
+  static_assert(16 * Geo<MODE, PAIR>::kStages + 48 + (MODE == kGroupedQ ? 16 * kQStages : 0) <= kSignalOff,
+                "control block");
   static_assert(MODE != kGroupedQ || PAIR, "the fused dequantisation runs on CTA pairs");
 };
 
@@ -233,7 +236,7 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
         // rows) in the staging ring, and the converter warps write it to sb.
         if (!mbar_wait(qempty0 + 8 * qstage, qphase ^ 1, abort, p.status, p.timeout_ns)) goto done;
         const uint32_t qfull = qfull0 + 8 * qstage, qs = qbase + qstage * kQStageBytes;
-        if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kABytes);
+        if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kABytes + 2 * kConvWarps * kSignalBytes);
         tma_load_3d_pair(sa, tmA, k0, ar, ti.a_b, mapa_shared(full, 0));
         const int32_t kq = kb / p.kb_per_q;
         mbar_arrive_expect_tx(qfull, kQTileBytes + 256 + (p.wzp_present ? 128 : 0));
@@ -437,12 +440,12 @@ __device__ __forceinline__ uint32_t requant_byte_fast(int32_t acc, float sa, flo
 
 // ------------------------------------------------------------------ dequantising converters (kGroupedQ)
 
-// Four warps (128 threads) per CTA turn each k-block's int8/uint8 weight tile
+// kConvWarps warps per CTA turn each k-block's int8/uint8 weight tile
 // (64 k x this CTA's 128 columns, in the staging ring) into the MMA's B
 // operand: W = T((q - zp) * scale), rounded once to bf16/f16, written in the
 // MN-major 128-byte-swizzled layout a TMA load would give (two 64-column
 // sub-tiles; the 16-byte chunk c of row k sits at chunk c ^ (k % 8)).  Thread t
-// owns columns 8*(t%16) .. +7 and rows t/16 + 8*i.  The difference q - zp is
+// owns columns 8*(t%16) .. +7 and rows t/16 + R*i, R = 2*kConvWarps.  q - zp is
 // formed exactly in fp32: the byte placed in the low mantissa of 2^23 (after
 // adding 128 to int8 values) minus 2^23 + 128 + zp.  Its product with a bf16
 // or f16 scale has at most 9 + 11 significant bits, so it is exact too and the
@@ -450,8 +453,8 @@ __device__ __forceinline__ uint32_t requant_byte_fast(int32_t acc, float sa, flo
 // visible to the tensor cores, frees the staging slot and arrives on the
 // leader CTA's stage barrier, which the MMA waits on.
 template <int MODE, bool PAIR>
-__device__ void run_convert(const TcParams& p, uint32_t sbase, uint32_t full0, uint32_t qbase, uint32_t qfull0,
-                            uint32_t qempty0, volatile int* abort) {
+__device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, uint32_t full0, uint32_t qbase,
+                            uint32_t qfull0, uint32_t qempty0, uint32_t ctrl_u32, volatile int* abort) {
   using G = Geo<MODE, PAIR>;
   const int ct = (int)threadIdx.x - Cfg<MODE, PAIR>::kConvWarp0 * 32;
   const int lane = threadIdx.x & 31;
@@ -459,6 +462,9 @@ __device__ void run_convert(const TcParams& p, uint32_t sbase, uint32_t full0, u
   const int sub = cc >> 3, c = cc & 7;
   const uint32_t flip = p.w_signed ? 0x80808080u : 0u;
   const float zbias = 8388608.f + (p.w_signed ? 128.f : 0.f);
+  const bool f16 = p.out_f16 != 0;
+  // smem is the kernel's shared memory; sbase and qbase are shared addresses in it.
+  const uint32_t sm0 = smem_u32(smem);
   const int64_t total = total_tiles<MODE>(p);
   uint32_t stage = 0, qstage = 0, qphase = 0;
   Tile ti;
@@ -466,9 +472,17 @@ __device__ void run_convert(const TcParams& p, uint32_t sbase, uint32_t full0, u
   for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (!__all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qstage, qphase, abort, p.status, p.timeout_ns))) return;
-      const uint32_t qs = qbase + qstage * kQStageBytes;
-      const uint4 sraw = lds128(qs + kQScaleOff + cc * 16);
-      const uint2 zraw = p.wzp_present ? lds64(qs + kQZeroOff + cc * 8) : make_uint2(0u, 0u);
+      const uint8_t* qs = smem + (qbase - sm0) + qstage * kQStageBytes;
+      // All of this thread's staged bytes first (kRows rows x 8 bytes), then the
+      // arithmetic, then the stores: the loads overlap instead of each waiting
+      // for the previous chunk's store.
+      constexpr int kRowStep = 2 * kConvWarps, kRows = 64 / kRowStep;
+      uint2 raw[kRows];
+#pragma unroll
+      for (int i = 0; i < kRows; ++i)
+        raw[i] = *reinterpret_cast<const uint2*>(qs + (k_first + kRowStep * i) * 128 + cc * 8);
+      const uint4 sraw = *reinterpret_cast<const uint4*>(qs + kQScaleOff + cc * 16);
+      const uint2 zraw = p.wzp_present ? *reinterpret_cast<const uint2*>(qs + kQZeroOff + cc * 8) : make_uint2(0u, 0u);
       float sc[8], cz[8];
       {
         const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
@@ -476,34 +490,38 @@ __device__ void run_convert(const TcParams& p, uint32_t sbase, uint32_t full0, u
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const uint32_t h = (sw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-          sc[e] = p.out_f16 ? __half2float(__ushort_as_half((unsigned short)h)) : __uint_as_float(h << 16);
+          sc[e] = f16 ? __half2float(__ushort_as_half((unsigned short)h)) : __uint_as_float(h << 16);
           const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
           cz[e] = zbias + (float)(p.w_signed ? (int)(int8_t)zb : (int)zb);
         }
       }
-      const uint32_t bsm = sbase + stage * G::kStageBytes + G::kABytes + sub * 8192;
+      uint8_t* bsm = smem + (sbase - sm0) + stage * G::kStageBytes + G::kABytes + sub * 8192;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = k_first + 8 * i;
-        uint2 q = lds64(qs + k * 128 + cc * 8);
-        q.x ^= flip;
-        q.y ^= flip;
+      for (int i = 0; i < kRows; ++i) {
+        const int k = k_first + kRowStep * i;
+        const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
         uint32_t w[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) {
-          const uint32_t src = e2 < 2 ? q.x : q.y;
+          const uint32_t src = e2 < 2 ? qx : qy;
           const int b0 = (e2 & 1) * 2;
           const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
           const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
-          w[e2] = pack2(__fmul_rn(f0, sc[2 * e2]), __fmul_rn(f1, sc[2 * e2 + 1]), p.out_f16);
+          w[e2] = pack2(__fmul_rn(f0, sc[2 * e2]), __fmul_rn(f1, sc[2 * e2 + 1]), f16);
         }
-        sts128(bsm + k * 128 + ((c ^ (k & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+        *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      // Publish the stage: each lane orders its writes before the async
+      // proxy; then one 16-byte bulk copy into the leader CTA completes its
+      // bytes on the leader's stage barrier, which the MMA waits on.  (A
+      // cluster-scope release arrive did the same but held the warp for
+      // about 1100 cycles per k-block; the copy is issued without waiting.)
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(qempty0 + 8 * qstage);
-        mbar_arrive_cluster(mapa_shared(full0 + 8 * stage, 0));
+        bulk_copy_to_cluster(mapa_shared(ctrl_u32 + kSignalOff, 0), ctrl_u32 + kSignalOff, kSignalBytes,
+                             mapa_shared(full0 + 8 * stage, 0));
       }
       if (++stage == G::kStages) stage = 0;
       if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
@@ -755,10 +773,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    // kGroupedQ: a stage is full once the leader's producer has armed it (A
-    // bytes of both CTAs) and the converter warps of both CTAs have arrived.
+    // kGroupedQ: a stage is full once the leader's producer has armed it and
+    // both CTAs' A bytes and converter signals (below) have landed.
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, MODE == kGroupedQ ? 1 + 2 * kConvWarps : 1);
+      mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     if (MODE == kGroupedQ)
@@ -805,7 +823,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
                       (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
     run_epilogue<MODE, PAIR>(p, tmem, accf0, acce0, abort, stage);
   } else if (MODE == kGroupedQ) {
-    run_convert<MODE, PAIR>(p, sbase, full0, qbase, qfull0, qempty0, abort);
+    run_convert<MODE, PAIR>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
   }
   tc_fence_before();
   __syncthreads();

@@ -169,6 +169,17 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
+// cluster CTA's shared memory, completing its bytes on that CTA's mbarrier
+// (both given as cluster-window addresses).  Issued without waiting.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
 // Orders this thread's shared-memory writes (generic proxy) before later
 // reads by the tensor cores and TMA (async proxy).
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -139,3 +139,31 @@ def _grouped_check(d, seed):
     scale = oracle.grouped_abs_scale(x, w, gi_local, bias)
     got = to_np(out[toks][:, :, cols_t])
     assert max_rel_err(got, ref, scale) <= 1e-2
+
+
+@pytest.mark.parametrize("block", [0, 128])
+def test_grouped_qweights_sampled_tokens_and_columns(block):
+    """int8 weight-only experts at the GroupedMatMul workload's size, fused dequantization."""
+    d = workloads.grouped_qweights(device=DEV, block=block)
+    out = qg.mm_grouped_matmul_qweights(d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"],
+                                        d["block_size"], d["group_indices"], d["bias"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    toks = _rows(16384, 6, 9)
+    cols = np.sort(np.random.default_rng(10).choice(14336, size=512, replace=False))
+    gi = d["group_indices"][toks].cpu().numpy()
+    used = sorted(set(gi.ravel().tolist()))
+    gi_local = np.vectorize({g: j for j, g in enumerate(used)}.get)(gi).astype(np.int64)
+    used_t = torch.tensor(used, device=DEV)
+    cols_t = torch.from_numpy(cols).to(DEV)
+    wq = d["weights_q"][used_t][:, :, cols_t].cpu().numpy()
+    sc = to_np(d["w_scale"][used_t][:, :, cols_t])
+    zp = d["w_zero_point"][used_t][:, :, cols_t].cpu().numpy()
+    bias = to_np(d["bias"][used_t][:, cols_t])
+    x = to_np(d["input"][toks])
+    args = (x, wq, sc, zp, block, gi_local, bias, "bf16")
+    ref = oracle.grouped_matmul_qweights(*args)
+    scale = oracle.grouped_qweights_abs_scale(*args)
+    got = to_np(out[toks][:, :, cols_t])
+    assert max_rel_err(got, ref, scale) <= 1e-2
+

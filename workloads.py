@@ -31,7 +31,8 @@ Workloads (shapes and distributions as specified for the benchmark):
 
 Variants of 4 and 5 at the same sizes (``QLINEAR_VARIANTS``; ``grouped_bf16``
 with ``dtype`` float16 and int64 indices) cover the other operand types,
-float16 scales and batch-indexed quantisation parameters.
+float16 scales and batch-indexed quantisation parameters; ``grouped_qweights``
+is the GroupedMatMul workload with int8 weight-only quantized experts.
 """
 
 import json
@@ -173,3 +174,25 @@ def grouped_bf16(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, dty
         "bias": normal((G, N), device, seed + 2, 0.1, dtype),
         "group_indices": zipf_two_distinct(M, G, S, 1.1, device, seed + 3, index_dtype),
     }
+
+
+def grouped_qweights(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, block=0, dtype=torch.bfloat16):
+    """The GroupedMatMul workload with weight-only int8 experts.
+
+    Same input, routing and bias as ``grouped_bf16``; weights_q int8 [G,K,N]
+    uniform on {-128..127}, zero points int8 uniform on {-8..8} and scales
+    uniform on (1.5e-4, 2.7e-4) rounded to ``dtype``, one per group and output
+    column (block 0) or per ``block`` rows of K, so that the dequantized
+    weights have about the standard deviation 1/64 of the bf16 workload.
+    """
+    kb = 1 if block == 0 else -(-K // block)
+    return {
+        "input": normal((M, K), device, seed, 1.0, dtype),
+        "weights_q": uniform_int((G, K, N), -128, 127, torch.int8, device, seed + 1),
+        "w_scale": uniform((G, kb, N), 1.5e-4, 2.7e-4, device, seed + 4, dtype),
+        "w_zero_point": uniform_int((G, kb, N), -8, 8, torch.int8, device, seed + 5),
+        "block_size": block,
+        "bias": normal((G, N), device, seed + 2, 0.1, dtype),
+        "group_indices": zipf_two_distinct(M, G, S, 1.1, device, seed + 3),
+    }
+
