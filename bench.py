@@ -273,6 +273,21 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
                          "l2": "flushed between iterations"}
     del d, Y1, Y2
 
+    # 2b. The headline Gemm in fp32 (three tf32 tensor-core products per step).
+    d = workloads.gemm_bf16(device=dev, dtype=torch.float32)
+    Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
+    ms, _ = time_loop(lambda: qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], 0, 1, out=Yf), 10, 3, world,
+                      stream)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    tf = 2 * 8192 ** 3 / ms / 1e9
+    tf32_peak = bf16_peak * 1.1 / 2.25      # measured bf16 peak x nominal dense tf32/bf16 (1.1 / 2.25 PFLOP/s)
+    out["gemm_f32"] = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor",
+                       "pipe": "tf32 x3 (hi*hi + hi*lo + lo*hi)", "peak_tflops": tf32_peak / 3,
+                       "frac": tf / (tf32_peak / 3), "kernels_per_call": 1,
+                       "peak_note": "measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25), / 3 products"}
+    del d, Yf
+    torch.cuda.empty_cache()
+
     # 3. bf16 batched MatMul A[8,32,2048,128] @ B[1,32,128,2048]: HBM-bound (2.15 GB output).
     d = workloads.matmul_bf16_bcast(device=dev)
     Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
@@ -554,6 +569,10 @@ def run_profile_workload(args):
     name = args.profile_workload
     if name == "gemm_bf16":
         _, _, step = gemm_case(dev)
+    elif name == "gemm_f32":
+        d = workloads.gemm_bf16(device=dev, dtype=torch.float32)
+        Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
+        step = lambda: qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], 0, 1, out=Yf)
     elif name == "matmul_bf16_bcast":
         d = workloads.matmul_bf16_bcast(device=dev)
         Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)

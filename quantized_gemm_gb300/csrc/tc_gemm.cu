@@ -68,11 +68,14 @@ constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
 template <int MODE, bool PAIR>
 struct Geo {
   static constexpr int kBRows = PAIR ? BN / 2 : BN;     // B columns (rows of B') held by one CTA
-  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kABytes = BM * BK * 2;           // 128 rows x 128 bytes (64 x 16-bit or 32 x fp32)
   static constexpr int kBBytes = kBRows * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  // kTF32: each stage holds the loaded (then high) parts of A and B followed
+  // by their low parts at kLoOff.
+  static constexpr int kLoOff = MODE == kTF32 ? kABytes + kBBytes : 0;
+  static constexpr int kStageBytes = (kABytes + kBBytes) * (MODE == kTF32 ? 2 : 1);
   // kGroupedQ gives one stage's worth of shared memory to its int8 staging ring.
-  static constexpr int kStages = PAIR ? (MODE == kGroupedQ ? 5 : 6) : 4;
+  static constexpr int kStages = MODE == kTF32 ? (PAIR ? 3 : 2) : PAIR ? (MODE == kGroupedQ ? 5 : 6) : 4;
   static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
@@ -100,12 +103,12 @@ constexpr int kStageWords = 32 * 16;             // float per-warp output stagin
 // warps of 128 columns plus 4 converter warps (14 warps: 128 registers).
 template <int MODE, bool PAIR>
 struct Cfg {
-  static constexpr int kEpiWarps = MODE == kGroupedQ ? 8 : 16;
-  static constexpr int kConv = MODE == kGroupedQ ? kConvWarps : 0;
+  static constexpr int kEpiWarps = (MODE == kGroupedQ || MODE == kTF32) ? 8 : 16;
+  static constexpr int kConv = (MODE == kGroupedQ || MODE == kTF32) ? kConvWarps : 0;
   static constexpr int kConvWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps + kConv) * 32;
   static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
-  static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : kStageWords;
+  static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : MODE == kTF32 ? 0 : kStageWords;
   static constexpr int kEpiBytes = kEpiWarps * kWarpWords * 4;
   // kGroupedQ staging ring, after the epilogue's slices (1024-byte aligned)
   static constexpr int kQOff = (Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes + 1023) / 1024 * 1024;
@@ -113,7 +116,9 @@ struct Cfg {
                                                   : Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes) +
                                1024;
   static_assert(kSmem <= 232448, "shared memory per block");
-  static_assert(16 * Geo<MODE, PAIR>::kStages + 48 + (MODE == kGroupedQ ? 16 * kQStages : 0) <= kSignalOff,
+  static_assert(16 * Geo<MODE, PAIR>::kStages + 48 +
+                        (MODE == kGroupedQ ? 16 * kQStages : MODE == kTF32 ? 8 * Geo<MODE, PAIR>::kStages : 0) <=
+                    kSignalOff,
                 "control block");
   static_assert(MODE != kGroupedQ || PAIR, "the fused dequantisation runs on CTA pairs");
 };
@@ -229,9 +234,19 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
       if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.status, p.timeout_ns)) goto done;
       const uint32_t full = full0 + 8 * stage;
       const uint32_t sa = sbase + stage * G::kStageBytes, sb = sa + G::kABytes;
-      const int32_t k0 = kb * BK;
+      const int32_t k0 = kb * (MODE == kTF32 ? 32 : BK);
       const int32_t ar = ti.a_row + arow_off, bc = (int32_t)ti.n0 + bcol_off;
-      if (MODE == kGroupedQ) {
+      if (MODE == kTF32) {
+        // fp32 tiles land on this CTA's own "loaded" barrier; the converter
+        // warps split them and then arm the stage (see run_split).
+        const uint32_t ld = qfull0 + 8 * stage;
+        if (PAIR && rank == 0) mbar_arrive_expect_tx(full, 2 * kConvWarps * kSignalBytes);
+        mbar_arrive_expect_tx(ld, G::kABytes + G::kBBytes);
+        tma_load_3d(sa, tmA, k0, ar, ti.a_b, ld);
+        tma_load_3d(sb, tmB, k0, bc, ti.b_b, ld);
+        qpending |= 1u << stage;
+        qpend_parity = (qpend_parity & ~(1u << stage)) | (phase << stage);
+      } else if (MODE == kGroupedQ) {
         // A as usual; the B half arrives as int8 (plus its scale and zero-point
         // rows) in the staging ring, and the converter warps write it to sb.
         if (!mbar_wait(qempty0 + 8 * qstage, qphase ^ 1, abort, p.status, p.timeout_ns)) goto done;
@@ -297,8 +312,8 @@ done:
         if (PAIR) mbar_wait_teardown_cluster(full0 + 8 * s, (pend_parity >> s) & 1u, left());
         else mbar_wait_teardown(full0 + 8 * s, (pend_parity >> s) & 1u, left());
       }
-  if (MODE == kGroupedQ)
-    for (int s = 0; s < kQStages; ++s)
+  if (MODE == kGroupedQ || MODE == kTF32)
+    for (int s = 0; s < (MODE == kTF32 ? G::kStages : kQStages); ++s)
       if (qpending & (1u << s)) mbar_wait_teardown(qfull0 + 8 * s, (qpend_parity >> s) & 1u, left());
 }
 
@@ -337,8 +352,25 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
           const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
           const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
           const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-          if (PAIR) tc_mma_f16_pair(d, ad, bd, p.idesc, acc);
-          else tc_mma_f16(d, ad, bd, p.idesc, acc);
+          if (MODE == kTF32) {
+            // 8 fp32 of k per instruction: lo*hi and hi*lo (the small terms
+            // first), then hi*hi.
+            const uint64_t adl = smem_desc_sw128(sa + G::kLoOff + k * 32, 16, 1024);
+            const uint64_t bdl = smem_desc_sw128(sb + G::kLoOff + k * 32, 16, 1024);
+            if (PAIR) {
+              tc_mma_tf32_pair(d, adl, bd, p.idesc, acc);
+              tc_mma_tf32_pair(d, ad, bdl, p.idesc, 1u);
+              tc_mma_tf32_pair(d, ad, bd, p.idesc, 1u);
+            } else {
+              tc_mma_tf32(d, adl, bd, p.idesc, acc);
+              tc_mma_tf32(d, ad, bdl, p.idesc, 1u);
+              tc_mma_tf32(d, ad, bd, p.idesc, 1u);
+            }
+          } else if (PAIR) {
+            tc_mma_f16_pair(d, ad, bd, p.idesc, acc);
+          } else {
+            tc_mma_f16(d, ad, bd, p.idesc, acc);
+          }
         }
         if (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
         else tc_commit(empty0 + 8 * stage);
@@ -525,6 +557,67 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
       }
       if (++stage == G::kStages) stage = 0;
       if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ fp32 splitting converters (kTF32)
+
+// Four warps per CTA turn each loaded fp32 k-block (A and this CTA's part of
+// B, 32 values of k per 128-byte row, 128-byte swizzled) into two tf32
+// operands in place: hi = tf32(x) overwrites x and lo = tf32(x - hi) goes to
+// the same offset of the low-part buffer, so both keep the loaded layout.
+// x - hi is exact in fp32, and ab - (hi_a hi_b + hi_a lo_b + lo_a hi_b) is at
+// most about 3 * 2^-22 |ab|.  The stage is then published to the MMA as in
+// run_convert (bulk-copy signals for a pair; plain arrivals for one CTA).
+template <int MODE, bool PAIR>
+__device__ void run_split(const TcParams& p, uint8_t* smem, uint32_t sbase, uint32_t full0, uint32_t ld0,
+                          uint32_t ctrl_u32, volatile int* abort) {
+  using G = Geo<MODE, PAIR>;
+  constexpr int kThr = kConvWarps * 32;
+  constexpr int kChunks = (G::kABytes + G::kBBytes) / 16;   // 16-byte pieces per stage
+  constexpr int kBatchN = 8;
+  static_assert(kChunks % (kThr * kBatchN) == 0, "split work per thread");
+  const int ct = (int)threadIdx.x - Cfg<MODE, PAIR>::kConvWarp0 * 32;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sm0 = smem_u32(smem);
+  const int64_t total = total_tiles<MODE>(p);
+  uint32_t stage = 0, phase = 0;
+  Tile ti;
+  int gh = 0;
+  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      if (!__all_sync(0xffffffffu, mbar_wait(ld0 + 8 * stage, phase, abort, p.status, p.timeout_ns))) return;
+      uint8_t* st = smem + (sbase - sm0) + stage * G::kStageBytes;
+#pragma unroll 1
+      for (int j0 = ct; j0 < kChunks; j0 += kThr * kBatchN) {
+        float4 x[kBatchN];
+#pragma unroll
+        for (int u = 0; u < kBatchN; ++u) x[u] = *reinterpret_cast<const float4*>(st + (j0 + u * kThr) * 16);
+#pragma unroll
+        for (int u = 0; u < kBatchN; ++u) {
+          const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = cvt_tf32(v[e]);
+            lo[e] = cvt_tf32(__fsub_rn(v[e], __uint_as_float(hi[e])));
+          }
+          uint8_t* q = st + (j0 + u * kThr) * 16;
+          *reinterpret_cast<uint4*>(q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(q + G::kLoOff) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR)
+          bulk_copy_to_cluster(mapa_shared(ctrl_u32 + kSignalOff, 0), ctrl_u32 + kSignalOff, kSignalBytes,
+                               mapa_shared(full0 + 8 * stage, 0));
+        else
+          mbar_arrive(full0 + 8 * stage);
+      }
+      if (++stage == G::kStages) { stage = 0; phase ^= 1; }
     }
   }
 }
@@ -717,6 +810,33 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         for (int h = 0; h < 2; ++h) {
           const int64_t n = ncol0 + q64 * 64 + 32 * h;
           if (n >= p.N) break;
+          if constexpr (MODE == kTF32) {
+            // fp32 output: each thread writes its row's 32 values (128 bytes).
+            if (row_ok) {
+              const int64_t m = ti.m0 + row_off + rloc;
+              float* yf = static_cast<float*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
+              const float* cf = p.c ? static_cast<const float*>(p.c) + batch_off(p, p.c_bstride, ti.batch) +
+                                          m * p.c_rs
+                                    : nullptr;
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                v[j] = p.alpha * __uint_as_float(r[h][j]);
+                if (cf && n + j < p.N) v[j] = __fmaf_rn(p.beta, cf[(n + j) * p.c_cs], v[j]);
+              }
+              if (p.y_vec && n + 32 <= p.N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  *reinterpret_cast<float4*>(yf + n + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                                           v[4 * q + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n + j < p.N) yf[n + j] = v[j];
+              }
+            }
+            continue;
+          }
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
@@ -775,10 +895,13 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   if (threadIdx.x == 0) {
     // kGroupedQ: a stage is full once the leader's producer has armed it and
     // both CTAs' A bytes and converter signals (below) have landed.
+    // kTF32 on one CTA: the converter warps' arrivals fill the stage.
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, (MODE == kTF32 && !PAIR) ? kConvWarps : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    if (MODE == kTF32)
+      for (int s = 0; s < S; ++s) mbar_init(qfull0 + 8 * s, 1);
     if (MODE == kGroupedQ)
       for (int s = 0; s < kQStages; ++s) {
         mbar_init(qfull0 + 8 * s, 1);
@@ -824,6 +947,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
     run_epilogue<MODE, PAIR>(p, tmem, accf0, acce0, abort, stage);
   } else if (MODE == kGroupedQ) {
     run_convert<MODE, PAIR>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
+  } else if (MODE == kTF32) {
+    run_split<MODE, PAIR>(p, smem_raw, sbase, full0, qfull0, cbase, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -890,7 +1015,7 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
   int64_t nbat = 1;
   for (int d = 0; d < kMaxBatchDims; ++d) out->bc[d] = 0;
   if (unit != 0) {
-    if (unit % 8) return false;
+    if (unit % (dtype == MM_F32 ? 4 : 8)) return false;
     int64_t maxc = 0;
     for (int d = 0; d < bm.nb; ++d)
       if (bm.shape[d] > 1 && bstride[d] != 0) {
@@ -900,11 +1025,24 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
     nbat = maxc + 1;
     if (nbat > 0x7fffffffLL) return false;
   }
-  const CUtensorMapDataType dt = dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[3];
   cuuint64_t strides[2];
   cuuint32_t box[3];
   const cuuint32_t estr[3] = {1, 1, 1};
+  if (dtype == MM_F32) {
+    // fp32 (three-tf32 products): K-major only, 32-element (128-byte) k boxes.
+    if (!(k_stride == 1 && mn_stride > 0 && mn_stride % 4 == 0) || (unit % 4)) return false;
+    out->mn_major = 0;
+    dims[0] = (cuuint64_t)k_len; dims[1] = (cuuint64_t)mn_len; dims[2] = (cuuint64_t)nbat;
+    strides[0] = (cuuint64_t)mn_stride * 4;
+    strides[1] = unit != 0 ? (cuuint64_t)unit * 4 : (cuuint64_t)(((strides[0] * dims[1]) + 15) & ~15ull);
+    if (strides[0] >= (1ull << 40) || strides[1] >= (1ull << 40)) return false;
+    box[0] = 32; box[1] = (cuuint32_t)box_mn; box[2] = 1;
+    return encode(&out->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const CUtensorMapDataType dt = dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (k_stride == 1 && mn_stride > 0 && mn_stride % 8 == 0) {
     out->mn_major = 0;
     dims[0] = (cuuint64_t)k_len; dims[1] = (cuuint64_t)mn_len; dims[2] = (cuuint64_t)nbat;
@@ -953,6 +1091,12 @@ uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair) {
          | ((f16 ? 0u : 1u) << 10)              // B: f16 (0) / bf16 (1)
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
          | ((uint32_t)(BN >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// kind::tf32: A and B tf32 (format 2), D fp32, both K-major.
+uint32_t make_idesc_tf32(bool pair) {
+  const uint32_t m = pair ? 2 * BM : BM;
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) | ((m >> 4) << 24);
 }
 
 namespace {
@@ -1049,7 +1193,8 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
   p.a_mn = a.mn_major;
   p.b_mn = b.mn_major;
   for (int d = 0; d < kMaxBatchDims; ++d) { p.a_bc[d] = a.bc[d]; p.b_bc[d] = b.bc[d]; }
-  p.num_kb = (int)((p.K + BK - 1) / BK);
+  const int kb_elems = mode == kTF32 ? 32 : BK;   // k-block: one 128-byte row of the operand type
+  p.num_kb = (int)((p.K + kb_elems - 1) / kb_elems);
   int64_t work = 0;
   if (!is_grouped(mode)) {
     const int64_t rows = pair ? 2 * BM : BM;
@@ -1086,6 +1231,9 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
                   : launch_kernel<kGrouped, false>(a, b, ms, mz, p, work, stream);
     case kQLinear:   // single CTAs only: the product is bound by its epilogue
       return pair ? MM_ERR_UNSUPPORTED : launch_kernel<kQLinear, false>(a, b, ms, mz, p, work, stream);
+    case kTF32:
+      return pair ? launch_kernel<kTF32, true>(a, b, ms, mz, p, work, stream)
+                  : launch_kernel<kTF32, false>(a, b, ms, mz, p, work, stream);
     case kGroupedQ:  // CTA pairs only
       if (!pair || !s) return MM_ERR_UNSUPPORTED;
       return launch_kernel<kGroupedQ, true>(a, b, ms, mz, p, work, stream);
@@ -1116,7 +1264,7 @@ int sm_count_public() { return sm_count(); }
 namespace {
 
 bool plan_dense(const GemmArgs& g, bool pair, OperandPlan* a, OperandPlan* b) {
-  if (g.dtype != MM_BF16 && g.dtype != MM_F16) return false;
+  if (g.dtype != MM_BF16 && g.dtype != MM_F16 && g.dtype != MM_F32) return false;
   if (g.M < 2 || g.N < 2 || g.K < 1) return false;
   if (g.y.cs != 1) return false;
   if (!plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM, a)) return false;
@@ -1138,19 +1286,21 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.bm = g.bm;
   p.out_f16 = g.dtype == MM_F16;
+  p.out_f32 = g.dtype == MM_F32;
+  const int64_t vec = p.out_f32 ? 4 : 8;      // elements per 16 bytes
   p.y = const_cast<void*>(g.y.ptr);
   for (int d = 0; d < kMaxBatchDims; ++d) { p.y_bstride[d] = g.y.bstride[d]; p.c_bstride[d] = g.c.bstride[d]; }
   p.y_rs = g.y.rs;
-  p.y_vec = (reinterpret_cast<uintptr_t>(g.y.ptr) % 16 == 0) && (g.y.rs % 8 == 0);
-  for (int d = 0; d < g.bm.nb; ++d) p.y_vec = p.y_vec && (g.y.bstride[d] % 8 == 0);
+  p.y_vec = (reinterpret_cast<uintptr_t>(g.y.ptr) % 16 == 0) && (g.y.rs % vec == 0);
+  for (int d = 0; d < g.bm.nb; ++d) p.y_vec = p.y_vec && (g.y.bstride[d] % vec == 0);
   p.alpha = g.alpha;
   p.beta = g.beta;
   if (g.c.ptr) {
     p.c = g.c.ptr;
     p.c_rs = g.c.rs;
     p.c_cs = g.c.cs;
-    p.c_vec = g.c.cs == 1 && (reinterpret_cast<uintptr_t>(g.c.ptr) % 16 == 0) && (g.c.rs % 8 == 0);
-    for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % 8 == 0);
+    p.c_vec = g.c.cs == 1 && (reinterpret_cast<uintptr_t>(g.c.ptr) % 16 == 0) && (g.c.rs % vec == 0);
+    for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % vec == 0);
   }
   p.status = status;
   // CTA pairs (256-row tiles) for long-K products with more than one row tile;
@@ -1159,8 +1309,8 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
     const bool pair = attempt == 0;
     OperandPlan a, b;
     if (!plan_dense(g, pair, &a, &b)) return MM_ERR_UNSUPPORTED;
-    p.idesc = make_idesc(p.out_f16, a.mn_major, b.mn_major, pair);
-    const mm_status st = launch_tc(kDense, pair, a, b, p, stream);
+    p.idesc = p.out_f32 ? make_idesc_tf32(pair) : make_idesc(p.out_f16, a.mn_major, b.mn_major, pair);
+    const mm_status st = launch_tc(p.out_f32 ? kTF32 : kDense, pair, a, b, p, stream);
     if (st != MM_ERR_UNSUPPORTED || !pair) return st;
   }
   return MM_ERR_UNSUPPORTED;

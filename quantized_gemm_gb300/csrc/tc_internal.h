@@ -15,7 +15,9 @@ constexpr int kTileK = 64;    // one 128-byte swizzle row of 16-bit elements
 
 // kGroupedQ: GroupedMatMul whose weights arrive as int8/uint8 with scales and
 // zero points (DequantizeLinear fused into the mainloop; CTA pairs only).
-enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3 };
+// kTF32: fp32 MatMul / Gemm as three tf32 products (hi*hi + hi*lo + lo*hi of
+// each operand's split x = hi + lo, split in shared memory by converter warps).
+enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3, kTF32 = 4 };
 
 struct TcParams {
   int64_t M, N, K;
@@ -35,7 +37,7 @@ struct TcParams {
   void* y;
   int64_t y_bstride[kMaxBatchDims];
   int64_t y_rs;
-  int y_vec, out_f16;
+  int y_vec, out_f16, out_f32;
   // float epilogue: v = alpha*acc + beta*C
   float alpha, beta;
   const void* c;
@@ -77,6 +79,7 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
 bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int64_t d2, int64_t s1, int64_t s2,
                    int box0, int box1, OperandPlan* out);
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair);
+uint32_t make_idesc_tf32(bool pair);
 void init_params(TcParams* p);
 // Fills the tile bookkeeping and launches tc_gemm_kernel: one CTA per SM, or
 // (pair) 2-CTA clusters computing 256-row tiles with cta_group::2 MMAs.

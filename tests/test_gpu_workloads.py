@@ -50,6 +50,21 @@ def test_gemm_bf16_8192_sampled_rows():
     assert torch.isfinite(Y.float()).all()
 
 
+def test_gemm_f32_8192_sampled_rows():
+    """The headline Gemm in fp32: three-tf32 tensor-core products within 1e-5."""
+    d = workloads.gemm_bf16(device=DEV, dtype=torch.float32)
+    Y = qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], d["transA"], d["transB"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    rows = _rows(8192, 10, 11)
+    A = to_np(d["A"][rows])
+    B = to_np(d["B"])
+    C = to_np(d["C"])
+    kw = dict(alpha=d["alpha"], beta=d["beta"], transA=0, transB=1)
+    ref = oracle.gemm(A, B, C, **kw)
+    assert max_rel_err(to_np(Y[rows]), ref, oracle.gemm_abs_scale(A, B, C, **kw)) <= 1e-5
+
+
 def test_matmul_bf16_bcast_sampled():
     d = workloads.matmul_bf16_bcast(device=DEV)
     Y = qg.mm_matmul(d["A"], d["B"])

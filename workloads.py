@@ -95,12 +95,13 @@ def matmul_f32(device="cpu", seed=0):
     }
 
 
-def gemm_bf16(device="cuda", seed=0, M=8192, N=8192, K=8192):
+def gemm_bf16(device="cuda", seed=0, M=8192, N=8192, K=8192, dtype=torch.bfloat16):
+    """The headline Gemm; with dtype float32 the same draws kept in fp32."""
     std = 1.0 / math.sqrt(K)
     return {
-        "A": normal((M, K), device, seed, std, torch.bfloat16),
-        "B": normal((N, K), device, seed + 1, std, torch.bfloat16),   # stored [N, K]: transB = 1
-        "C": normal((1, N), device, seed + 2, 1.0, torch.bfloat16),
+        "A": normal((M, K), device, seed, std, dtype),
+        "B": normal((N, K), device, seed + 1, std, dtype),   # stored [N, K]: transB = 1
+        "C": normal((1, N), device, seed + 2, 1.0, dtype),
         "alpha": 0.5, "beta": 2.0, "transA": 0, "transB": 1,
     }
 
