@@ -107,9 +107,12 @@ mm_status mm_set_wait_limit_ns(uint64_t ns);
  * leading (batch) dimensions are right-aligned and broadcast (each pair equal
  * or containing a 1).  T is one of bf16, f16, f32, f64, i32, i64, u32, u64 and
  * is shared by A, B and Y.
- * Arithmetic: bf16/f16 and f32 accumulate in fp32 (f32 uses FFMA, never TF32),
- * f64 in fp64, then one round-to-nearest-even conversion to T; integer types
- * wrap modulo 2^n.  K = 0 gives zeros. */
+ * Arithmetic: bf16/f16 and f32 accumulate in fp32, f64 in fp64, then one
+ * round-to-nearest-even conversion to T; integer types wrap modulo 2^n.  f32
+ * never uses plain TF32: small or strided f32 products use FFMA, large ones
+ * with a unit-stride matrix dimension per operand use three tf32 tensor-core
+ * products (each operand split into tf32 high and low parts; relative error
+ * about 3 * 2^-22 per product, within the fp32 bound).  K = 0 gives zeros. */
 mm_status mm_matmul_output_shape(const mm_tensor* A, const mm_tensor* B,
                                  int32_t* out_ndim, int64_t* out_shape /* [MM_MAX_DIMS] */);
 mm_status mm_matmul(const mm_tensor* A, const mm_tensor* B, const mm_tensor* Y, void* stream);

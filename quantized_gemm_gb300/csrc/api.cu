@@ -165,6 +165,11 @@ int choose(bool tensor_ok, bool tensor_pays) {
 bool tensor_pays(int64_t M, int64_t N, int64_t K, int64_t batch) {
   return (double)M * (double)N * (double)K * (double)batch >= 2097152.0;
 }
+// fp32 runs as three tf32 products on the tensor cores: it needs 8x more work
+// than the 16-bit types before it beats the CUDA-core kernel.
+bool tensor_pays_dense(int dtype, int64_t M, int64_t N, int64_t K, int64_t batch) {
+  return dtype == MM_F32 ? tensor_pays(M, N, K, 8 * batch) : tensor_pays(M, N, K, batch);
+}
 
 mm_status finish(mm_status s, int path) {
   if (s == MM_OK) g_last_path = path;
@@ -234,7 +239,7 @@ mm_status mm_matmul(const mm_tensor* A, const mm_tensor* B, const mm_tensor* Y, 
   g.alpha = 1.f; g.beta = 0.f; g.alpha_d = 1.0; g.beta_d = 0.0; g.alpha_i = 1; g.beta_i = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool tc_ok = tc_gemm_supported(g);
-  const int path = choose(tc_ok, tensor_pays(p.M, p.N, p.K, p.bm.count));
+  const int path = choose(tc_ok, tensor_pays_dense(g.dtype, p.M, p.N, p.K, p.bm.count));
   if (path < 0) return MM_ERR_UNSUPPORTED;
   if (path == MM_PATH_TENSOR) return finish(launch_tc_gemm(g, device_status_ptr(), st), MM_PATH_TENSOR);
   return finish(launch_simt_gemm(g, st), MM_PATH_SIMT);
@@ -301,7 +306,7 @@ mm_status mm_gemm(const mm_tensor* A, const mm_tensor* B, const mm_tensor* C, fl
   g.alpha = alpha; g.beta = beta; g.alpha_d = (double)alpha; g.beta_d = (double)beta;
   if (M == 0 || N == 0) return finish(MM_OK, MM_PATH_NONE);
   cudaStream_t stp = static_cast<cudaStream_t>(stream);
-  const int path = choose(tc_gemm_supported(g), tensor_pays(M, N, K, 1));
+  const int path = choose(tc_gemm_supported(g), tensor_pays_dense(g.dtype, M, N, K, 1));
   if (path < 0) return MM_ERR_UNSUPPORTED;
   if (path == MM_PATH_TENSOR) return finish(launch_tc_gemm(g, device_status_ptr(), stp), MM_PATH_TENSOR);
   return finish(launch_simt_gemm(g, stp), MM_PATH_SIMT);

@@ -242,8 +242,21 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
         const uint32_t ld = qfull0 + 8 * stage;
         if (PAIR && rank == 0) mbar_arrive_expect_tx(full, 2 * kConvWarps * kSignalBytes);
         mbar_arrive_expect_tx(ld, G::kABytes + G::kBBytes);
-        tma_load_3d(sa, tmA, k0, ar, ti.a_b, ld);
-        tma_load_3d(sb, tmB, k0, bc, ti.b_b, ld);
+        // K-major tiles load straight into the high-part buffer; MN-major
+        // tiles (32 x 32 boxes) into the low-part buffer, to be transposed.
+        if (!p.a_mn) {
+          tma_load_3d(sa, tmA, k0, ar, ti.a_b, ld);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BM / 32; ++j) tma_load_3d(sa + G::kLoOff + j * 4096, tmA, ar + 32 * j, k0, ti.a_b, ld);
+        }
+        if (!p.b_mn) {
+          tma_load_3d(sb, tmB, k0, bc, ti.b_b, ld);
+        } else {
+#pragma unroll
+          for (int j = 0; j < G::kBRows / 32; ++j)
+            tma_load_3d(sb + G::kLoOff + j * 4096, tmB, bc + 32 * j, k0, ti.b_b, ld);
+        }
         qpending |= 1u << stage;
         qpend_parity = (qpend_parity & ~(1u << stage)) | (phase << stage);
       } else if (MODE == kGroupedQ) {
@@ -349,8 +362,10 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
         for (int k = 0; k < BK / 16; ++k) {
           // K-major: advance 32 bytes inside the 128-byte swizzle row.
           // MN-major: advance two 8-row (1024-byte) swizzle atoms.
-          const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
+          // (kTF32 operands are K-major in shared memory whatever their layout in memory.)
+          const bool amn = MODE != kTF32 && p.a_mn, bmn = MODE != kTF32 && p.b_mn;
+          const uint64_t ad = amn ? smem_desc_sw128(sa + k * 2048, 8192, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = bmn ? smem_desc_sw128(sb + k * 2048, 8192, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
           const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
           if (MODE == kTF32) {
             // 8 fp32 of k per instruction: lo*hi and hi*lo (the small terms
@@ -570,44 +585,87 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
 // x - hi is exact in fp32, and ab - (hi_a hi_b + hi_a lo_b + lo_a hi_b) is at
 // most about 3 * 2^-22 |ab|.  The stage is then published to the MMA as in
 // run_convert (bulk-copy signals for a pair; plain arrivals for one CTA).
+// hi = tf32(x), lo = tf32(x - hi) for four values.
+__device__ __forceinline__ void split4(const float4& x, uint4& hi, uint4& lo) {
+  hi.x = cvt_tf32(x.x); lo.x = cvt_tf32(__fsub_rn(x.x, __uint_as_float(hi.x)));
+  hi.y = cvt_tf32(x.y); lo.y = cvt_tf32(__fsub_rn(x.y, __uint_as_float(hi.y)));
+  hi.z = cvt_tf32(x.z); lo.z = cvt_tf32(__fsub_rn(x.z, __uint_as_float(hi.z)));
+  hi.w = cvt_tf32(x.w); lo.w = cvt_tf32(__fsub_rn(x.w, __uint_as_float(hi.w)));
+}
+
 template <int MODE, bool PAIR>
 __device__ void run_split(const TcParams& p, uint8_t* smem, uint32_t sbase, uint32_t full0, uint32_t ld0,
                           uint32_t ctrl_u32, volatile int* abort) {
   using G = Geo<MODE, PAIR>;
   constexpr int kThr = kConvWarps * 32;
-  constexpr int kChunks = (G::kABytes + G::kBBytes) / 16;   // 16-byte pieces per stage
   constexpr int kBatchN = 8;
-  static_assert(kChunks % (kThr * kBatchN) == 0, "split work per thread");
   const int ct = (int)threadIdx.x - Cfg<MODE, PAIR>::kConvWarp0 * 32;
   const int lane = threadIdx.x & 31;
   const uint32_t sm0 = smem_u32(smem);
+  // K-major operand of `bytes` at `hi`: split each 16-byte piece in place,
+  // the low parts at the same offset + kLoOff.
+  auto split_k = [&](uint8_t* hi, int bytes) {
+#pragma unroll 1
+    for (int j0 = ct; j0 < bytes / 16; j0 += kThr * kBatchN) {
+      float4 x[kBatchN];
+#pragma unroll
+      for (int u = 0; u < kBatchN; ++u) x[u] = *reinterpret_cast<const float4*>(hi + (j0 + u * kThr) * 16);
+#pragma unroll
+      for (int u = 0; u < kBatchN; ++u) {
+        uint4 h, l;
+        split4(x[u], h, l);
+        uint8_t* q = hi + (j0 + u * kThr) * 16;
+        *reinterpret_cast<uint4*>(q) = h;
+        *reinterpret_cast<uint4*>(q + G::kLoOff) = l;
+      }
+    }
+  };
+  // MN-major operand of `boxes` 32 x 32 boxes loaded at hi + kLoOff (box j:
+  // k-row r of 128 bytes holds mn 32j..32j+31, 16-byte chunk c at c ^ (r % 8)).
+  // Written K-major: row mn of 128 bytes holds k 0..31, chunk c at c ^ (mn % 8).
+  // Box j's K-major rows (mn 32j..) occupy exactly its own bytes, so boxes are
+  // independent; within a pass of two boxes every thread reads its 4 x 4 block
+  // before any thread writes.
+  auto split_mn = [&](uint8_t* hi, int boxes) {
+    uint8_t* lo = hi + G::kLoOff;
+    const int kb4 = ct & 7, mb4 = (ct >> 3) & 7, half = ct >> 6;
+#pragma unroll 1
+    for (int pass = 0; pass < boxes / 2; ++pass) {
+      const int box = 2 * pass + half;
+      float4 x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 4 * kb4 + i;
+        x[i] = *reinterpret_cast<const float4*>(lo + box * 4096 + r * 128 + ((mb4 ^ (r & 7)) << 4));
+      }
+      bar1_sync(kThr);
+      const float t[4][4] = {{x[0].x, x[1].x, x[2].x, x[3].x}, {x[0].y, x[1].y, x[2].y, x[3].y},
+                             {x[0].z, x[1].z, x[2].z, x[3].z}, {x[0].w, x[1].w, x[2].w, x[3].w}};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int mn = 32 * box + 4 * mb4 + i;
+        uint4 h, l;
+        split4(make_float4(t[i][0], t[i][1], t[i][2], t[i][3]), h, l);
+        const int off = mn * 128 + ((kb4 ^ (mn & 7)) << 4);
+        *reinterpret_cast<uint4*>(hi + off) = h;
+        *reinterpret_cast<uint4*>(lo + off) = l;
+      }
+    }
+  };
   const int64_t total = total_tiles<MODE>(p);
   uint32_t stage = 0, phase = 0;
   Tile ti;
   int gh = 0;
   for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      if (!__all_sync(0xffffffffu, mbar_wait(ld0 + 8 * stage, phase, abort, p.status, p.timeout_ns))) return;
+      // One decision for all converter warps (they meet at named barriers).
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(ld0 + 8 * stage, phase, abort, p.status, p.timeout_ns));
+      if (!bar1_and(ok, kThr)) return;
       uint8_t* st = smem + (sbase - sm0) + stage * G::kStageBytes;
-#pragma unroll 1
-      for (int j0 = ct; j0 < kChunks; j0 += kThr * kBatchN) {
-        float4 x[kBatchN];
-#pragma unroll
-        for (int u = 0; u < kBatchN; ++u) x[u] = *reinterpret_cast<const float4*>(st + (j0 + u * kThr) * 16);
-#pragma unroll
-        for (int u = 0; u < kBatchN; ++u) {
-          const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hi[e] = cvt_tf32(v[e]);
-            lo[e] = cvt_tf32(__fsub_rn(v[e], __uint_as_float(hi[e])));
-          }
-          uint8_t* q = st + (j0 + u * kThr) * 16;
-          *reinterpret_cast<uint4*>(q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(q + G::kLoOff) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      }
+      if (p.a_mn) split_mn(st, BM / 32);
+      else split_k(st, G::kABytes);
+      if (p.b_mn) split_mn(st + G::kABytes, G::kBRows / 32);
+      else split_k(st + G::kABytes, G::kBBytes);
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
@@ -1030,14 +1088,27 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
   cuuint32_t box[3];
   const cuuint32_t estr[3] = {1, 1, 1};
   if (dtype == MM_F32) {
-    // fp32 (three-tf32 products): K-major only, 32-element (128-byte) k boxes.
-    if (!(k_stride == 1 && mn_stride > 0 && mn_stride % 4 == 0) || (unit % 4)) return false;
-    out->mn_major = 0;
-    dims[0] = (cuuint64_t)k_len; dims[1] = (cuuint64_t)mn_len; dims[2] = (cuuint64_t)nbat;
-    strides[0] = (cuuint64_t)mn_stride * 4;
+    // fp32 (three-tf32 products): K-major tiles as 32-element (128-byte) k
+    // boxes of box_mn rows; MN-major tiles as 32 x 32 boxes, transposed to
+    // K-major by the splitting converters.
+    if (unit % 4) return false;
+    if (k_stride == 1 && mn_stride > 0 && mn_stride % 4 == 0) {
+      out->mn_major = 0;
+      dims[0] = (cuuint64_t)k_len; dims[1] = (cuuint64_t)mn_len;
+      strides[0] = (cuuint64_t)mn_stride * 4;
+      box[0] = 32; box[1] = (cuuint32_t)box_mn;
+    } else if (mn_stride == 1 && k_stride > 0 && k_stride % 4 == 0) {
+      out->mn_major = 1;
+      dims[0] = (cuuint64_t)mn_len; dims[1] = (cuuint64_t)k_len;
+      strides[0] = (cuuint64_t)k_stride * 4;
+      box[0] = 32; box[1] = 32;
+    } else {
+      return false;
+    }
+    dims[2] = (cuuint64_t)nbat;
+    box[2] = 1;
     strides[1] = unit != 0 ? (cuuint64_t)unit * 4 : (cuuint64_t)(((strides[0] * dims[1]) + 15) & ~15ull);
     if (strides[0] >= (1ull << 40) || strides[1] >= (1ull << 40)) return false;
-    box[0] = 32; box[1] = (cuuint32_t)box_mn; box[2] = 1;
     return encode(&out->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

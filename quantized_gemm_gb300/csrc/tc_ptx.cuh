@@ -169,6 +169,21 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+// Named barrier 1 over `count` threads, returning whether `pred` held in all of them.
+__device__ __forceinline__ bool bar1_and(bool pred, int count) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(count)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar1_sync(int count) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); }
+
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
 // cluster CTA's shared memory, completing its bytes on that CTA's mbarrier
 // (both given as cluster-window addresses).  Issued without waiting.

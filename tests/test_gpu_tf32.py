@@ -1,7 +1,7 @@
 """fp32 MatMul / Gemm on the tensor cores as three tf32 products (each operand
 split x = hi + lo in shared memory; hi*hi + hi*lo + lo*hi), held to the same
 per-element bound as the fp32 CUDA-core path: 1e-5 of sum_k |a||b| (+|beta C|).
-The operands must be K-major (A row-major, B given as [N, K] rows)."""
+Operands may be K-major or MN-major (unit stride in one matrix dimension)."""
 
 import contextlib
 
@@ -86,9 +86,34 @@ def test_tf32x3_is_needed_for_the_bound():
     assert plain > 4 * TOL32 and ours <= TOL32 and ours < plain / 4
 
 
-def test_tf32x3_rejects_mn_major_b_under_forced_tensor_policy():
-    A = rand_tensor((256, 256), torch.float32, 66, DEV)
-    B = rand_tensor((256, 256), torch.float32, 67, DEV)           # row-major [K, N]: MN-major B
+@pytest.mark.parametrize("M,N,K", [(300, 264, 328), (260, 520, 1100)])
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 0), (1, 1)])
+def test_tf32x3_mn_major_operands(M, N, K, tA, tB):
+    # MN-major operands (row-major B of a MatMul, or A given transposed) are
+    # loaded as 32 x 32 boxes and transposed to K-major while being split.
+    A = rand_tensor((K, M) if tA else (M, K), torch.float32, 68, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), torch.float32, 69, DEV)
+    C = rand_tensor((M, 1), torch.float32, 70, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 1.25, -0.5, tA, tB)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    a, b, c = to_np(A), to_np(B), to_np(C)
+    kw = dict(alpha=1.25, beta=-0.5, transA=tA, transB=tB)
+    assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= TOL32
+
+
+def test_tf32x3_row_major_matmul_takes_the_tensor_path():
+    A = rand_tensor((512, 384), torch.float32, 71, DEV)
+    B = rand_tensor((384, 640), torch.float32, 72, DEV)           # row-major [K, N]
+    Y = qg.mm_matmul(A, B)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= TOL32
+
+
+def test_tf32x3_rejects_strided_operands_under_forced_tensor_policy():
+    A = rand_tensor((256, 512), torch.float32, 66, DEV)[:, ::2]   # neither dimension contiguous
+    B = rand_tensor((256, 256), torch.float32, 67, DEV)
     with tensor_path():
         with pytest.raises(qg.MMError) as e:
             qg.mm_matmul(A, B)
