@@ -584,8 +584,9 @@ def run_profile_workload(args):
         ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
         step = lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws)
     elif name.startswith("grouped_qweights"):
-        block = int(name.split("_b")[1]) if "_b" in name else 0   # grouped_qweights_b128: blocks of 128 rows
-        d = workloads.grouped_qweights(device=dev, block=block)
+        # grouped_qweights_b128: blocks of 128 rows; a _gN suffix: N groups (same M, K, N)
+        parts = dict((t[0], int(t[1:])) for t in name[len("grouped_qweights"):].split("_") if t)
+        d = workloads.grouped_qweights(device=dev, block=parts.get("b", 0), G=parts.get("g", 64))
         yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
         qargs = (d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"], d["block_size"], d["group_indices"])
         ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*qargs), dtype=torch.uint8, device=dev)
