@@ -28,8 +28,7 @@ Each module cites the page and section it follows:
 
 Parity status: every function here is pinned by tests in
 ``tests/test_oracle_pins.py`` (printed worked examples, brute force on tiny
-inputs, closed forms and identities); none is "parity unpinned" except the
-integer-Gemm corner with non-integral alpha/beta, which this oracle rejects.
+inputs, closed forms and identities); none is "parity unpinned".
 """
 
 from .matmul import matmul, matmul_output_shape, matmul_abs_scale

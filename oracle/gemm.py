@@ -21,9 +21,12 @@ Readings of points the page leaves open (each is listed in the design notes):
   and (M, N).
 * Float types: the contraction is done in float64 and Y is returned unrounded.
   alpha and beta are float32 attributes, widened exactly.
-* Integer types: alpha and beta must hold integral values; Y is then computed
-  exactly modulo 2**n of T.  Non-integral alpha/beta with an integer T is not
-  defined by the page and is rejected here (NotImplementedError).
+* Integer types with integral alpha and beta: Y is computed exactly modulo
+  2**n of T.  With a non-integral alpha or beta (the page does not say how a
+  real-valued result becomes a T): the product A' @ B' is taken modulo 2**n
+  as a T value, then r = alpha * acc + beta * C is evaluated in float64 (each
+  product rounded, then the sum) and truncated toward zero.  Results outside
+  T's range are undefined; the oracle raises ValueError for them.
 """
 
 import numpy as np
@@ -55,11 +58,25 @@ def _broadcast_c(C, M, N):
     return np.broadcast_to(C.reshape((1,) * (2 - C.ndim) + C.shape), (M, N))
 
 
-def _integral(x, name):
+def _is_integral(x):
     xf = float(np.float32(x))
-    if xf != np.floor(xf):
-        raise NotImplementedError("integer Gemm with non-integral %s=%r is not defined" % (name, x))
-    return int(xf)
+    return np.isfinite(xf) and xf == np.floor(xf)
+
+
+def _integer_gemm_real(P, A_dtype, C, alpha, beta, M, N):
+    """trunc(alpha * acc + beta * C) in float64 for an integer T (non-integral alpha/beta)."""
+    acc = from_u64(P, A_dtype).astype(np.float64)          # the wrapped T value, rounded to float64
+    r = np.float64(np.float32(alpha)) * acc
+    if C is not None:
+        r = r + np.float64(np.float32(beta)) * np.asarray(_broadcast_c(C, M, N)).astype(np.float64)
+    t = np.trunc(r)
+    bits = np.dtype(A_dtype).itemsize * 8
+    lo, hi = (-(2.0 ** (bits - 1)), 2.0 ** (bits - 1)) if np.issubdtype(A_dtype, np.signedinteger) else (0.0, 2.0 ** bits)
+    if not np.all((t >= lo) & (t < hi)):
+        raise ValueError("integer Gemm result outside the range of %s is undefined" % np.dtype(A_dtype))
+    if np.issubdtype(A_dtype, np.signedinteger):
+        return t.astype(np.int64).astype(A_dtype)
+    return np.array([int(v) for v in t.ravel()], dtype=np.uint64).reshape(t.shape).astype(A_dtype)
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=1.0, transA=0, transB=0):
@@ -72,9 +89,11 @@ def gemm(A, B, C=None, alpha=1.0, beta=1.0, transA=0, transB=0):
     if is_integer_dtype(A.dtype):
         if B.dtype != A.dtype or (C is not None and np.asarray(C).dtype != A.dtype):
             raise TypeError("Gemm operands must share one type T")
-        a_int = np.uint64(_integral(alpha, "alpha") % (1 << 64))
-        b_int = np.uint64(_integral(beta, "beta") % (1 << 64))
         P = np.matmul(to_u64(Ap), to_u64(Bp))  # uint64: wraps modulo 2**64
+        if not (_is_integral(alpha) and _is_integral(beta)):
+            return _integer_gemm_real(P, A.dtype, C, alpha, beta, M, N)
+        a_int = np.uint64(int(np.float32(alpha)) % (1 << 64))
+        b_int = np.uint64(int(np.float32(beta)) % (1 << 64))
         Y = a_int * P
         if C is not None:
             Y = Y + b_int * to_u64(_broadcast_c(C, M, N))

@@ -297,11 +297,14 @@ mm_status mm_gemm(const mm_tensor* A, const mm_tensor* B, const mm_tensor* C, fl
     g.c.ptr = C->data; g.c.rs = st[0]; g.c.cs = st[1];
   }
   if (is_int_type(A->dtype)) {
-    if (!std::isfinite(alpha) || !std::isfinite(beta) || alpha != std::floor(alpha) || beta != std::floor(beta) ||
-        std::fabs(alpha) >= 9.2e18f || std::fabs(beta) >= 9.2e18f)
-      return MM_ERR_UNSUPPORTED;
-    g.alpha_i = (uint64_t)(int64_t)alpha;
-    g.beta_i = (uint64_t)(int64_t)beta;
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) return MM_ERR_UNSUPPORTED;
+    if (alpha == std::floor(alpha) && beta == std::floor(beta) && std::fabs(alpha) < 9.2e18f &&
+        std::fabs(beta) < 9.2e18f) {
+      g.alpha_i = (uint64_t)(int64_t)alpha;     // exact modulo 2^n
+      g.beta_i = (uint64_t)(int64_t)beta;
+    } else {
+      g.int_float = 1;                          // fp64 evaluation, truncated toward zero
+    }
   }
   g.alpha = alpha; g.beta = beta; g.alpha_d = (double)alpha; g.beta_d = (double)beta;
   if (M == 0 || N == 0) return finish(MM_OK, MM_PATH_NONE);

@@ -19,6 +19,9 @@ struct GemmArgs {
   float alpha, beta;         // float types
   double alpha_d, beta_d;    // f64
   uint64_t alpha_i, beta_i;  // integer types: two's complement of the integral values
+  // Integer types with a non-integral alpha or beta: y = trunc(alpha*acc + beta*c)
+  // evaluated in fp64 (each product, then the sum, rounded once), saturated to T.
+  int int_float;
 };
 
 // QLinearMatMul.

@@ -80,8 +80,29 @@ template <> struct Epi<double> {
     return r;
   }
 };
+// Integer T.  Integral alpha and beta: exact modulo 2^n.  Otherwise (a reading
+// of the Gemm page, which leaves this open): the accumulator taken as a T value
+// and C widened to fp64, r = (alpha*acc) + (beta*c) with each product and the
+// sum rounded once in fp64, then truncated toward zero; the hardware's
+// round-toward-zero conversions saturate values outside T's range.
+template <typename T> __device__ __forceinline__ double int_to_f64(T x);
+template <> __device__ __forceinline__ double int_to_f64<int32_t>(int32_t x) { return (double)x; }
+template <> __device__ __forceinline__ double int_to_f64<uint32_t>(uint32_t x) { return (double)x; }
+template <> __device__ __forceinline__ double int_to_f64<int64_t>(int64_t x) { return __ll2double_rn(x); }
+template <> __device__ __forceinline__ double int_to_f64<uint64_t>(uint64_t x) { return __ull2double_rn(x); }
+template <typename T> __device__ __forceinline__ T f64_to_int_rz(double x);
+template <> __device__ __forceinline__ int32_t f64_to_int_rz<int32_t>(double x) { return __double2int_rz(x); }
+template <> __device__ __forceinline__ uint32_t f64_to_int_rz<uint32_t>(double x) { return __double2uint_rz(x); }
+template <> __device__ __forceinline__ int64_t f64_to_int_rz<int64_t>(double x) { return __double2ll_rz(x); }
+template <> __device__ __forceinline__ uint64_t f64_to_int_rz<uint64_t>(double x) { return __double2ull_rz(x); }
+
 template <typename T, typename U> struct EpiInt {
   static __device__ __forceinline__ U apply(const GemmArgs& p, U v, const T* c) {
+    if (p.int_float) {
+      double r = __dmul_rn(p.alpha_d, int_to_f64<T>((T)v));
+      if (c) r = __dadd_rn(r, __dmul_rn(p.beta_d, int_to_f64<T>(*c)));
+      return (U)f64_to_int_rz<T>(r);
+    }
     U r = (U)p.alpha_i * v;
     if (c) r += (U)p.beta_i * Arith<T>::load(c);
     return r;

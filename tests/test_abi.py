@@ -117,11 +117,11 @@ def test_validation_errors_before_any_launch(lib):
     bad = T((2,) * 8)
     bad.ndim = 9
     assert lib.mm_matmul(ref(bad), ref(B), ref(T((4, 16))), None) == 1
-    # Gemm: C not unidirectionally broadcastable, rank-3 operand, integer T with fractional alpha
+    # Gemm: C not unidirectionally broadcastable, rank-3 operand, integer T with a non-finite alpha
     assert lib.mm_gemm(ref(A), ref(B), ref(T((3, 16))), 1.0, 1.0, 0, 0, ref(T((4, 16))), None) == 2
     assert lib.mm_gemm(ref(T((1, 4, 8))), ref(B), None, 1.0, 1.0, 0, 0, ref(T((4, 16))), None) == 2
     Ai, Bi, Yi = T((4, 8), dtype=4), T((8, 16), dtype=4), T((4, 16), dtype=4)
-    assert lib.mm_gemm(ref(Ai), ref(Bi), None, 0.5, 1.0, 0, 0, ref(Yi), None) == 4
+    assert lib.mm_gemm(ref(Ai), ref(Bi), None, float("nan"), 1.0, 0, 0, ref(Yi), None) == 4
     # GroupedMatMul: types, shapes, bias shape
     x, w, gi = T((6, 8), 0), T((3, 8, 16), 0), T((6, 2), 4)
     out = T((6, 2, 16), 0)

@@ -278,3 +278,33 @@ def test_grouped_empty_and_page_examples():
     gi = torch.tensor([[0], [0], [2], [2]], dtype=torch.int64, device=DEV)
     out = qg.mm_grouped_matmul(x, w, gi)
     assert out.cpu().tolist() == [[[4, 7]], [[8, 15]], [[100, 111]], [[136, 151]]]
+
+
+@pytest.mark.parametrize("dtype", [np.int32, np.uint32, np.int64, np.uint64], ids=lambda t: np.dtype(t).name)
+@pytest.mark.parametrize("alpha,beta", [(0.37, -1.25), (-2.5, 0.5), (0.5, 1.0)])
+def test_gemm_integer_non_integral_alpha_beta(dtype, alpha, beta):
+    # trunc(alpha * acc + beta * C) in float64, the accumulator wrapped in T
+    # first (the integer-Gemm reading): bit-exact against the oracle on values
+    # that stay inside T's range.
+    g = np.random.default_rng(80)
+    lo = 0 if np.dtype(dtype).kind == "u" else -20
+    A = g.integers(lo, 21, (70, 33)).astype(dtype)
+    B = g.integers(lo, 21, (33, 45)).astype(dtype)
+    C = g.integers(lo, 21, (1, 45)).astype(dtype)
+    if np.dtype(dtype).kind == "u" and (alpha < 0 or beta < 0):
+        A, C = A // 4, C * 0          # keep unsigned results non-negative
+        alpha, beta = abs(alpha), abs(beta)
+    ref = oracle.gemm(A, B, C, alpha=alpha, beta=beta)
+    Y = qg.mm_gemm(from_np(A, DEV), from_np(B, DEV), from_np(C, DEV), alpha, beta, 0, 0)
+    assert qg.mm_last_path() == qg.MM_PATH_SIMT
+    assert np.array_equal(Y.cpu().numpy(), ref)
+
+
+def test_gemm_integer_non_integral_saturates():
+    # Outside T's range the reading leaves the value undefined; the kernels saturate.
+    A = from_np(np.array([[2 ** 31 - 1, 2 ** 31 - 1]], np.int32), DEV)
+    B = from_np(np.array([[1], [-1]], np.int32), DEV)
+    Y = qg.mm_gemm(A, B, None, 1.5, 1.0, 0, 0)                     # acc = 0 -> 0
+    assert Y.item() == 0
+    Y = qg.mm_gemm(A[:, :1], B[:1], None, 1.5, 1.0, 0, 0)          # 1.5 * (2^31 - 1) > 2^31 - 1
+    assert Y.item() == 2 ** 31 - 1

@@ -345,7 +345,7 @@ def test_gemm_brute_force(tA, tB, c_shape):
     assert np.array_equal(got, want)
 
 
-def test_gemm_integer_exact_and_non_integral_rejected():
+def test_gemm_integer_exact():
     A = np.array([[2 ** 31 - 1, 1]], np.int32)
     B = np.array([[1], [1]], np.int32)
     C = np.array([[5]], np.int32)
@@ -353,8 +353,30 @@ def test_gemm_integer_exact_and_non_integral_rejected():
     got = oracle.gemm(A, B, C, alpha=3.0, beta=-1.0)
     want = ((3 * 2 ** 31 - 5) + 2 ** 31) % 2 ** 32 - 2 ** 31
     assert got.item() == want
-    with pytest.raises(NotImplementedError):
-        oracle.gemm(A, B, C, alpha=0.5)
+
+
+def test_gemm_integer_non_integral_alpha_beta():
+    # The accumulator wraps in T first: A @ B = 2^31 is the int32 -2^31, so
+    # 0.5 * acc + (-1) * 5 = -2^30 - 5.
+    A = np.array([[2 ** 31 - 1, 1]], np.int32)
+    B = np.array([[1], [1]], np.int32)
+    C = np.array([[5]], np.int32)
+    assert oracle.gemm(A, B, C, alpha=0.5, beta=-1.0).item() == -(2 ** 30) - 5
+    # truncation toward zero: acc = +-3, alpha 0.5 -> +-1.5; with beta 0.25 and C = +-7 -> +-3.25
+    A2 = np.array([[1, 2], [-1, -2]], np.int32)
+    B2 = np.array([[1], [1]], np.int32)
+    assert oracle.gemm(A2, B2, None, alpha=0.5).ravel().tolist() == [1, -1]
+    C2 = np.array([[7], [-7]], np.int32)
+    assert oracle.gemm(A2, B2, C2, alpha=0.5, beta=0.25).ravel().tolist() == [3, -3]
+    # unsigned: 5 * float32(0.3) = 1.50000006 -> 1
+    U = np.array([[5]], np.uint32)
+    assert oracle.gemm(U, np.array([[1]], np.uint32), None, alpha=0.3).item() == 1
+    # int64: the accumulator is rounded to float64 first: 2^54 + 3 -> 2^54 + 4, times 0.5
+    L = np.array([[2 ** 54 + 3]], np.int64)
+    assert oracle.gemm(L, np.array([[1]], np.int64), None, alpha=0.5).item() == 2 ** 53 + 2
+    # results outside T's range are undefined: rejected
+    with pytest.raises(ValueError):
+        oracle.gemm(np.array([[2 ** 31 - 1]], np.int32), np.array([[1]], np.int32), None, alpha=1.5)
 
 
 def test_gemm_transpose_identity():
