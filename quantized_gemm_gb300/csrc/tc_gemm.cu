@@ -509,6 +509,7 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
   const int sub = cc >> 3, c = cc & 7;
   const uint32_t flip = p.w_signed ? 0x80808080u : 0u;
   const float zbias = 8388608.f + (p.w_signed ? 128.f : 0.f);
+  const float hbias = 1024.f + (p.w_signed ? 128.f : 0.f);
   const bool f16 = p.out_f16 != 0;
   // smem is the kernel's shared memory; sbase and qbase are shared addresses in it.
   const uint32_t sm0 = smem_u32(smem);
@@ -530,33 +531,65 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
         raw[i] = *reinterpret_cast<const uint2*>(qs + (k_first + kRowStep * i) * 128 + cc * 8);
       const uint4 sraw = *reinterpret_cast<const uint4*>(qs + kQScaleOff + cc * 16);
       const uint2 zraw = p.wzp_present ? *reinterpret_cast<const uint2*>(qs + kQZeroOff + cc * 8) : make_uint2(0u, 0u);
-      float sc[8], cz[8];
-      {
-        const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
-        const uint32_t zw[2] = {zraw.x, zraw.y};
+      // Per column pair e2: the scales as staged (a bf16/f16 pair) and the
+      // zero-point bias cz = bias + zp, in fp32 (bf16) or as an f16 pair.
+      const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
+      const uint32_t zw[2] = {zraw.x, zraw.y};
+      int zp[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t h = (sw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-          sc[e] = f16 ? __half2float(__ushort_as_half((unsigned short)h)) : __uint_as_float(h << 16);
-          const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-          cz[e] = zbias + (float)(p.w_signed ? (int)(int8_t)zb : (int)zb);
-        }
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+        zp[e] = p.w_signed ? (int)(int8_t)zb : (int)zb;
       }
       uint8_t* bsm = smem + (sbase - sm0) + stage * G::kStageBytes + G::kABytes + sub * 8192;
+      if (f16) {
+        // 1024 + u as f16 (byte u in the low mantissa of 0x6400) minus
+        // 1024 + 128*signed + zp is q - zp exactly (all below 2048); the f16
+        // pair product is rounded once.
+        __half2 czh[4];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const int k = k_first + kRowStep * i;
-        const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
-        uint32_t w[4];
+        for (int e2 = 0; e2 < 4; ++e2)
+          czh[e2] = __floats2half2_rn(hbias + (float)zp[2 * e2], hbias + (float)zp[2 * e2 + 1]);
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const uint32_t src = e2 < 2 ? qx : qy;
-          const int b0 = (e2 & 1) * 2;
-          const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
-          const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
-          w[e2] = pack2(__fmul_rn(f0, sc[2 * e2]), __fmul_rn(f1, sc[2 * e2 + 1]), f16);
+        for (int i = 0; i < kRows; ++i) {
+          const int k = k_first + kRowStep * i;
+          const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+          uint32_t w[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const uint32_t src = e2 < 2 ? qx : qy;
+            const uint32_t hv = __byte_perm(src, 0x64u, (e2 & 1) ? 0x4342u : 0x4140u);
+            const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&hv), czh[e2]);
+            const __half2 y = __hmul2(d, *reinterpret_cast<const __half2*>(&sw[e2]));
+            w[e2] = *reinterpret_cast<const uint32_t*>(&y);
+          }
+          *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        // q - zp exactly in fp32; an integer of at most 8 significant bits, so
+        // its bf16 is the upper half of the fp32 pattern; the bf16 pair product
+        // is rounded once.
+        float cz[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cz[e] = zbias + (float)zp[e];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const int k = k_first + kRowStep * i;
+          const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+          uint32_t w[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const uint32_t src = e2 < 2 ? qx : qy;
+            const int b0 = (e2 & 1) * 2;
+            const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
+            const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
+            const uint32_t dv = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+            const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dv),
+                                             *reinterpret_cast<const __nv_bfloat162*>(&sw[e2]));
+            w[e2] = *reinterpret_cast<const uint32_t*>(&y);
+          }
+          *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       // Publish the stage: each lane orders its writes before the async
       // proxy; then one 16-byte bulk copy into the leader CTA completes its
