@@ -25,7 +25,7 @@
 // issues the MMAs for both, and commits are multicast to the pair.  Each SM
 // then takes in 64 bytes of operands per MMA cycle instead of 96.
 //
-// Tiles are numbered in a grouped raster (bands of 16 row tiles, for L2 reuse)
+// Tiles are numbered in a grouped raster (bands of 8 row tiles, for L2 reuse)
 // and decoded with 32-bit multiply-shift division by precomputed divisors.
 //
 // Modes (template parameter):
@@ -79,7 +79,11 @@ struct Geo {
   static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
-constexpr int kGroupM = 16;                      // raster band height (tiles), a power of two
+// Raster band height (tiles, a power of two).  On the 8192^3 Gemm, bands of
+// 8 pair tiles read 1.08 GB from DRAM per call against 1.28 GB for 16 (4:
+// 1.41 GB, 32: 2.05 GB); under the power cap that traffic costs clock: 1620
+// against 1608 TFLOP/s over 1000 calls.
+constexpr int kGroupM = 8;
 // kGroupedQ staging ring (per CTA and stage): the int8 weight tile (64 k x 128
 // n), the k-block's scale row (128 x 16-bit) and zero-point row (128 bytes).
 constexpr int kQStages = 4;
