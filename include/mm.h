@@ -71,7 +71,7 @@ typedef struct mm_tensor {
 typedef enum mm_path {
   MM_PATH_AUTO = 0,    /* policy only: let the planner choose */
   MM_PATH_SIMT = 1,    /* CUDA-core kernels (every type, every stride pattern) */
-  MM_PATH_TENSOR = 2,  /* tcgen05 tensor-core kernels (bf16/f16 and 8-bit quantized operands) */
+  MM_PATH_TENSOR = 2,  /* tcgen05 tensor-core kernels (bf16/f16, fp32 as three tf32 products, 8-bit quantized operands) */
   MM_PATH_NONE = 3     /* result only: no kernel was needed (an empty output) */
 } mm_path;
 

@@ -1079,17 +1079,20 @@ int64_t gcd64(int64_t a, int64_t b) {
   return a;
 }
 
+// Per-device values cached on first use; host threads may race to fill an
+// entry, which is harmless (they compute the same value), so atomics suffice.
 int sm_count() {
-  static int counts[128] = {};
+  static std::atomic<int> counts[128];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128) return 148;
-  if (!counts[dev]) {
-    int c = 0;
+  int c = counts[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    counts[dev] = c > 0 ? c : 148;
+    if (c <= 0) c = 148;
+    counts[dev].store(c, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return c;
 }
 
 }  // namespace
@@ -1228,12 +1231,13 @@ namespace {
 // kernel, queried once per device (0 if none).
 template <int MODE>
 int max_pair_clusters() {
-  static int cache[128];
-  static bool done[128];
+  static std::atomic<int> cache[128];   // value + 1 once known (0: not yet queried)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128) return 0;
-  if (!done[dev]) {
+  const int known = cache[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known - 1;
+  {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1252,10 +1256,9 @@ int max_pair_clusters() {
       cudaGetLastError();
       n = 0;
     }
-    cache[dev] = n;
-    done[dev] = true;
+    cache[dev].store(n + 1, std::memory_order_relaxed);
+    return n;
   }
-  return cache[dev];
 }
 
 template <int MODE, bool PAIR>
