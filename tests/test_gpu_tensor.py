@@ -55,6 +55,23 @@ def test_gemm_tensor(dtype, tA, tB, M, N, K):
     assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("M,N,K", [(640, 264, 1024), (1024, 520, 1096), (1304, 264, 1024)])
+@pytest.mark.parametrize("tA,tB", [(0, 1), (0, 0), (1, 0)])
+def test_gemm_tensor_pairs_ragged(M, N, K, tA, tB):
+    # K >= 1024: CTA pairs (256-row tiles); 640 and 1304 rows end in a partial
+    # pair tile, K = 1096 in a partial k-block, N = 264 in a partial column tile.
+    A = rand_tensor((K, M) if tA else (M, K), torch.bfloat16, 90, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), torch.bfloat16, 91, DEV)
+    C = rand_tensor((1, N), torch.bfloat16, 92, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 0.75, 1.5, tA, tB)
+    ran_on_tensor_cores()
+    assert qg.mm_get_device_status() == "MM_OK"
+    a, b, c = to_np(A), to_np(B), to_np(C)
+    kw = dict(alpha=0.75, beta=1.5, transA=tA, transB=tB)
+    assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= 1e-2
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 72), (131, 9, 200)])
 def test_gemm_tensor_odd_m_n(M, N, K):
     # transA = 0, transB = 1: the stored strides are K and K; M and N are odd,
