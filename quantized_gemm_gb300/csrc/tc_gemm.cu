@@ -280,8 +280,12 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
         if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
       } else if (PAIR) {
         const uint32_t bar = mapa_shared(full, 0);
-        if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kStageBytes);
-        if (!p.a_mn) {
+        // A tail tile (at most 128 rows) takes 64 rows of A per CTA.
+        const bool tail = p.pair_tail && ti.rows <= BM;
+        if (rank == 0) mbar_arrive_expect_tx(full, 2 * (tail ? G::kStageBytes - G::kABytes / 2 : G::kStageBytes));
+        if (tail) {
+          tma_load_3d_pair(sa, tmS, k0, ti.a_row + (int32_t)(rank * (BM / 2)), ti.a_b, bar);
+        } else if (!p.a_mn) {
           tma_load_3d_pair(sa, tmA, k0, ar, ti.a_b, bar);
         } else {
           tma_load_3d_pair(sa, tmA, ar, k0, ti.a_b, bar);
@@ -356,6 +360,7 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
       tc_fence_after();
       const uint32_t d = tmem + buf * BN;
       const int kb1 = min(kb0 + p.kb_per_seg, p.num_kb);
+      const uint32_t idesc = (PAIR && p.pair_tail && ti.rows <= BM) ? p.idesc_tail : p.idesc;
       for (int kb = kb0; kb < kb1; ++kb) {
         const bool got = PAIR ? mbar_wait_cluster(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns)
                               : mbar_wait(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
@@ -386,7 +391,7 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
               tc_mma_tf32(d, ad, bd, p.idesc, 1u);
             }
           } else if (PAIR) {
-            tc_mma_f16_pair(d, ad, bd, p.idesc, acc);
+            tc_mma_f16_pair(d, ad, bd, idesc, acc);
           } else {
             tc_mma_f16(d, ad, bd, p.idesc, acc);
           }
@@ -867,19 +872,36 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       ++seg;
       if (!__all_sync(0xffffffffu, wait_full(buf, aph))) return;
       tc_fence_after();
+      // A pair's tail tile (one M = 128 MMA) leaves this CTA's 64 rows in
+      // TMEM lanes 0-63 for the tile's columns 0-127 and again in lanes
+      // 64-127 for columns 128-255, in TMEM columns 0-127: the warps of
+      // column slices 0 and 1 hold it, the others only release the buffer.
+      const bool tail = PAIR && p.pair_tail && ti.rows <= BM;
+      if (tail && slice * kCols >= BN / 2) {
+        tc_fence_before();
+        __syncwarp();
+        release(buf);
+        continue;
+      }
+      const int64_t roff = tail ? (int64_t)rank * (BM / 2) : row_off;
+      const int rbase = tail ? (quad & 1) * 32 : quad * 32;
+      const int rl = rbase + lane;
+      const int rows_t = PAIR ? max(0, min(tail ? BM / 2 : BM, ti.rows - (int)roff)) : ti.rows;
+      const bool rok = rl < rows_t;
+      const int64_t ncol = ncol0 + (tail ? (int64_t)(quad >> 1) * (BN / 2) : 0);
       const uint32_t taddr0 = tmem + tlane + buf * BN + slice * kCols;
       // This thread's output row (kept even when the row is past the tile's
       // valid rows: it is then only shuffled around, never dereferenced).
       uint16_t* yrow;
       const uint16_t* crow = nullptr;
       if (is_grouped(MODE)) {
-        const int64_t orow = row_ok ? p.g_rowlist[ti.a_row + row_off + rloc] : 0;
+        const int64_t orow = rok ? p.g_rowlist[ti.a_row + roff + rl] : 0;
         yrow = static_cast<uint16_t*>(p.y) + orow * p.y_rs;
-        if (p.c && row_ok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
+        if (p.c && rok) crow = static_cast<const uint16_t*>(p.c) + (int64_t)ti.g * p.c_gs;
       } else {
-        const int64_t m = ti.m0 + row_off + rloc;
+        const int64_t m = ti.m0 + roff + rl;
         yrow = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
-        if (p.c && row_ok)
+        if (p.c && rok)
           crow = static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs;
       }
       // The warp's columns, 64 at a time (two tcgen05.ld of 32); the
@@ -903,12 +925,12 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         // rows x 64 bytes of whole 32-byte sectors.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int64_t n = ncol0 + q64 * 64 + 32 * h;
+          const int64_t n = ncol + q64 * 64 + 32 * h;
           if (n >= p.N) break;
           if constexpr (MODE == kTF32) {
             // fp32 output: each thread writes its row's 32 values (128 bytes).
-            if (row_ok) {
-              const int64_t m = ti.m0 + row_off + rloc;
+            if (rok) {
+              const int64_t m = ti.m0 + roff + rl;
               float* yf = static_cast<float*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
               const float* cf = p.c ? static_cast<const float*>(p.c) + batch_off(p, p.c_bstride, ti.batch) +
                                           m * p.c_rs
@@ -951,10 +973,10 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
               const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
               uint16_t* dst = reinterpret_cast<uint16_t*>(
                   __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(yrow), rr));
-              if (quad * 32 + rr < rows_cta) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
+              if (rbase + rr < rows_t) *reinterpret_cast<uint4*>(dst + n + pc * 8) = val;
             }
             __syncwarp();
-          } else if (row_ok) {
+          } else if (rok) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
@@ -1196,7 +1218,10 @@ bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int6
 }
 
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair) {
-  const uint32_t m = pair ? 2 * BM : BM;        // a pair's MMA covers both CTAs' rows
+  return make_idesc_rows(f16, a_mn, b_mn, pair ? 2 * BM : BM);   // a pair's MMA covers both CTAs' rows
+}
+
+uint32_t make_idesc_rows(int f16, int a_mn, int b_mn, uint32_t m) {
   return (1u << 4)                              // D: fp32
          | ((f16 ? 0u : 1u) << 7)               // A: f16 (0) / bf16 (1)
          | ((f16 ? 0u : 1u) << 10)              // B: f16 (0) / bf16 (1)
@@ -1358,14 +1383,13 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
 // on single CTAs, whose smaller tiles keep more epilogues in flight.
 bool use_pair(int64_t M, int64_t K) { return M > BM && K >= kPairMinK; }
 
-// Grouped products pay for pairs with more padding (each group's last tile is
-// 256 rows instead of 128).  Measured on 16384 x 2 routed rows, K = 4096,
-// N = 14336: pairs are 5% faster with 8 groups (4096 rows each on average)
-// and 1.5% slower with 64 groups (512 rows), so they need 1024 rows a group.
+// Grouped pairs: a group's last row tile with at most 128 rows runs as an
+// M = 128 MMA, so pairs pad each group no more than single CTAs do; they need
+// groups of 256 rows on average to have full pair tiles to gain on.
 bool grouped_q_pairs_available() { return max_pair_clusters<kGroupedQ>() > 0; }
 
 bool use_grouped_pair(int64_t rows, int64_t G, int64_t K) {
-  return K >= kPairMinK && rows >= 8 * BM * G && max_pair_clusters<kGrouped>() > 0;
+  return K >= kPairMinK && rows >= 2 * BM * G && max_pair_clusters<kGrouped>() > 0;
 }
 
 int sm_count_public() { return sm_count(); }
@@ -1418,10 +1442,15 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
   // one CTA per tile otherwise, or if no pair can be placed.
   for (int attempt = use_pair(g.M, g.K) ? 0 : 1; attempt < 2; ++attempt) {
     const bool pair = attempt == 0;
-    OperandPlan a, b;
+    OperandPlan a, b, a_tail;
     if (!plan_dense(g, pair, &a, &b)) return MM_ERR_UNSUPPORTED;
     p.idesc = p.out_f32 ? make_idesc_tf32(pair) : make_idesc(p.out_f16, a.mn_major, b.mn_major, pair);
-    const mm_status st = launch_tc(p.out_f32 ? kTF32 : kDense, pair, a, b, p, stream);
+    // 16-bit pairs with K-major A run a last row tile of at most 128 rows as
+    // one M = 128 MMA fed by 64 rows of A per CTA.
+    p.pair_tail = pair && !p.out_f32 && !a.mn_major &&
+                  plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM / 2, &a_tail);
+    if (p.pair_tail) p.idesc_tail = make_idesc_rows(p.out_f16, 0, b.mn_major, BM);
+    const mm_status st = launch_tc(p.out_f32 ? kTF32 : kDense, pair, a, b, p, stream, p.pair_tail ? &a_tail : nullptr);
     if (st != MM_ERR_UNSUPPORTED || !pair) return st;
   }
   return MM_ERR_UNSUPPORTED;

@@ -33,6 +33,11 @@ struct TcParams {
   int a_mn, b_mn;                              // operand is MN-major in shared memory
   int num_kb, kb_per_seg;                      // k-blocks; k-blocks per accumulation segment
   uint32_t idesc;                              // tcgen05 instruction descriptor
+  // CTA pairs: a pair tile with at most 128 valid rows (the last row tile of
+  // a group, or of a dense product) runs as one M = 128 cta_group::2 MMA
+  // (idesc_tail) whose A rows (64 per CTA) come from the second A map.
+  int pair_tail;
+  uint32_t idesc_tail;
   // output: dense/qlinear y + boff(batch) + m*y_rs + n; grouped y + out_row*y_rs + n
   void* y;
   int64_t y_bstride[kMaxBatchDims];
@@ -79,12 +84,15 @@ bool plan_operand(const void* ptr, int dtype, int64_t mn_len, int64_t k_len, int
 bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int64_t d2, int64_t s1, int64_t s2,
                    int box0, int box1, OperandPlan* out);
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair);
+// The same with an explicit MMA height (128 or 256 rows).
+uint32_t make_idesc_rows(int f16, int a_mn, int b_mn, uint32_t m);
 uint32_t make_idesc_tf32(bool pair);
 void init_params(TcParams* p);
 // Fills the tile bookkeeping and launches tc_gemm_kernel: one CTA per SM, or
 // (pair) 2-CTA clusters computing 256-row tiles with cta_group::2 MMAs.
 // Returns MM_ERR_UNSUPPORTED when pairs cannot be placed.
-// kGroupedQ also takes the scale and zero-point maps (s, z).
+// kGroupedQ also takes the scale and zero-point maps (s, z); for kDense and
+// kGrouped pairs with p.pair_tail set, s is A's map with a 64-row box.
 mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan& b, TcParams& p,
                     cudaStream_t stream, const OperandPlan* s = nullptr, const OperandPlan* z = nullptr);
 // Whether an M x K problem uses CTA pairs.

@@ -533,6 +533,10 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   for (int d = 0; d < kMaxBatchDims; ++d) bm1.shape[d] = 1;
   int64_t zero[kMaxBatchDims] = {0, 0, 0, 0, 0, 0};
   if (!plan_operand(xperm, g.dtype, rows, g.K, l.kp, 1, bm1, zero, kTileM, &a)) return MM_ERR_UNSUPPORTED;
+  // Pairs run each group's last row tile, when it has at most 128 rows, as
+  // one M = 128 MMA fed by 64 rows of A per CTA (a 64-row box of the same rows).
+  OperandPlan a_tail;
+  const bool tail = pair && !g.wq && plan_operand(xperm, g.dtype, rows, g.K, l.kp, 1, bm1, zero, kTileM / 2, &a_tail);
 
   if (cudaMemsetAsync(count, 0, l.off_offset - l.off_count, stream) != cudaSuccess) return MM_ERR_CUDA;
   const int64_t cb = (rows + 255) / 256;
@@ -553,6 +557,10 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.M = rows; p.N = g.N; p.K = g.K;
   p.nt = nt;
   p.idesc = make_idesc(g.dtype == MM_F16, a.mn_major, b.mn_major, pair);
+  if (tail) {
+    p.pair_tail = 1;
+    p.idesc_tail = make_idesc_rows(g.dtype == MM_F16, a.mn_major, b.mn_major, kTileM);
+  }
   if (g.wq) {
     p.w_signed = g.wq == 1;
     p.wzp_present = g.wzp != nullptr;
@@ -574,7 +582,7 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
   p.status = status;
   // The tile count is known only on the device: one persistent CTA (pair) per SM (pair).
   if (g.wq) return launch_tc(kGroupedQ, true, a, b, p, stream, &sm, g.wzp ? &zm : nullptr);
-  return launch_tc(kGrouped, pair, a, b, p, stream);
+  return launch_tc(kGrouped, pair, a, b, p, stream, tail ? &a_tail : nullptr);
 }
 
 }  // namespace qg

@@ -55,11 +55,16 @@ def test_gemm_tensor(dtype, tA, tB, M, N, K):
     assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("M,N,K", [(640, 264, 1024), (1024, 520, 1096), (1304, 264, 1024)])
+@pytest.mark.parametrize("M,N,K", [(640, 264, 1024), (1024, 520, 1096), (1304, 264, 1024), (1128, 264, 1024),
+                                   (1064, 520, 1024)])
 @pytest.mark.parametrize("tA,tB", [(0, 1), (0, 0), (1, 0)])
 def test_gemm_tensor_pairs_ragged(M, N, K, tA, tB):
     # K >= 1024: CTA pairs (256-row tiles); 640 and 1304 rows end in a partial
     # pair tile, K = 1096 in a partial k-block, N = 264 in a partial column tile.
+    # With K-major A a last tile of at most 128 rows runs as one M = 128 MMA of
+    # 64 rows per CTA: 640 (128 rows: both CTAs full), 1128 (104: the second
+    # CTA holds 40), 1304 and 1064 (24 and 40: the second CTA holds none).
+    # Every M is a multiple of 8: with transA it is A's stored row stride.
     A = rand_tensor((K, M) if tA else (M, K), torch.bfloat16, 90, DEV)
     B = rand_tensor((N, K) if tB else (K, N), torch.bfloat16, 91, DEV)
     C = rand_tensor((1, N), torch.bfloat16, 92, DEV)
@@ -359,6 +364,31 @@ def test_grouped_tensor_cta_pairs(dtype, with_bias):
     p = np.array([0.63, 0.345, 0.0, 0.025])
     gi = torch.from_numpy(np.random.default_rng(33).choice(G, size=(M, S), p=p)).to(torch.int32).to(DEV)
     bias = rand_tensor((G, N), dtype, 34, DEV) if with_bias else None
+    _grouped(x, w, gi, bias)
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
+# Group sizes whose last 256-row pair tile holds every kind of remainder: none
+# (256, 512), at most 64 rows (1, 63, 64, 257, 320: the second CTA of the tail
+# tile holds none), 65-128 rows (65, 127, 128, 384, 600: the tail tile splits
+# 64 + the rest), and 129-255 rows (129, 200, 255, 385, 1500: a full-height
+# pair tile), plus an empty group.
+_TAIL_SIZES = [1, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 320, 384, 385, 512, 600, 1500, 0]
+
+
+@pytest.mark.parametrize("dtype", HALF, ids=str)
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_grouped_tensor_cta_pair_tail_tiles(dtype, with_bias):
+    # 5246 routed rows over 18 groups (291 a group on average) and K >= 1024:
+    # CTA pairs, each group's last tile of at most 128 rows as one M = 128 MMA.
+    G, S, K, N = len(_TAIL_SIZES), 2, 1024, 520
+    ids = np.repeat(np.arange(G), _TAIL_SIZES)
+    np.random.default_rng(38).shuffle(ids)
+    M = ids.size // S
+    gi = torch.from_numpy(ids.reshape(M, S)).to(torch.int32).to(DEV)
+    x = rand_tensor((M, K), dtype, 39, DEV)
+    w = rand_tensor((G, K, N), dtype, 40, DEV)
+    bias = rand_tensor((G, N), dtype, 41, DEV) if with_bias else None
     _grouped(x, w, gi, bias)
     assert qg.mm_get_device_status() == "MM_OK"
 
