@@ -362,21 +362,79 @@ __device__ __forceinline__ int64_t load_index(const void* gi, int64_t off, int i
   return ind64 ? static_cast<const int64_t*>(gi)[off] : (int64_t) static_cast<const int32_t*>(gi)[off];
 }
 
-__global__ void route_count_kernel(const void* gi, int ind64, int64_t gi_ms, int64_t gi_ss, int64_t M, int64_t S,
-                                   int64_t G, int32_t* count, unsigned* status) {
+// Up to kHistGroups groups are counted in a shared-memory histogram per block
+// (lanes of a warp that pick the same group add once, by popcount), then added
+// to the global counts; more groups count with global atomics directly.
+constexpr int kHistGroups = 4096;
+
+__global__ void __launch_bounds__(256) route_count_kernel(const void* gi, int ind64, int64_t gi_ms, int64_t gi_ss,
+                                                          int64_t M, int64_t S, int64_t G, int32_t* count,
+                                                          unsigned* status) {
+  __shared__ int32_t hist[kHistGroups];
   const int64_t total = M * S;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = e / S, i = e - m * S;
-    const int64_t g = load_index(gi, m * gi_ms + i * gi_ss, ind64);
-    if (g >= 0 && g < G) atomicAdd(count + g, 1);
-    else atomicOr(status, kStatusIndexRange);
+  const bool shared_hist = G <= kHistGroups;
+  if (shared_hist) {
+    for (int g = threadIdx.x; g < G; g += blockDim.x) hist[g] = 0;
+    __syncthreads();
+  }
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // Every lane of a warp runs the same number of iterations (the loop bound is
+  // rounded up to whole warps), so the warp-wide match below is well defined.
+  const int64_t total_w = (total + 31) / 32 * 32;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total_w; e += stride) {
+    int64_t g = -1;
+    bool valid = false;
+    if (e < total) {
+      const int64_t m = e / S, i = e - m * S;
+      g = load_index(gi, m * gi_ms + i * gi_ss, ind64);
+      valid = g >= 0 && g < G;
+      if (!valid) atomicOr(status, kStatusIndexRange);
+    }
+    if (shared_hist) {
+      const int key = valid ? (int)g : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, key);
+      if (valid && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(hist + key, __popc(same));
+    } else if (valid) {
+      atomicAdd(count + g, 1);
+    }
+  }
+  if (shared_hist) {
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      if (hist[g]) atomicAdd(count + g, hist[g]);
   }
 }
 
-// One block: offset[g] = sum_{h<g} count[h]; tile_start[g] = sum_{h<g} ceil(count[h]/128) * nt.
+// Inclusive sum of v over the threads of the block, in thread order (warp
+// shuffles, then one warp over the per-warp totals); `part` holds 32 values.
+__device__ __forceinline__ int64_t block_inclusive_sum(int64_t v, int64_t* part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) part[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < (int)(blockDim.x >> 5) ? part[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    part[lane] = w;
+  }
+  __syncthreads();
+  const int64_t r = v + (warp > 0 ? part[warp - 1] : 0);
+  __syncthreads();   // part may be reused by the caller
+  return r;
+}
+
+// One block: offset[g] = sum_{h<g} count[h]; tile_start[g] = sum_{h<g} ceil(count[h]/tile_rows) * nt.
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, int64_t G, int64_t nt,
                                                           int tile_rows, int32_t* offset, int32_t* tile_start) {
-  __shared__ int64_t part_rows[1024], part_tiles[1024];
+  __shared__ int64_t part[32];
   const int t = threadIdx.x, T = blockDim.x;
   const int64_t per = (G + T - 1) / T;
   const int64_t lo = min(G, (int64_t)t * per), hi = min(G, lo + per);
@@ -385,22 +443,9 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, 
     rows += count[g];
     tiles += (count[g] + tile_rows - 1) / tile_rows * nt;
   }
-  part_rows[t] = rows;
-  part_tiles[t] = tiles;
-  __syncthreads();
-  if (t == 0) {
-    int64_t r = 0, k = 0;
-    for (int u = 0; u < T; ++u) {
-      const int64_t a = part_rows[u], b = part_tiles[u];
-      part_rows[u] = r;
-      part_tiles[u] = k;
-      r += a;
-      k += b;
-    }
-  }
-  __syncthreads();
-  rows = part_rows[t];
-  tiles = part_tiles[t];
+  // Exclusive prefix of this thread's range.
+  rows = block_inclusive_sum(rows, part) - rows;
+  tiles = block_inclusive_sum(tiles, part) - tiles;
   for (int64_t g = lo; g < hi; ++g) {
     offset[g] = (int32_t)rows;
     tile_start[g] = (int32_t)tiles;

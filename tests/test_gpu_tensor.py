@@ -190,6 +190,16 @@ def test_qlinear_tensor(ta, tb, ty, gran, M, K, N):
     _q(_qcase(M, K, N, ta, tb, ty, gran))
 
 
+@pytest.mark.parametrize("M,K,N,gran,batch", [(600, 1096, 264, "vector", ()), (1000, 2048, 520, "matrix", ()),
+                                               (300, 1024, 264, "matrix", (2,))])
+def test_qlinear_tensor_long_k_ragged(M, K, N, gran, batch):
+    # K >= 1024 (several exact 1024-deep segments) with ragged edges: 600 and
+    # 1000 rows end in partial row tiles, K = 1096 in a partial k-block and a
+    # 72-deep last segment, N = 264 in a partial column tile; the last case has
+    # batch-indexed per-row and per-column parameters.
+    _q(_qcase(M, K, N, torch.int8, torch.uint8, torch.int8, gran, batch_a=batch, batch_b=batch, seed=M))
+
+
 def test_qlinear_tensor_f16_scales_and_batch():
     _q(_qcase(150, 300, 200, torch.int8, torch.int8, torch.int8, "matrix", torch.float16,
               batch_a=(2, 3), batch_b=(2, 3)))
