@@ -577,29 +577,66 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
           *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       } else {
-        // q - zp exactly in fp32; an integer of at most 8 significant bits, so
-        // its bf16 is the upper half of the fp32 pattern; the bf16 pair product
-        // is rounded once.
-        float cz[8];
+        // The byte u (q moved to [0, 255]) in byte 1 of the pattern 0x47000000
+        // is the fp32 value 32768 + u.  With the column's bf16 scale s (8
+        // significant bits) and kc = -(32768 + c) * s, c = 128*signed + zp
+        // (a 16-bit integer times s: at most 24 significant bits, exact),
+        // fma(32768 + u, s, kc) is (u - c) * s = (q - zp) * s before its one
+        // rounding, and that value has at most 9 + 8 significant bits: the
+        // fp32 result is exact and the pair conversion to bf16 is the only
+        // rounding.  Two columns per packed fp32x2 FMA.  (kc overflows for
+        // |s| near 2^112; a scale of 2^100 or more in any of the thread's
+        // columns takes the subtract-then-multiply form below instead.)
+        float sf[8], kc[8], smax = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) cz[e] = zbias + (float)zp[e];
+        for (int e = 0; e < 8; ++e) {
+          sf[e] = __uint_as_float((e & 1) ? (sw[e >> 1] & 0xFFFF0000u) : (sw[e >> 1] << 16));
+          kc[e] = __fmul_rn(-(32768.f + (p.w_signed ? 128.f : 0.f) + (float)zp[e]), sf[e]);
+          smax = fmaxf(smax, fabsf(sf[e]));
+        }
+        if (smax < 0x1p100f) {
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-          const int k = k_first + kRowStep * i;
-          const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
-          uint32_t w[4];
+          for (int i = 0; i < kRows; ++i) {
+            const int k = k_first + kRowStep * i;
+            const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+            uint32_t w[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const uint32_t src = e2 < 2 ? qx : qy;
-            const int b0 = (e2 & 1) * 2;
-            const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
-            const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
-            const uint32_t dv = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
-            const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dv),
-                                             *reinterpret_cast<const __nv_bfloat162*>(&sw[e2]));
-            w[e2] = *reinterpret_cast<const uint32_t*>(&y);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const uint32_t src = e2 < 2 ? qx : qy;
+              const uint32_t j = (e2 & 1) * 2;
+              const float2 f = make_float2(__uint_as_float(__byte_perm(src, 0x47000000u, 0x7404u + (j << 4))),
+                                           __uint_as_float(__byte_perm(src, 0x47000000u, 0x7404u + ((j + 1) << 4))));
+              const float2 y = fma2_rn(f, make_float2(sf[2 * e2], sf[2 * e2 + 1]), make_float2(kc[2 * e2], kc[2 * e2 + 1]));
+              const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
+              w[e2] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          // q - zp exactly in fp32 (the byte in the low mantissa of 2^23, minus
+          // 2^23 + c); at most 8 significant bits, so its bf16 is the upper
+          // half of the fp32 pattern; the bf16 pair product is rounded once.
+          float cz[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cz[e] = zbias + (float)zp[e];
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const int k = k_first + kRowStep * i;
+            const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+            uint32_t w[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const uint32_t src = e2 < 2 ? qx : qy;
+              const int b0 = (e2 & 1) * 2;
+              const float f0 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0)), cz[2 * e2]);
+              const float f1 = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4Bu, 0x4550u + b0 + 1)), cz[2 * e2 + 1]);
+              const uint32_t dv = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+              const __nv_bfloat162 y = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&dv),
+                                               *reinterpret_cast<const __nv_bfloat162*>(&sw[e2]));
+              w[e2] = *reinterpret_cast<const uint32_t*>(&y);
+            }
+            *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       // Publish the stage: each lane orders its writes before the async

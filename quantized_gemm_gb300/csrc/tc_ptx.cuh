@@ -279,6 +279,15 @@ __device__ __forceinline__ void tc_mma_tf32_pair(uint32_t d, uint64_t adesc, uin
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// a * b + c for two fp32 lanes at once (one rounding each, to nearest even).
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
 // x rounded to tf32 (10 mantissa bits; nearest, ties away from zero), as fp32 bits.
 __device__ __forceinline__ uint32_t cvt_tf32(float x) {
   uint32_t r;

@@ -114,6 +114,34 @@ def test_qweights_tensor_dequantized_values_exact(dtype, wdtype):
     assert np.array_equal(to_np(y)[:, 0, :], want)
 
 
+@pytest.mark.parametrize("wdtype", [torch.int8, torch.uint8], ids=str)
+def test_qweights_tensor_extreme_scales_exact(wdtype):
+    # bf16 scales by blocks of 8 columns (one converter thread's columns):
+    # even blocks cycle over 1 + 2^-7, 2^-120, 0.75 and 3 * 2^90 (the
+    # converters' fused multiply-add form), odd blocks over 2^110, 3 * 2^105,
+    # 1 + 2^-7 and 2^-120 (a scale of 2^100 or more: the subtract-then-multiply
+    # form).  With one-hot input rows both must give the oracle's dequantized
+    # weights bit for bit (1 + 2^-7 times odd integers rounds at ties).
+    M, K, N, G = 256, 192, 256, 2
+    d = _case(M, K, N, G, 1, torch.bfloat16, wdtype, 0, True, False, 56)
+    ordinary = [1 + 2.0 ** -7, 2.0 ** -120, 0.75, 3 * 2.0 ** 90]
+    huge = [2.0 ** 110, 3 * 2.0 ** 105, 1 + 2.0 ** -7, 2.0 ** -120]
+    cols = [(huge if (n // 8) % 2 else ordinary)[n % 4] for n in range(N)]
+    d["w_scale"] = torch.tensor(cols, dtype=torch.float64).reshape(1, 1, N).expand(G, 1, N).to(
+        torch.bfloat16).contiguous().to(DEV)
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    ks = np.arange(M) % K
+    x[np.arange(M), ks] = 1
+    d["input"] = x.to(DEV)
+    with path(qg.MM_PATH_TENSOR):
+        y = _run(d)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    w = oracle.dequantize_linear(d["weights_q"].cpu().numpy(), to_np(d["w_scale"]),
+                                 d["w_zero_point"].cpu().numpy(), 0, "bf16")
+    gi = d["group_indices"].cpu().numpy()
+    assert np.array_equal(to_np(y)[:, 0, :], w[gi[:, 0], ks, :])
+
+
 def test_qweights_tensor_invalid_indices():
     d = _case(300, 256, 256, 3, 2, torch.bfloat16, torch.int8, 0, True, False, 53)
     gi = torch.from_numpy(np.random.default_rng(54).integers(-1, 4, size=(300, 2)).astype(np.int64)).to(DEV)
