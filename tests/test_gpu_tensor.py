@@ -403,6 +403,27 @@ def test_grouped_tensor_cta_pair_tail_tiles(dtype, with_bias):
     assert qg.mm_get_device_status() == "MM_OK"
 
 
+@pytest.mark.parametrize("pairs", [False, True])
+def test_grouped_tensor_padded_and_transposed_input(pairs):
+    # The same product with the input in two layouts, both copied into group
+    # order by the routing: rows 16-byte aligned with a padded row stride
+    # (16-byte vector copies) and stored transposed (column stride M:
+    # element-wise copies).  K = 1024 with 300 routed rows a group on average
+    # takes CTA pairs (tail tiles included), K = 512 single CTAs.
+    M, S, G, N = 900, 2, 6, 520
+    K = 1024 if pairs else 512
+    g = np.random.default_rng(42)
+    gi = torch.from_numpy(g.choice(G, size=(M, S), p=[0.4, 0.25, 0.15, 0.1, 0.07, 0.03]).astype(np.int32)).to(DEV)
+    x_pad = rand_tensor((M, K + 64), torch.bfloat16, 43, DEV)
+    x_rows = x_pad[:, :K]                                   # row stride K + 64, unit column stride
+    x_cols = x_rows.t().contiguous().t()                    # the same values, column stride M
+    w = rand_tensor((G, K, N), torch.bfloat16, 44, DEV)
+    bias = rand_tensor((G, N), torch.bfloat16, 45, DEV)
+    for x in (x_rows, x_cols):
+        _grouped(x, w, gi, bias)
+        assert qg.mm_get_device_status() == "MM_OK"
+
+
 def test_grouped_tensor_cta_pairs_invalid_indices():
     M, K, N, G = 2200, 1024, 256, 2
     x = rand_tensor((M, K), torch.bfloat16, 35, DEV)
