@@ -150,11 +150,15 @@ __global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
 // partial column sums are combined in shared memory, and one atomic add per
 // column and block accumulates the band into the column sums (which start at
 // zero).  Consecutive threads read consecutive 16-byte pieces of a row.
+// Two blocks per SM: unbounded, the batched loads and decoded values took 246
+// registers a thread and one block per SM; capped at 122 (no spills) the
+// int8 workload's call is 0.4145 -> 0.4087 ms, its 4-batch variant (four b
+// matrices) 0.481 -> 0.457 ms.
 constexpr int kColRows = 128;
 constexpr int kColGroups = 16;                   // 16-column groups per block
 constexpr int kRowLanes = 16;
 
-__global__ void __launch_bounds__(kColGroups * kRowLanes) shift_cols_kernel(const ShiftArgs p) {
+__global__ void __launch_bounds__(kColGroups * kRowLanes, 2) shift_cols_kernel(const ShiftArgs p) {
   __shared__ uint32_t part_s[kRowLanes][kColGroups * 16 + 1];
   const int cgl = threadIdx.x % kColGroups, lane_r = threadIdx.x / kColGroups;
   const int64_t cgroups = (p.cols + 15) / 16;
