@@ -77,6 +77,38 @@ def test_gemm_tensor_pairs_ragged(M, N, K, tA, tB):
     assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= 1e-2
 
 
+# More tiles than the persistent grid, with ragged edges.  Singles: 1104 x
+# 4600 is 9 x 18 = 162 tiles on 152 CTAs (ragged M, N and K).  Pairs (K >=
+# 1024): 1304 x 4104 is 6 x 17 = 102 pair tiles on 76 pairs, the last row
+# tile 24 rows (an M = 128 tail tile when A is K-major), the last column tile
+# 8 columns.  M and N are multiples of 8: stored row strides under transA /
+# transB = 0.
+@pytest.mark.parametrize("M,N,K", [(1104, 4600, 328), (1304, 4104, 1096)])
+@pytest.mark.parametrize("tA,tB", [(0, 1), (0, 0), (1, 1)])
+def test_gemm_tensor_many_tiles_ragged(M, N, K, tA, tB):
+    A = rand_tensor((K, M) if tA else (M, K), torch.bfloat16, 93, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), torch.bfloat16, 94, DEV)
+    C = rand_tensor((M, 1), torch.bfloat16, 95, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 0.5, 2.0, tA, tB)
+    ran_on_tensor_cores()
+    a, b, c = to_np(A), to_np(B), to_np(C)
+    kw = dict(alpha=0.5, beta=2.0, transA=tA, transB=tB)
+    assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= 1e-2
+
+
+def test_matmul_tensor_many_tiles_batched_f16():
+    # A [9, 640, 328] @ B [1, 328, 1024]: 9 x 5 x 4 = 180 single-CTA tiles on
+    # 152 CTAs, B broadcast over the batch.
+    A = rand_tensor((9, 640, 328), torch.float16, 96, DEV)
+    B = rand_tensor((1, 328, 1024), torch.float16, 97, DEV)
+    with tensor_path():
+        Y = qg.mm_matmul(A, B)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= TOL[torch.float16]
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 72), (131, 9, 200)])
 def test_gemm_tensor_odd_m_n(M, N, K):
     # transA = 0, transB = 1: the stored strides are K and K; M and N are odd,
