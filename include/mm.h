@@ -19,7 +19,10 @@
  *   shape returns MM_ERR_SHAPE and any other type MM_ERR_DTYPE.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Calls are asynchronous: the return value reports host-side
- *   validation and launch errors only.  Device-side conditions (an out-of-range
+ *   validation and launch errors only.  mm_matmul, mm_gemm, mm_qlinear_matmul
+ *   and mm_grouped_matmul enqueue only kernels and asynchronous memsets, so
+ *   once one call has run on the device (it caches per-device properties)
+ *   they can be captured in a CUDA graph and replayed.  Device-side conditions (an out-of-range
  *   group index, a pipeline wait that timed out) are recorded in a per-device
  *   status word read with mm_get_device_status().
  * Memory.  The library never allocates device memory.  Operators whose fast
