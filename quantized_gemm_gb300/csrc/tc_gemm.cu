@@ -1439,9 +1439,16 @@ namespace {
 
 bool plan_dense(const GemmArgs& g, bool pair, OperandPlan* a, OperandPlan* b) {
   if (g.dtype != MM_BF16 && g.dtype != MM_F16 && g.dtype != MM_F32) return false;
-  if (g.M < 2 || g.N < 2 || g.K < 1) return false;
+  if (g.M < 1 || g.N < 2 || g.K < 1) return false;
   if (g.y.cs != 1) return false;
-  if (!plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM, a)) return false;
+  // A single row of A' (a vector-matrix product: M = 1, MatMul's promoted 1-D
+  // A) with unit stride along k is a K-major tile whatever its row stride
+  // (0 for a promoted vector, 1 for A stored [K, 1]), which only row 0 uses:
+  // give the tensor map a row pitch TMA accepts.  The other 127 rows of the
+  // tile read the fill value and are never stored.
+  const int64_t vec = g.dtype == MM_F32 ? 4 : 8;
+  const int64_t a_rs = (g.M == 1 && g.a.cs == 1) ? (g.K + vec - 1) / vec * vec : g.a.rs;
+  if (!plan_operand(g.a.ptr, g.dtype, g.M, g.K, a_rs, g.a.cs, g.bm, g.a.bstride, BM, a)) return false;
   if (!plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, pair ? BN / 2 : BN, b)) return false;
   return true;
 }
