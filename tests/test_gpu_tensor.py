@@ -109,6 +109,24 @@ def test_matmul_tensor_many_tiles_batched_f16():
     assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= TOL[torch.float16]
 
 
+# Single-CTA products with fewer tiles than SMs and a full C: 640 x 2560 is
+# 5 x 10 = 50 tiles, 296 x 3000 is 3 x 12 = 36 tiles with a ragged last
+# row and column tile.  K < 1024: single CTAs.
+@pytest.mark.parametrize("dtype", HALF, ids=str)
+@pytest.mark.parametrize("M,N,K", [(640, 2560, 512), (296, 3000, 328)])
+@pytest.mark.parametrize("tA,tB", [(0, 1), (0, 0), (1, 0)])
+def test_gemm_tensor_few_tiles(dtype, M, N, K, tA, tB):
+    A = rand_tensor((K, M) if tA else (M, K), dtype, 98, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), dtype, 99, DEV)
+    C = rand_tensor((M, N), dtype, 100, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 0.5, -1.0, tA, tB)
+    ran_on_tensor_cores()
+    a, b, c = to_np(A), to_np(B), to_np(C)
+    kw = dict(alpha=0.5, beta=-1.0, transA=tA, transB=tB)
+    assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 72), (131, 9, 200)])
 def test_gemm_tensor_odd_m_n(M, N, K):
     # transA = 0, transB = 1: the stored strides are K and K; M and N are odd,
