@@ -67,15 +67,19 @@ constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
 // 6 stages.
 template <int MODE, bool PAIR>
 struct Geo {
-  static constexpr int kBRows = PAIR ? BN / 2 : BN;     // B columns (rows of B') held by one CTA
-  static constexpr int kABytes = BM * BK * 2;           // 128 rows x 128 bytes (64 x 16-bit or 32 x fp32)
+  // kSkinny: 64-column tiles with 64-row A boxes; the M = 128 MMA's rows
+  // 64..127 read the stage's B bytes and are never stored.
+  static constexpr int kTileN = MODE == kSkinny ? 64 : BN;
+  static constexpr int kBRows = PAIR ? BN / 2 : kTileN;  // B columns (rows of B') held by one CTA
+  static constexpr int kABytes = (MODE == kSkinny ? BM / 2 : BM) * BK * 2;   // rows x 128 bytes
   static constexpr int kBBytes = kBRows * BK * 2;
   // kTF32: each stage holds the loaded (then high) parts of A and B followed
   // by their low parts at kLoOff.
   static constexpr int kLoOff = MODE == kTF32 ? kABytes + kBBytes : 0;
   static constexpr int kStageBytes = (kABytes + kBBytes) * (MODE == kTF32 ? 2 : 1);
   // kGroupedQ gives one stage's worth of shared memory to its int8 staging ring.
-  static constexpr int kStages = MODE == kTF32 ? (PAIR ? 3 : 2) : PAIR ? (MODE == kGroupedQ ? 5 : 6) : 4;
+  static constexpr int kStages =
+      MODE == kTF32 ? (PAIR ? 3 : 2) : PAIR ? (MODE == kGroupedQ ? 5 : 6) : MODE == kSkinny ? 12 : 4;
   static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
@@ -191,7 +195,7 @@ __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t t
   ti.batch = b;
   ti.g = 0;
   ti.m0 = (int64_t)mtile * Geo<MODE, PAIR>::kTileRows;
-  ti.n0 = (int64_t)ntile * BN;
+  ti.n0 = (int64_t)ntile * Geo<MODE, PAIR>::kTileN;
   ti.a_row = (int32_t)ti.m0;
   ti.a_b = (int32_t)batch_off(p, p.a_bc, b);
   ti.b_b = (int32_t)batch_off(p, p.b_bc, b);
@@ -916,7 +920,7 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
       // 64-127 for columns 128-255, in TMEM columns 0-127: the warps of
       // column slices 0 and 1 hold it, the others only release the buffer.
       const bool tail = PAIR && p.pair_tail && ti.rows <= BM;
-      if (tail && slice * kCols >= BN / 2) {
+      if ((tail && slice * kCols >= BN / 2) || slice * kCols >= Geo<MODE, PAIR>::kTileN) {
         tc_fence_before();
         __syncwarp();
         release(buf);
@@ -1260,12 +1264,14 @@ uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair) {
   return make_idesc_rows(f16, a_mn, b_mn, pair ? 2 * BM : BM);   // a pair's MMA covers both CTAs' rows
 }
 
-uint32_t make_idesc_rows(int f16, int a_mn, int b_mn, uint32_t m) {
+uint32_t make_idesc_rows(int f16, int a_mn, int b_mn, uint32_t m) { return make_idesc_mn(f16, a_mn, b_mn, m, BN); }
+
+uint32_t make_idesc_mn(int f16, int a_mn, int b_mn, uint32_t m, uint32_t n) {
   return (1u << 4)                              // D: fp32
          | ((f16 ? 0u : 1u) << 7)               // A: f16 (0) / bf16 (1)
          | ((f16 ? 0u : 1u) << 10)              // B: f16 (0) / bf16 (1)
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
-         | ((uint32_t)(BN >> 3) << 17) | ((m >> 4) << 24);
+         | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // kind::tf32: A and B tf32 (format 2), D fp32, both K-major.
@@ -1373,8 +1379,9 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
   int64_t work = 0;
   if (!is_grouped(mode)) {
     const int64_t rows = pair ? 2 * BM : BM;
+    const int64_t cols = mode == kSkinny ? 64 : BN;
     p.mt = (p.M + rows - 1) / rows;
-    p.nt = (p.N + BN - 1) / BN;
+    p.nt = (p.N + cols - 1) / cols;
     p.tiles = p.mt * p.nt * p.bm.count;
     if (p.tiles >= (1ll << 31) || p.mt * p.nt >= (1ll << 31)) return MM_ERR_UNSUPPORTED;
     const uint32_t per_batch = (uint32_t)(p.mt * p.nt);
@@ -1401,6 +1408,8 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
     case kDense:
       return pair ? launch_kernel<kDense, true>(a, b, ms, mz, p, work, stream)
                   : launch_kernel<kDense, false>(a, b, ms, mz, p, work, stream);
+    case kSkinny:   // single CTAs only
+      return pair ? MM_ERR_UNSUPPORTED : launch_kernel<kSkinny, false>(a, b, ms, mz, p, work, stream);
     case kGrouped:
       return pair ? launch_kernel<kGrouped, true>(a, b, ms, mz, p, work, stream)
                   : launch_kernel<kGrouped, false>(a, b, ms, mz, p, work, stream);
@@ -1484,6 +1493,21 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
     for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % vec == 0);
   }
   p.status = status;
+  // A few rows (at most 64, K-major A) against a wide B' with fewer whole
+  // tiles than half the SMs: the skinny configuration streams B' with 64-
+  // column tiles and a deep ring.
+  if (!p.out_f32 && g.M <= BM / 2 &&
+      ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * g.bm.count * 2 <= sm_count()) {
+    OperandPlan a, b;
+    const int64_t vec = 8;
+    const int64_t a_rs = (g.M == 1 && g.a.cs == 1) ? (g.K + vec - 1) / vec * vec : g.a.rs;
+    if (g.N >= 2 && g.y.cs == 1 &&
+        plan_operand(g.a.ptr, g.dtype, g.M, g.K, a_rs, g.a.cs, g.bm, g.a.bstride, BM / 2, &a) && !a.mn_major &&
+        plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, 64, &b)) {
+      p.idesc = make_idesc_mn(p.out_f16, 0, b.mn_major, BM, 64);
+      return launch_tc(kSkinny, false, a, b, p, stream);
+    }
+  }
   // CTA pairs (256-row tiles) for long-K products with more than one row tile;
   // one CTA per tile otherwise, or if no pair can be placed.
   for (int attempt = use_pair(g.M, g.K) ? 0 : 1; attempt < 2; ++attempt) {

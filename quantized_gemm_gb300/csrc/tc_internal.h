@@ -17,7 +17,10 @@ constexpr int kTileK = 64;    // one 128-byte swizzle row of 16-bit elements
 // zero points (DequantizeLinear fused into the mainloop; CTA pairs only).
 // kTF32: fp32 MatMul / Gemm as three tf32 products (hi*hi + hi*lo + lo*hi of
 // each operand's split x = hi + lo, split in shared memory by converter warps).
-enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3, kTF32 = 4 };
+// kSkinny: dense bf16/f16 products with at most 64 rows and few tiles (a
+// vector or a few rows against a wide B'): 64-column tiles, 64-row A boxes
+// and a 12-stage ring of 16 KB, so that many more bytes of B' are in flight.
+enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3, kTF32 = 4, kSkinny = 5 };
 
 struct TcParams {
   int64_t M, N, K;
@@ -86,6 +89,8 @@ bool plan_plain_3d(const void* ptr, int elem_bytes, int64_t d0, int64_t d1, int6
 uint32_t make_idesc(int f16, int a_mn, int b_mn, bool pair);
 // The same with an explicit MMA height (128 or 256 rows).
 uint32_t make_idesc_rows(int f16, int a_mn, int b_mn, uint32_t m);
+// The same with an explicit MMA width (16..256 columns, a multiple of 16).
+uint32_t make_idesc_mn(int f16, int a_mn, int b_mn, uint32_t m, uint32_t n);
 uint32_t make_idesc_tf32(bool pair);
 void init_params(TcParams* p);
 // Fills the tile bookkeeping and launches tc_gemm_kernel: one CTA per SM, or
