@@ -23,7 +23,9 @@
 // 256 x 256 tile with tcgen05.mma.cta_group::2: each loads its 128 rows of A
 // and half of the tile's B columns (6-stage ring of 32 KB), the even CTA
 // issues the MMAs for both, and commits are multicast to the pair.  Each SM
-// then takes in 64 bytes of operands per MMA cycle instead of 96.
+// then takes in 64 bytes of operands per MMA cycle instead of 96.  A pair
+// tile with at most 128 valid rows (a group's or a product's last row tile)
+// runs as one M = 128 cta_group::2 MMA fed by 64 rows of A per CTA.
 //
 // Tiles are numbered in a grouped raster (bands of 8 row tiles, for L2 reuse)
 // and decoded with 32-bit multiply-shift division by precomputed divisors.
@@ -41,6 +43,12 @@
 //             exactly in the fp32 accumulator; the epilogue converts each
 //             segment to int32, adds with wrap-around, applies the zero points
 //             from the operands' row and column sums, then requantises.
+//   kGroupedQ GroupedMatMul with int8/uint8 weights: converter warps form
+//             T((q - zp) * scale) in shared memory (CTA pairs).
+//   kTF32     fp32 MatMul / Gemm as three tf32 products of split operands.
+//   kSkinny   kDense for at most 64 rows against a wide B': 64-column tiles,
+//             64-row A boxes and a 12-stage ring of 16 KB, so that many CTAs
+//             stream B' with many bytes in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
