@@ -290,6 +290,26 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
                          "hbm_gbs": nbytes / ms / 1e6, "kernels_per_call": 2, "l2": "flushed between iterations"}
     del d, Y1, Y2, graph
 
+    # 2a. Skinny products of the headline Gemm's B (stored [N, K], transB = 1):
+    # one row (a vector-matrix product) and 16 rows against 8192 x 8192 bf16.
+    # One stream over B (134 MB > L2): bound by HBM bandwidth.
+    Bs = workloads.gemm_bf16(device=dev)["B"]
+    for rows in (1, 16):
+        As = (torch.randn((rows, 8192), generator=torch.Generator(device=dev).manual_seed(rows), device=dev)
+              / math.sqrt(8192)).to(torch.bfloat16)
+        Ys = torch.empty((rows, 8192), dtype=torch.bfloat16, device=dev)
+        ms, _ = time_loop(lambda: qg.mm_gemm(As, Bs, None, 1.0, 1.0, 0, 1, out=Ys), 50, 5, world, stream,
+                          idle_s=EXTRA_IDLE_S)
+        assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+        nbytes = 2 * (rows * 8192 + 8192 * 8192 + rows * 8192)
+        out["gemm_bf16_skinny_m%d" % rows] = {
+            "value": nbytes / ms / 1e6, "unit": "GB/s", "us_per_call": ms * 1e3, "bound": "hbm", "peak_gbs": hbm,
+            "frac": nbytes / ms / 1e6 / hbm, "tflops": 2 * rows * 8192 * 8192 / ms / 1e9, "kernels_per_call": 1,
+            "shape": "[%d, 8192] @ B^T, B [8192, 8192] bf16" % rows, "l2": "B (134 MB) larger than L2"}
+        del As, Ys
+    del Bs
+    torch.cuda.empty_cache()
+
     # 2b. The headline Gemm in fp32 (three tf32 tensor-core products per step).
     d = workloads.gemm_bf16(device=dev, dtype=torch.float32)
     Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
