@@ -622,6 +622,12 @@ def run_profile_workload(args):
         d = workloads.gemm_bf16(device=dev, dtype=torch.float32)
         Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
         step = lambda: qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], 0, 1, out=Yf)
+    elif name.startswith("gemm_bf16_skinny_m"):
+        rows = int(name[len("gemm_bf16_skinny_m"):])          # [rows, 8192] @ B^T, B the headline's
+        Bs = workloads.gemm_bf16(device=dev)["B"]
+        As = (torch.randn((rows, 8192), device=dev) / math.sqrt(8192)).to(torch.bfloat16)
+        Ys = torch.empty((rows, 8192), dtype=torch.bfloat16, device=dev)
+        step = lambda: qg.mm_gemm(As, Bs, None, 1.0, 1.0, 0, 1, out=Ys)
     elif name == "matmul_bf16_bcast":
         d = workloads.matmul_bf16_bcast(device=dev)
         Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
@@ -668,7 +674,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--profile-workload", default=None,
-                    help="run only this workload (gemm_bf16, matmul_bf16_bcast, qlinear_s8 or a QLinear variant, "
+                    help="run only this workload (gemm_bf16, gemm_bf16_skinny_mR, matmul_bf16_bcast, qlinear_s8 or a "
+                         "QLinear variant, "
                          "grouped_bf16[_gG][_nN])")
     args = ap.parse_args()
     if args.warmup < 3:
