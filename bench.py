@@ -291,23 +291,44 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     del d, Y1, Y2, graph
 
     # 2a. Skinny products of the headline Gemm's B (stored [N, K], transB = 1):
-    # one row (a vector-matrix product) and 16 rows against 8192 x 8192 bf16.
-    # One stream over B (134 MB > L2): bound by HBM bandwidth.
+    # one row (a vector-matrix product), 4 and 16 rows against 8192 x 8192 bf16.
+    # One stream over B (134 MB): bound by HBM bandwidth.  1 and 4 rows run the
+    # few-row CUDA-core kernel, 16 rows the tensor cores.  A call takes about as
+    # long as the binding's host work, so the value is taken from a CUDA graph
+    # of 10 calls that alternate between two copies of B (each call reads the B
+    # the previous call did not: nothing of it is left in L2); us_per_call is
+    # the same call made directly, back to back.
     Bs = workloads.gemm_bf16(device=dev)["B"]
-    for rows in (1, 16):
+    Bs2 = Bs.clone()
+    reps = 10
+    for rows in (1, 4, 16):
         As = (torch.randn((rows, 8192), generator=torch.Generator(device=dev).manual_seed(rows), device=dev)
               / math.sqrt(8192)).to(torch.bfloat16)
         Ys = torch.empty((rows, 8192), dtype=torch.bfloat16, device=dev)
-        ms, _ = time_loop(lambda: qg.mm_gemm(As, Bs, None, 1.0, 1.0, 0, 1, out=Ys), 50, 5, world, stream,
-                          idle_s=EXTRA_IDLE_S)
-        assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+        ms_call, _ = time_loop(lambda: qg.mm_gemm(As, Bs, None, 1.0, 1.0, 0, 1, out=Ys), 50, 5, world, stream,
+                               idle_s=EXTRA_IDLE_S)
+        path = qg.mm_last_path()
+        assert path == (qg.MM_PATH_VECTOR if rows <= 4 else qg.MM_PATH_TENSOR)
+
+        def calls():
+            for i in range(reps):
+                qg.mm_gemm(As, (Bs, Bs2)[i % 2], None, 1.0, 1.0, 0, 1, out=Ys)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            calls()
+        torch.cuda.synchronize()
+        ms_graph, _ = time_loop(graph.replay, 10, 3, world, torch.cuda.current_stream(dev))
+        ms = ms_graph / reps
         nbytes = 2 * (rows * 8192 + 8192 * 8192 + rows * 8192)
         out["gemm_bf16_skinny_m%d" % rows] = {
-            "value": nbytes / ms / 1e6, "unit": "GB/s", "us_per_call": ms * 1e3, "bound": "hbm", "peak_gbs": hbm,
+            "value": nbytes / ms / 1e6, "unit": "GB/s", "us_per_call_in_graph": ms * 1e3,
+            "us_per_call": ms_call * 1e3, "bound": "hbm", "peak_gbs": hbm,
             "frac": nbytes / ms / 1e6 / hbm, "tflops": 2 * rows * 8192 * 8192 / ms / 1e9, "kernels_per_call": 1,
-            "shape": "[%d, 8192] @ B^T, B [8192, 8192] bf16" % rows, "l2": "B (134 MB) larger than L2"}
-        del As, Ys
-    del Bs
+            "kernel": "vec_gemm_kernel" if path == qg.MM_PATH_VECTOR else "tc_gemm_kernel<kSkinny>",
+            "shape": "[%d, 8192] @ B^T, B [8192, 8192] bf16" % rows,
+            "l2": "each call in the graph reads the copy of B the previous call did not"}
+        del As, Ys, graph
+    del Bs, Bs2
     torch.cuda.empty_cache()
 
     # 2b. The headline Gemm in fp32 (three tf32 tensor-core products per step).

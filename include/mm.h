@@ -75,7 +75,9 @@ typedef enum mm_path {
   MM_PATH_AUTO = 0,    /* policy only: let the planner choose */
   MM_PATH_SIMT = 1,    /* CUDA-core kernels (every type, every stride pattern) */
   MM_PATH_TENSOR = 2,  /* tcgen05 tensor-core kernels (bf16/f16, fp32 as three tf32 products, 8-bit quantized operands) */
-  MM_PATH_NONE = 3     /* result only: no kernel was needed (an empty output) */
+  MM_PATH_NONE = 3,    /* result only: no kernel was needed (an empty output) */
+  MM_PATH_VECTOR = 4   /* MatMul/Gemm with 1 to 4 rows of A' (bf16/f16/f32, k contiguous in A' and B',
+                          16-byte aligned rows of A' and columns of B'): one pass over B' on the CUDA cores */
 } mm_path;
 
 /* Human-readable name of a status code; never NULL. */
@@ -85,9 +87,13 @@ const char* mm_status_string(mm_status status);
 const char* mm_version(void);
 
 /* Process-wide planner policy (MM_PATH_AUTO by default).  MM_PATH_SIMT forces
- * the CUDA-core kernels; MM_PATH_TENSOR forces the tensor-core kernels and
- * makes calls they cannot run return MM_ERR_UNSUPPORTED.  Meant for tests and
- * measurements.  Returns MM_ERR_INVALID_ARG for an unknown value. */
+ * the CUDA-core tile kernels; MM_PATH_TENSOR forces the tensor-core kernels and
+ * makes calls they cannot run return MM_ERR_UNSUPPORTED.  MM_PATH_VECTOR forces
+ * the few-row kernel for MatMul and Gemm (MM_ERR_UNSUPPORTED where it does not
+ * apply) and acts as MM_PATH_AUTO for the other operators.  Under
+ * MM_PATH_AUTO every MatMul/Gemm call the few-row kernel takes goes to it.
+ * Meant for tests and measurements.  Returns MM_ERR_INVALID_ARG for an unknown
+ * value. */
 mm_status mm_set_path_policy(int32_t policy);
 
 /* The mm_path taken by the most recent successful compute call made on the

@@ -20,11 +20,11 @@ __all__ = [
     "library_path",
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "mm_grouped_matmul_qweights", "mm_grouped_matmul_qweights_workspace_size",
-    "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE",
+    "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE", "MM_PATH_VECTOR",
 ]
 
 MM_MAX_DIMS = 8
-MM_PATH_AUTO, MM_PATH_SIMT, MM_PATH_TENSOR, MM_PATH_NONE = 0, 1, 2, 3
+MM_PATH_AUTO, MM_PATH_SIMT, MM_PATH_TENSOR, MM_PATH_NONE, MM_PATH_VECTOR = 0, 1, 2, 3, 4
 _STATUS = ["MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_SHAPE", "MM_ERR_DTYPE", "MM_ERR_UNSUPPORTED",
            "MM_ERR_WORKSPACE", "MM_ERR_CUDA", "MM_ERR_TIMEOUT", "MM_ERR_INDEX_RANGE"]
 

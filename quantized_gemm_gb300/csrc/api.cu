@@ -176,6 +176,22 @@ mm_status finish(mm_status s, int path) {
   return s;
 }
 
+// MatMul and Gemm after validation: the few-row kernel where it applies (policy
+// MM_PATH_AUTO, or forced by MM_PATH_VECTOR), else the tensor-core or the
+// CUDA-core tiles.
+mm_status run_dense(const GemmArgs& g, bool pays, cudaStream_t st) {
+  const int pol = g_policy.load();
+  const bool vec_ok = vec_gemm_supported(g);
+  if (pol == MM_PATH_VECTOR || (pol == MM_PATH_AUTO && vec_ok)) {
+    if (!vec_ok) return MM_ERR_UNSUPPORTED;
+    return finish(launch_vec_gemm(g, st), MM_PATH_VECTOR);
+  }
+  const int path = choose(tc_gemm_supported(g), pays);
+  if (path < 0) return MM_ERR_UNSUPPORTED;
+  if (path == MM_PATH_TENSOR) return finish(launch_tc_gemm(g, device_status_ptr(), st), MM_PATH_TENSOR);
+  return finish(launch_simt_gemm(g, st), MM_PATH_SIMT);
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,7 +214,8 @@ const char* mm_status_string(mm_status s) {
 const char* mm_version(void) { return "0.1.0"; }
 
 mm_status mm_set_path_policy(int32_t policy) {
-  if (policy != MM_PATH_AUTO && policy != MM_PATH_SIMT && policy != MM_PATH_TENSOR) return MM_ERR_INVALID_ARG;
+  if (policy != MM_PATH_AUTO && policy != MM_PATH_SIMT && policy != MM_PATH_TENSOR && policy != MM_PATH_VECTOR)
+    return MM_ERR_INVALID_ARG;
   g_policy.store(policy);
   return MM_OK;
 }
@@ -237,12 +254,7 @@ mm_status mm_matmul(const mm_tensor* A, const mm_tensor* B, const mm_tensor* Y, 
   g.c.ptr = nullptr;
   g.y = output_view(Y, p, A->ndim == 1, B->ndim == 1);
   g.alpha = 1.f; g.beta = 0.f; g.alpha_d = 1.0; g.beta_d = 0.0; g.alpha_i = 1; g.beta_i = 0;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool tc_ok = tc_gemm_supported(g);
-  const int path = choose(tc_ok, tensor_pays_dense(g.dtype, p.M, p.N, p.K, p.bm.count));
-  if (path < 0) return MM_ERR_UNSUPPORTED;
-  if (path == MM_PATH_TENSOR) return finish(launch_tc_gemm(g, device_status_ptr(), st), MM_PATH_TENSOR);
-  return finish(launch_simt_gemm(g, st), MM_PATH_SIMT);
+  return run_dense(g, tensor_pays_dense(g.dtype, p.M, p.N, p.K, p.bm.count), static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ Gemm
@@ -308,11 +320,7 @@ mm_status mm_gemm(const mm_tensor* A, const mm_tensor* B, const mm_tensor* C, fl
   }
   g.alpha = alpha; g.beta = beta; g.alpha_d = (double)alpha; g.beta_d = (double)beta;
   if (M == 0 || N == 0) return finish(MM_OK, MM_PATH_NONE);
-  cudaStream_t stp = static_cast<cudaStream_t>(stream);
-  const int path = choose(tc_gemm_supported(g), tensor_pays_dense(g.dtype, M, N, K, 1));
-  if (path < 0) return MM_ERR_UNSUPPORTED;
-  if (path == MM_PATH_TENSOR) return finish(launch_tc_gemm(g, device_status_ptr(), stp), MM_PATH_TENSOR);
-  return finish(launch_simt_gemm(g, stp), MM_PATH_SIMT);
+  return run_dense(g, tensor_pays_dense(g.dtype, M, N, K, 1), static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ QLinearMatMul

@@ -58,6 +58,12 @@ struct GroupedArgs {
 };
 
 mm_status launch_simt_gemm(const GemmArgs& args, cudaStream_t stream);
+// Products with at most kVecMaxRows rows of A', k contiguous in A' and B' and
+// 16-byte aligned rows/columns (bf16, f16, f32): one pass over B' on the CUDA
+// cores.  vec_gemm_supported says whether launch_vec_gemm takes the call.
+constexpr int kVecMaxRows = 4;
+bool vec_gemm_supported(const GemmArgs& args);
+mm_status launch_vec_gemm(const GemmArgs& args, cudaStream_t stream);
 mm_status launch_simt_qlinear(const QLinearArgs& args, cudaStream_t stream);
 mm_status launch_simt_grouped(const GroupedArgs& args, unsigned* status, cudaStream_t stream);
 

@@ -7,6 +7,9 @@
 // outputs each, strided by 16 so shared-memory reads are conflict-free and
 // global stores are coalesced along the row); K is staged through shared
 // memory 16 at a time with plain strided loads.
+#include <atomic>
+#include <cstring>
+
 #include "kernels.h"
 
 namespace qg {
@@ -180,6 +183,212 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmArgs p) {
       }
     }
   }
+}
+
+// ------------------------------------------------------------------ few-row products
+
+// With at most 4 rows of A' a product reads each element of B' once and does
+// 1 to 4 multiply-adds with it: one pass over B' at memory speed.  This kernel
+// takes B' K-major (column n of B' contiguous in k, as for weights stored
+// [N, K]) and A' with k contiguous.  A warp owns a few adjacent columns; each
+// lane loads 16-byte pieces (8 values of k; 4 for fp32) of every column, a
+// round of several pieces of each before it uses any, and the same pieces of
+// the rows of A' (read by every warp: they stay in L1, while the stream over
+// B' bypasses it), and accumulates in fp32 (FFMA, never TF32).  The lanes'
+// partial sums are added with shuffles.  The launch gives every warp the same
+// number of column groups, so no warp is left streaming alone at the end.
+constexpr int kVecWarps = 4;   // warps per block
+
+// Columns per warp, pieces per column in a round, and whether the pieces of
+// A' are loaded as they are used (L1 hits) instead of with the round: the
+// fastest of 8 shapes timed on 1, 2 and 4 x 8192 x 8192 bf16 products.
+template <int MT> struct VecShape {
+  static constexpr int cols = MT == 4 ? 4 : 2;
+  static constexpr int steps = MT == 4 ? 8 : 16;
+  static constexpr bool a_late = MT < 4;
+};
+
+// One 16-byte piece of B', read once: not kept in L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// acc + the dot product of two 16-byte pieces of T values, in fp32.
+template <typename T> __device__ __forceinline__ float dot16(float acc, uint4 a, uint4 b);
+template <> __device__ __forceinline__ float dot16<__nv_bfloat16>(float acc, uint4 a, uint4 b) {
+  const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {   // a bf16 value is the upper half of its fp32 pattern
+    acc = __fmaf_rn(__uint_as_float(x[j] << 16), __uint_as_float(y[j] << 16), acc);
+    acc = __fmaf_rn(__uint_as_float(x[j] & 0xffff0000u), __uint_as_float(y[j] & 0xffff0000u), acc);
+  }
+  return acc;
+}
+template <> __device__ __forceinline__ float dot16<__half>(float acc, uint4 a, uint4 b) {
+  const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __half2 hx, hy;
+    memcpy(&hx, &x[j], 4);
+    memcpy(&hy, &y[j], 4);
+    const float2 fx = __half22float2(hx), fy = __half22float2(hy);
+    acc = __fmaf_rn(fx.x, fy.x, acc);
+    acc = __fmaf_rn(fx.y, fy.y, acc);
+  }
+  return acc;
+}
+template <> __device__ __forceinline__ float dot16<float>(float acc, uint4 a, uint4 b) {
+  acc = __fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), acc);
+  acc = __fmaf_rn(__uint_as_float(a.y), __uint_as_float(b.y), acc);
+  acc = __fmaf_rn(__uint_as_float(a.z), __uint_as_float(b.z), acc);
+  return __fmaf_rn(__uint_as_float(a.w), __uint_as_float(b.w), acc);
+}
+
+// Warp w takes the column groups t = w, w + warps, ... of groups x batches
+// (group t: batch t / groups, columns kVecCols * (t % groups) + 0 .. kVecCols - 1).
+template <typename T, int MT>
+__global__ void __launch_bounds__(kVecWarps * 32) vec_gemm_kernel(const GemmArgs p, int64_t groups, int64_t tasks,
+                                                                  int64_t warps) {
+  constexpr int kVecCols = VecShape<MT>::cols;
+  constexpr int U = VecShape<MT>::steps;
+  constexpr int kPiece = 16 / (int)sizeof(T);   // values of k in a 16-byte piece
+  constexpr int kStep = 32 * kPiece;            // values of k a warp covers per piece
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * kVecWarps + (threadIdx.x >> 5);
+  if (w >= warps) return;
+  const T* A = static_cast<const T*>(p.a.ptr);
+  const T* B = static_cast<const T*>(p.b.ptr);
+  const T* C = static_cast<const T*>(p.c.ptr);
+  T* Y = static_cast<T*>(const_cast<void*>(p.y.ptr));
+  const int64_t kmain = p.K / (kStep * U) * (kStep * U);
+  for (int64_t t = w; t < tasks; t += warps) {
+    const int64_t bt = t / groups, n0 = (t - bt * groups) * kVecCols;
+    const T* Ab = A + batch_offset(p.bm, p.a.bstride, bt);
+    const T* Bb = B + batch_offset(p.bm, p.b.bstride, bt);
+    const T* col[kVecCols];
+#pragma unroll
+    for (int r = 0; r < kVecCols; ++r) col[r] = Bb + (n0 + r < p.N ? n0 + r : p.N - 1) * p.b.cs;   // past N: never stored
+    const T* row[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) row[m] = Ab + (m < p.M ? m : p.M - 1) * p.a.rs;
+    float acc[MT][kVecCols];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < kVecCols; ++r) acc[m][r] = 0.f;
+
+    // Every lane runs the same number of these rounds: U pieces per column.
+    for (int64_t k0 = (int64_t)kPiece * lane; k0 < kmain; k0 += kStep * U) {
+      uint4 bv[U][kVecCols];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int r = 0; r < kVecCols; ++r) bv[u][r] = ld_stream(col[r] + k0 + u * kStep);
+      if constexpr (VecShape<MT>::a_late) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(row[m] + k0 + u * kStep));
+#pragma unroll
+            for (int r = 0; r < kVecCols; ++r) acc[m][r] = dot16<T>(acc[m][r], a, bv[u][r]);
+          }
+      } else {
+        uint4 av[U][MT];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int m = 0; m < MT; ++m) av[u][m] = __ldg(reinterpret_cast<const uint4*>(row[m] + k0 + u * kStep));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < kVecCols; ++r) acc[m][r] = dot16<T>(acc[m][r], av[u][m], bv[u][r]);
+      }
+    }
+    // The rest of k: whole pieces, then a ragged last piece value by value.
+    for (int64_t k = kmain + (int64_t)kPiece * lane; k < p.K; k += kStep) {
+      if (k + kPiece <= p.K) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint4 a = __ldg(reinterpret_cast<const uint4*>(row[m] + k));
+#pragma unroll
+          for (int r = 0; r < kVecCols; ++r) acc[m][r] = dot16<T>(acc[m][r], a, ld_stream(col[r] + k));
+        }
+      } else {
+        for (int64_t j = k; j < p.K; ++j)
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < kVecCols; ++r)
+              acc[m][r] = __fmaf_rn(Arith<T>::load(row[m] + j), Arith<T>::load(col[r] + j), acc[m][r]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < kVecCols; ++r)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[m][r] += __shfl_xor_sync(0xffffffffu, acc[m][r], o);
+    // Lane kVecCols * m + r stores output (m, n0 + r).
+    const T* Cb = C ? C + batch_offset(p.bm, p.c.bstride, bt) : nullptr;
+    T* Yb = Y + batch_offset(p.bm, p.y.bstride, bt);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < kVecCols; ++r) {
+        const int64_t n = n0 + r;
+        if (lane == kVecCols * m + r && m < p.M && n < p.N) {
+          const T* c = Cb ? Cb + m * p.c.rs + n * p.c.cs : nullptr;
+          Yb[m * p.y.rs + n * p.y.cs] = Arith<T>::store(Epi<T>::apply(p, acc[m][r], c));
+        }
+      }
+  }
+}
+
+int device_sm_count() {
+  static std::atomic<int> counts[128];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  int c = counts[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) return 0;
+    counts[dev].store(c, std::memory_order_relaxed);
+  }
+  return c;
+}
+
+template <typename T, int MT>
+mm_status launch_vec(const GemmArgs& p, cudaStream_t stream) {
+  static std::atomic<int> resident{0};   // blocks of this kernel one SM holds
+  int per_sm = resident.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vec_gemm_kernel<T, MT>, kVecWarps * 32, 0) !=
+            cudaSuccess || per_sm <= 0)
+      return MM_ERR_CUDA;
+    resident.store(per_sm, std::memory_order_relaxed);
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return MM_ERR_CUDA;
+  const int64_t groups = (p.N + VecShape<MT>::cols - 1) / VecShape<MT>::cols;
+  const int64_t tasks = groups * p.bm.count;
+  const int64_t wmax = (int64_t)sms * per_sm * kVecWarps;
+  const int64_t rounds = (tasks + wmax - 1) / wmax;
+  const int64_t warps = (tasks + rounds - 1) / rounds;   // every warp runs rounds or rounds - 1 groups
+  const int64_t blocks = (warps + kVecWarps - 1) / kVecWarps;
+  vec_gemm_kernel<T, MT><<<(unsigned)blocks, kVecWarps * 32, 0, stream>>>(p, groups, tasks, warps);
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+template <typename T>
+mm_status launch_vec_t(const GemmArgs& p, cudaStream_t stream) {
+  if (p.M == 1) return launch_vec<T, 1>(p, stream);
+  if (p.M == 2) return launch_vec<T, 2>(p, stream);
+  return launch_vec<T, 4>(p, stream);
 }
 
 // ------------------------------------------------------------------ QLinear
@@ -362,6 +571,29 @@ mm_status launch_simt_gemm(const GemmArgs& p, cudaStream_t stream) {
     default: return MM_ERR_DTYPE;
   }
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+bool vec_gemm_supported(const GemmArgs& p) {
+  if (p.dtype != MM_BF16 && p.dtype != MM_F16 && p.dtype != MM_F32) return false;
+  if (p.M < 1 || p.M > kVecMaxRows || p.N < 1 || p.K < 1) return false;
+  // k contiguous in both operands; 16-byte aligned columns of B' and rows of A'.
+  const int64_t e = p.dtype == MM_F32 ? 4 : 2, v = 16 / e;
+  if (p.b.rs != 1 || p.a.cs != 1) return false;
+  if (reinterpret_cast<uintptr_t>(p.b.ptr) % 16 || reinterpret_cast<uintptr_t>(p.a.ptr) % 16) return false;
+  if ((p.N > 1 && p.b.cs % v) || (p.M > 1 && p.a.rs % v)) return false;
+  for (int d = 0; d < p.bm.nb; ++d)
+    if (p.bm.shape[d] > 1 && (p.b.bstride[d] % v || p.a.bstride[d] % v)) return false;
+  return p.N <= (int64_t(1) << 40) / (p.bm.count > 0 ? p.bm.count : 1);   // column groups x batches in range
+}
+
+mm_status launch_vec_gemm(const GemmArgs& p, cudaStream_t stream) {
+  if (p.M == 0 || p.N == 0 || p.bm.count == 0) return MM_OK;
+  switch (p.dtype) {
+    case MM_BF16: return launch_vec_t<__nv_bfloat16>(p, stream);
+    case MM_F16: return launch_vec_t<__half>(p, stream);
+    case MM_F32: return launch_vec_t<float>(p, stream);
+    default: return MM_ERR_DTYPE;
+  }
 }
 
 mm_status launch_simt_qlinear(const QLinearArgs& p, cudaStream_t stream) {

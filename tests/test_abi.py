@@ -153,7 +153,8 @@ def test_qlinear_validation(lib):
 
 def test_policy_and_status_strings(lib):
     assert lib.mm_set_path_policy(7) == 1
-    for p in (1, 2, 0):
+    assert lib.mm_set_path_policy(3) == 1          # MM_PATH_NONE is a result, not a policy
+    for p in (1, 2, 4, 0):
         assert lib.mm_set_path_policy(p) == 0
     for s in range(9):
         assert lib.mm_status_string(s)

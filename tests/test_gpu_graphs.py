@@ -5,8 +5,8 @@ in a CUDA graph once and replays it, paying one graph launch instead of one
 host call per kernel.  The calls enqueue only kernels and asynchronous
 memsets on the caller's stream, so after a first call on the device (which
 caches per-device properties such as the SM count) they can be captured.
-These tests capture Gemm (tensor-core and CUDA-core paths), QLinearMatMul and
-GroupedMatMul with caller-provided outputs and workspaces, replay the graph
+These tests capture Gemm (tensor-core, CUDA-core and few-row paths),
+QLinearMatMul and GroupedMatMul with caller-provided outputs and workspaces, replay the graph
 twice on new input values, and compare every output bit for bit with direct
 calls on the same inputs.
 """
@@ -53,9 +53,11 @@ def test_products_captured_in_a_cuda_graph_match_direct_calls():
     w = rand_tensor((6, 512, 264), torch.bfloat16, 67, DEV)
     bias = rand_tensor((6, 264), torch.bfloat16, 68, DEV)
     gi = torch.from_numpy(np.random.default_rng(69).integers(0, 6, (400, 2)).astype(np.int32)).to(DEV)
+    Av = rand_tensor((2, 1024), torch.bfloat16, 72, DEV)     # two rows: the few-row kernel
 
     Y = torch.empty((640, 520), dtype=torch.bfloat16, device=DEV)
     Yf = torch.empty((96, 40), dtype=torch.float32, device=DEV)
+    Yv = torch.empty((2, 520), dtype=torch.bfloat16, device=DEV)
     yq = torch.empty((300, 264), dtype=torch.int8, device=DEV)
     wsq = torch.empty(qg.mm_qlinear_matmul_workspace_size(q["a"], q["b"]), dtype=torch.uint8, device=DEV)
     out = torch.empty((400, 2, 264), dtype=torch.bfloat16, device=DEV)
@@ -66,10 +68,12 @@ def test_products_captured_in_a_cuda_graph_match_direct_calls():
         qg.mm_matmul(Af, Bf, out=Yf)
         qg.mm_qlinear_matmul(*[q[k] for k in QKEYS], out=yq, workspace=wsq)
         qg.mm_grouped_matmul(x, w, gi, bias, out=out, workspace=wsg)
+        qg.mm_gemm(Av, B, C, 1.0, -1.0, 0, 1, out=Yv)
 
     def direct():
         return (qg.mm_gemm(A, B, C, 0.5, 2.0, 0, 1), qg.mm_matmul(Af, Bf),
-                qg.mm_qlinear_matmul(*[q[k] for k in QKEYS]), qg.mm_grouped_matmul(x, w, gi, bias))
+                qg.mm_qlinear_matmul(*[q[k] for k in QKEYS]), qg.mm_grouped_matmul(x, w, gi, bias),
+                qg.mm_gemm(Av, B, C, 1.0, -1.0, 0, 1))
 
     # First calls on the device, outside any capture, on a side stream as
     # torch's capture does.
@@ -86,7 +90,7 @@ def test_products_captured_in_a_cuda_graph_match_direct_calls():
 
     for seed in (70, 71):
         g = np.random.default_rng(seed)
-        for t in (A, B, C, x, w, bias):
+        for t in (A, B, C, x, w, bias, Av):
             t.copy_(torch.from_numpy(g.standard_normal(tuple(t.shape))).to(t.dtype))
         for t in (Af, Bf):
             t.copy_(torch.from_numpy(g.standard_normal(tuple(t.shape))).to(t.dtype))
@@ -97,6 +101,6 @@ def test_products_captured_in_a_cuda_graph_match_direct_calls():
         torch.cuda.synchronize()
         want = direct()
         torch.cuda.synchronize()
-        for got, ref in zip((Y, Yf, yq, out), want):
+        for got, ref in zip((Y, Yf, yq, out, Yv), want):
             assert torch.equal(got, ref)
     assert qg.mm_get_device_status() == "MM_OK"

@@ -1,15 +1,22 @@
-"""Vector-matrix products (one row of A') on the tensor cores, against the oracle.
+"""Products with few rows of A', against the oracle.
 
 A one-row A' (Gemm with M = 1, MatMul's promoted 1-D A, A stored [K, 1] with
 transA) is a K-major tile whatever its row stride: the tensor-core kernels
 take it as a 128-row tile whose other rows read the fill value and are never
 stored.  These tests cover both layouts of B', ragged N and K, every C
-broadcast shape, a broadcast batch, fp32 (three tf32 products), and check
-that the planner sends large one-row products to the tensor cores.
+broadcast shape, a broadcast batch and fp32 (three tf32 products) there.
+
+Products with 1 to 4 rows whose operands are contiguous along k also have a
+CUDA-core kernel that streams B' once (MM_PATH_VECTOR), which the planner
+prefers: the second half covers it with every row count, odd and ragged N,
+ragged K (padded views, so a last piece of fewer than 8 values), C shapes,
+broadcast batches, promoted vectors and the three float types, and checks
+which path the planner takes.
 """
 
 import contextlib
 
+import numpy as np
 import pytest
 import torch
 
@@ -89,7 +96,128 @@ def test_gemm_one_row_fp32_three_tf32():
         _gemm_check(A, B, rand_tensor((N,), torch.float32, 812, DEV), 1.0, 1.0, 0, 1)
 
 
-def test_planner_sends_large_one_row_products_to_tensor_cores():
+# ------------------------------------------------------------------ the few-row kernel
+
+@contextlib.contextmanager
+def vector_path():
+    qg.mm_set_path_policy(qg.MM_PATH_VECTOR)
+    try:
+        yield
+    finally:
+        qg.mm_set_path_policy(qg.MM_PATH_AUTO)
+
+
+def _vec_gemm_check(A, B, C, alpha, beta, tA, tB):
+    with vector_path():
+        Y = qg.mm_gemm(A, B, C, alpha, beta, tA, tB)
+    assert qg.mm_last_path() == qg.MM_PATH_VECTOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    a, b = to_np(A), to_np(B)
+    c = None if C is None else to_np(C)
+    kw = dict(alpha=alpha, beta=beta, transA=tA, transB=tB)
+    err = max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw))
+    assert err <= TOL[A.dtype], err
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32], ids=str)
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("N,K", [(520, 64), (1037, 1096), (257, 4160), (64, 8200)])
+def test_vector_gemm(dtype, M, N, K):
+    # B stored [N, K] (transB = 1): K-major B'.  K = 64 runs only the ragged
+    # loop; 4160 and 8200 full rounds of in-flight pieces plus whole pieces;
+    # odd N a last warp with one real column.
+    A = rand_tensor((M, K), dtype, 820 + M, DEV)
+    B = rand_tensor((N, K), dtype, 830, DEV)
+    C = rand_tensor((1, N), dtype, 831, DEV)
+    _vec_gemm_check(A, B, C, 0.5, 2.0, 0, 1)
+
+
+@pytest.mark.parametrize("cshape", [None, (3, 1), (3, 700), (700,), ()], ids=str)
+def test_vector_gemm_c_shapes(cshape):
+    A = rand_tensor((3, 2048), torch.bfloat16, 840, DEV)
+    B = rand_tensor((700, 2048), torch.bfloat16, 841, DEV)
+    C = None if cshape is None else rand_tensor(cshape, torch.bfloat16, 842, DEV)
+    _vec_gemm_check(A, B, C, -1.5, 0.75, 0, 1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=str)
+@pytest.mark.parametrize("K", [1, 7, 1001, 4099])
+def test_vector_gemm_ragged_k_in_padded_views(dtype, K):
+    # Rows of A and B padded to a 16-byte multiple: aligned pieces, then a last
+    # piece of K % 8 (bf16) or K % 4 (f32) values read one by one.
+    step = 16 // torch.tensor([], dtype=dtype).element_size()
+    Kp = (K + step - 1) // step * step + step
+    M, N = 4, 333
+    A = rand_tensor((M, Kp), dtype, 850, DEV)[:, :K]
+    B = rand_tensor((N, Kp), dtype, 851, DEV)[:, :K]
+    _vec_gemm_check(A, B, rand_tensor((N,), dtype, 852, DEV), 1.0, 1.0, 0, 1)
+
+
+def test_vector_gemm_transposed_a_stored_as_column():
+    # transA = 1 with A stored [K, 1]: A' is one row with k contiguous.
+    K, N = 3000, 1000
+    A = rand_tensor((K, 1), torch.float16, 853, DEV)
+    B = rand_tensor((N, K), torch.float16, 854, DEV)
+    _vec_gemm_check(A, B, None, 2.0, 0.0, 1, 1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=str)
+def test_vector_matmul_batched_and_promoted(dtype):
+    # A [2, 3, K] @ a K-major view of B [2, 1, N, K] (B broadcast over dim 1),
+    # a promoted vector [K] @ K-major views, and N = 1 (a [K, 1] B).
+    K, N = 2056, 264
+    cases = [
+        (rand_tensor((2, 3, K), dtype, 860, DEV), rand_tensor((2, 1, N, K), dtype, 861, DEV).transpose(-1, -2)),
+        (rand_tensor((K,), dtype, 862, DEV), rand_tensor((N, K), dtype, 863, DEV).t()),
+        (rand_tensor((K,), dtype, 864, DEV), rand_tensor((5, N, K), dtype, 865, DEV).transpose(-1, -2)),
+        (rand_tensor((2, K), dtype, 866, DEV), rand_tensor((K, 1), dtype, 867, DEV)),
+    ]
+    for a, B in cases:
+        with vector_path():
+            Y = qg.mm_matmul(a, B)
+        assert qg.mm_last_path() == qg.MM_PATH_VECTOR
+        an, bn = to_np(a), to_np(B)
+        assert max_rel_err(to_np(Y), oracle.matmul(an, bn), oracle.matmul_abs_scale(an, bn)) <= TOL[dtype]
+
+
+def test_vector_gemm_large_is_exact_on_integer_inputs():
+    # Small integers in fp32: every product and partial sum is exact, so the
+    # result is the oracle's bit for bit, whatever the order of the additions.
+    g = torch.Generator().manual_seed(870)
+    A = torch.randint(-3, 4, (2, 8192), generator=g).to(torch.float32).to(DEV)
+    B = torch.randint(-3, 4, (8192, 8192), generator=g).to(torch.float32).to(DEV)
+    with vector_path():
+        Y = qg.mm_gemm(A, B, None, 1.0, 1.0, 0, 1)
+    assert qg.mm_last_path() == qg.MM_PATH_VECTOR
+    assert np.array_equal(to_np(Y), oracle.gemm(to_np(A), to_np(B), None, transB=1))
+
+
+def test_vector_path_rejects_what_it_does_not_take():
+    A = rand_tensor((5, 256), torch.bfloat16, 871, DEV)          # 5 rows
+    B = rand_tensor((64, 256), torch.bfloat16, 872, DEV)
+    A2 = rand_tensor((2, 256), torch.bfloat16, 873, DEV)
+    B2 = rand_tensor((256, 64), torch.bfloat16, 874, DEV)        # MN-major B' (transB = 0)
+    A3 = rand_tensor((2, 256), torch.float64, 875, DEV)
+    B3 = rand_tensor((64, 256), torch.float64, 876, DEV)          # f64
+    A4 = rand_tensor((2, 260), torch.bfloat16, 877, DEV)[:, 1:257]  # rows start off a 16-byte boundary
+    for a, b, tB in ((A, B, 1), (A2, B2, 0), (A3, B3, 1), (A4, B, 1)):
+        with vector_path():
+            with pytest.raises(qg.MMError) as e:
+                qg.mm_gemm(a, b, None, 1.0, 1.0, 0, tB)
+        assert e.value.name == "MM_ERR_UNSUPPORTED"
+
+
+def test_planner_paths_for_few_row_products():
+    # K-major B' with 1-4 rows: the few-row kernel; MN-major B' and 5 or more
+    # rows: the tensor cores.
     A = rand_tensor((1, 4096), torch.bfloat16, 813, DEV)
     B = rand_tensor((4096, 4096), torch.bfloat16, 814, DEV)
-    _gemm_check(A, B, None, 1.0, 1.0, 0, 1)
+    a, b = to_np(A), to_np(B)
+    for tB, path in ((1, qg.MM_PATH_VECTOR), (0, qg.MM_PATH_TENSOR)):
+        Y = qg.mm_gemm(A, B, None, 1.0, 1.0, 0, tB)
+        assert qg.mm_last_path() == path
+        err = max_rel_err(to_np(Y), oracle.gemm(a, b, None, transB=tB), oracle.gemm_abs_scale(a, b, None, transB=tB))
+        assert err <= TOL[torch.bfloat16], err
+    A8 = rand_tensor((8, 4096), torch.bfloat16, 815, DEV)
+    qg.mm_gemm(A8, B, None, 1.0, 1.0, 0, 1)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
