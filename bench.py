@@ -644,7 +644,11 @@ def run_profile_workload(args):
         Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
         step = lambda: qg.mm_gemm(d["A"], d["B"], d["C"], d["alpha"], d["beta"], 0, 1, out=Yf)
     elif name.startswith("gemm_bf16_skinny_m"):
-        rows = int(name[len("gemm_bf16_skinny_m"):])          # [rows, 8192] @ B^T, B the headline's
+        # [rows, 8192] @ B^T, B the headline's; a _tensor suffix forces the
+        # tensor-core kernel where the planner would take the few-row one
+        rows = int(name[len("gemm_bf16_skinny_m"):].split("_")[0])
+        if name.endswith("_tensor"):
+            qg.mm_set_path_policy(qg.MM_PATH_TENSOR)
         Bs = workloads.gemm_bf16(device=dev)["B"]
         As = (torch.randn((rows, 8192), device=dev) / math.sqrt(8192)).to(torch.bfloat16)
         Ys = torch.empty((rows, 8192), dtype=torch.bfloat16, device=dev)
@@ -695,7 +699,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--profile-workload", default=None,
-                    help="run only this workload (gemm_bf16, gemm_bf16_skinny_mR, matmul_bf16_bcast, qlinear_s8 or a "
+                    help="run only this workload (gemm_bf16, gemm_bf16_skinny_mR[_tensor], matmul_bf16_bcast, qlinear_s8 or a "
                          "QLinear variant, "
                          "grouped_bf16[_gG][_nN])")
     args = ap.parse_args()
