@@ -76,8 +76,10 @@ typedef enum mm_path {
   MM_PATH_SIMT = 1,    /* CUDA-core kernels (every type, every stride pattern) */
   MM_PATH_TENSOR = 2,  /* tcgen05 tensor-core kernels (bf16/f16, fp32 as three tf32 products, 8-bit quantized operands) */
   MM_PATH_NONE = 3,    /* result only: no kernel was needed (an empty output) */
-  MM_PATH_VECTOR = 4   /* MatMul/Gemm with 1 to 4 rows of A' (bf16/f16/f32, k contiguous in A' and B',
-                          16-byte aligned rows of A' and columns of B'): one pass over B' on the CUDA cores */
+  MM_PATH_VECTOR = 4   /* MatMul/Gemm with 1 to 4 rows of A' (bf16/f16/f32) and B' either K-major (k
+                          contiguous in A' and B', 16-byte aligned rows of A' and columns of B') or
+                          MN-major (n contiguous, 16-byte aligned rows of B'): one pass over B' on the
+                          CUDA cores */
 } mm_path;
 
 /* Human-readable name of a status code; never NULL. */
@@ -91,7 +93,9 @@ const char* mm_version(void);
  * makes calls they cannot run return MM_ERR_UNSUPPORTED.  MM_PATH_VECTOR forces
  * the few-row kernel for MatMul and Gemm (MM_ERR_UNSUPPORTED where it does not
  * apply) and acts as MM_PATH_AUTO for the other operators.  Under
- * MM_PATH_AUTO every MatMul/Gemm call the few-row kernel takes goes to it.
+ * MM_PATH_AUTO the few-row kernels take every MatMul/Gemm call they can run,
+ * except 3 or 4 rows of bf16/f16 against MN-major B' (the tensor cores are as
+ * fast there).
  * Meant for tests and measurements.  Returns MM_ERR_INVALID_ARG for an unknown
  * value. */
 mm_status mm_set_path_policy(int32_t policy);

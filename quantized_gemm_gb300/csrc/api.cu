@@ -181,9 +181,8 @@ mm_status finish(mm_status s, int path) {
 // CUDA-core tiles.
 mm_status run_dense(const GemmArgs& g, bool pays, cudaStream_t st) {
   const int pol = g_policy.load();
-  const bool vec_ok = vec_gemm_supported(g);
-  if (pol == MM_PATH_VECTOR || (pol == MM_PATH_AUTO && vec_ok)) {
-    if (!vec_ok) return MM_ERR_UNSUPPORTED;
+  if (pol == MM_PATH_VECTOR || (pol == MM_PATH_AUTO && vec_gemm_preferred(g))) {
+    if (!vec_gemm_supported(g)) return MM_ERR_UNSUPPORTED;
     return finish(launch_vec_gemm(g, st), MM_PATH_VECTOR);
   }
   const int path = choose(tc_gemm_supported(g), pays);

@@ -58,11 +58,15 @@ struct GroupedArgs {
 };
 
 mm_status launch_simt_gemm(const GemmArgs& args, cudaStream_t stream);
-// Products with at most kVecMaxRows rows of A', k contiguous in A' and B' and
-// 16-byte aligned rows/columns (bf16, f16, f32): one pass over B' on the CUDA
-// cores.  vec_gemm_supported says whether launch_vec_gemm takes the call.
+// Products with at most kVecMaxRows rows of A' (bf16, f16, f32): one pass over
+// B' on the CUDA cores, for K-major B' (k contiguous in A' and B', 16-byte
+// aligned rows of A' and columns of B') and for MN-major B' (n contiguous,
+// 16-byte aligned rows of B'; A' any strides).  vec_gemm_supported says
+// whether launch_vec_gemm takes the call, vec_gemm_preferred whether the
+// planner should send it there.
 constexpr int kVecMaxRows = 4;
 bool vec_gemm_supported(const GemmArgs& args);
+bool vec_gemm_preferred(const GemmArgs& args);
 mm_status launch_vec_gemm(const GemmArgs& args, cudaStream_t stream);
 mm_status launch_simt_qlinear(const QLinearArgs& args, cudaStream_t stream);
 mm_status launch_simt_grouped(const GroupedArgs& args, unsigned* status, cudaStream_t stream);

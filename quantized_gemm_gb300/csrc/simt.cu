@@ -10,10 +10,14 @@
 #include <atomic>
 #include <cstring>
 
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 
 namespace qg {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kTile = 64;
 constexpr int kTk = 16;
@@ -240,6 +244,31 @@ template <> __device__ __forceinline__ float dot16<__half>(float acc, uint4 a, u
   }
   return acc;
 }
+// The values of a 16-byte piece as fp32.
+template <typename T> __device__ __forceinline__ void unpack16(uint4 u, float (&f)[16 / sizeof(T)]);
+template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(uint4 u, float (&f)[8]) {
+  const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(x[j] << 16);
+    f[2 * j + 1] = __uint_as_float(x[j] & 0xffff0000u);
+  }
+}
+template <> __device__ __forceinline__ void unpack16<__half>(uint4 u, float (&f)[8]) {
+  const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __half2 h;
+    memcpy(&h, &x[j], 4);
+    const float2 v = __half22float2(h);
+    f[2 * j] = v.x;
+    f[2 * j + 1] = v.y;
+  }
+}
+template <> __device__ __forceinline__ void unpack16<float>(uint4 u, float (&f)[4]) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+
 template <> __device__ __forceinline__ float dot16<float>(float acc, uint4 a, uint4 b) {
   acc = __fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), acc);
   acc = __fmaf_rn(__uint_as_float(a.y), __uint_as_float(b.y), acc);
@@ -350,6 +379,103 @@ __global__ void __launch_bounds__(kVecWarps * 32) vec_gemm_kernel(const GemmArgs
   }
 }
 
+// B' MN-major (n contiguous: B stored [K, N], MatMul's usual layout).  A
+// cluster of kMnSplit CTAs owns 32 pieces of adjacent columns (256 columns of
+// bf16/f16, 128 of fp32) of one batch: CTA c of the cluster takes the c-th
+// slice of k, its warp w the rows w, w + kMnWarps, ... of that slice, and each
+// lane one 16-byte piece of every such row, kMnRounds rows loaded before any is
+// used.  A' (any strides) is read value by value: every lane of a warp reads
+// the same value, one broadcast load.  The warps' fp32 partial sums go to
+// shared memory and the leader CTA adds all the cluster's, in a fixed order,
+// through distributed shared memory, then applies alpha, beta and C.
+constexpr int kMnSplit = 8;    // CTAs per cluster: slices of k
+constexpr int kMnWarps = 8;    // warps per CTA
+constexpr int kMnRounds = 8;   // rows of B' per warp in flight
+
+template <typename T, int MT>
+__global__ void __cluster_dims__(kMnSplit, 1, 1) __launch_bounds__(kMnWarps * 32)
+    vec_mn_kernel(const GemmArgs p) {
+  constexpr int kPiece = 16 / (int)sizeof(T);
+  constexpr int kSpan = 32 * kPiece;   // columns of a cluster
+  __shared__ __align__(16) float part[kMnWarps][MT][kSpan];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned crank = cluster.block_rank();
+  const int64_t n0 = (int64_t)blockIdx.y * kSpan + (int64_t)lane * kPiece;   // this lane's first column
+  const int nvalid = n0 >= p.N ? 0 : (int)min((int64_t)kPiece, p.N - n0);
+  const int64_t kslice = (p.K + kMnSplit - 1) / kMnSplit;
+  const int64_t kbeg = (int64_t)crank * kslice, kend = min(p.K, kbeg + kslice);
+  const T* A = static_cast<const T*>(p.a.ptr);
+  const T* B = static_cast<const T*>(p.b.ptr);
+  const T* C = static_cast<const T*>(p.c.ptr);
+  T* Y = static_cast<T*>(const_cast<void*>(p.y.ptr));
+  for (int64_t bt = blockIdx.z; bt < p.bm.count; bt += gridDim.z) {
+    const T* Ab = A + batch_offset(p.bm, p.a.bstride, bt);
+    const T* bcol = B + batch_offset(p.bm, p.b.bstride, bt) + (nvalid > 0 ? n0 : 0);
+    const T* row[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) row[m] = Ab + (m < p.M ? m : p.M - 1) * p.a.rs;
+    float acc[MT][kPiece];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < kPiece; ++j) acc[m][j] = 0.f;
+    // The piece of row k of B' (columns past N read as zero).
+    auto piece = [&](int64_t k) -> uint4 {
+      if (nvalid == kPiece) return ld_stream(bcol + k * p.b.rs);
+      T v[kPiece];
+#pragma unroll
+      for (int j = 0; j < kPiece; ++j) v[j] = j < nvalid ? bcol[k * p.b.rs + j] : T(0.f);
+      uint4 u;
+      memcpy(&u, v, 16);
+      return u;
+    };
+    auto use = [&](int64_t k, uint4 b) {
+      float f[kPiece];
+      unpack16<T>(b, f);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float a = Arith<T>::load(row[m] + k * p.a.cs);
+#pragma unroll
+        for (int j = 0; j < kPiece; ++j) acc[m][j] = __fmaf_rn(a, f[j], acc[m][j]);
+      }
+    };
+    int64_t k = kbeg + warp;
+    for (; k + (int64_t)(kMnRounds - 1) * kMnWarps < kend; k += (int64_t)kMnRounds * kMnWarps) {
+      uint4 bv[kMnRounds];
+#pragma unroll
+      for (int u = 0; u < kMnRounds; ++u) bv[u] = piece(k + (int64_t)u * kMnWarps);
+#pragma unroll
+      for (int u = 0; u < kMnRounds; ++u) use(k + (int64_t)u * kMnWarps, bv[u]);
+    }
+    for (; k < kend; k += kMnWarps) use(k, piece(k));
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < kPiece; ++j) part[warp][m][lane * kPiece + j] = acc[m][j];
+    cluster.sync();   // every CTA's partial sums visible to the leader
+    if (crank == 0) {
+      const T* Cb = C ? C + batch_offset(p.bm, p.c.bstride, bt) : nullptr;
+      T* Yb = Y + batch_offset(p.bm, p.y.bstride, bt);
+      for (int e = threadIdx.x; e < MT * kSpan; e += kMnWarps * 32) {
+        const int m = e / kSpan, c = e - m * kSpan;
+        const int64_t n = (int64_t)blockIdx.y * kSpan + c;
+        float sum = 0.f;
+        for (int r = 0; r < kMnSplit; ++r) {
+          const float* rp = cluster.map_shared_rank(&part[0][0][0], r);
+#pragma unroll
+          for (int w = 0; w < kMnWarps; ++w) sum += rp[(w * MT + m) * kSpan + c];
+        }
+        if (m < p.M && n < p.N) {
+          const T* cp = Cb ? Cb + m * p.c.rs + n * p.c.cs : nullptr;
+          Yb[m * p.y.rs + n * p.y.cs] = Arith<T>::store(Epi<T>::apply(p, sum, cp));
+        }
+      }
+    }
+    cluster.sync();   // the leader has read every CTA's shared memory
+  }
+}
+
 int device_sm_count() {
   static std::atomic<int> counts[128];
   int dev = 0;
@@ -384,11 +510,48 @@ mm_status launch_vec(const GemmArgs& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
+template <typename T, int MT>
+mm_status launch_vec_mn(const GemmArgs& p, cudaStream_t stream) {
+  constexpr int kSpan = 32 * (16 / (int)sizeof(T));
+  const int64_t spans = (p.N + kSpan - 1) / kSpan;
+  const unsigned gz = (unsigned)(p.bm.count < 65535 ? p.bm.count : 65535);
+  vec_mn_kernel<T, MT><<<dim3(kMnSplit, (unsigned)spans, gz), kMnWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+// K-major B' (vec_gemm_kernel): k contiguous in both operands, 16-byte
+// aligned columns of B' and rows of A'.
+bool vec_kmajor(const GemmArgs& p) {
+  const int64_t v = p.dtype == MM_F32 ? 4 : 8;   // values in 16 bytes
+  if (p.b.rs != 1 || p.a.cs != 1) return false;
+  if (reinterpret_cast<uintptr_t>(p.b.ptr) % 16 || reinterpret_cast<uintptr_t>(p.a.ptr) % 16) return false;
+  if ((p.N > 1 && p.b.cs % v) || (p.M > 1 && p.a.rs % v)) return false;
+  for (int d = 0; d < p.bm.nb; ++d)
+    if (p.bm.shape[d] > 1 && (p.b.bstride[d] % v || p.a.bstride[d] % v)) return false;
+  return p.N <= (int64_t(1) << 40) / (p.bm.count > 0 ? p.bm.count : 1);   // column groups x batches in range
+}
+
+// MN-major B' (vec_mn_kernel): n contiguous in B', 16-byte aligned rows of B';
+// A' any strides.
+bool vec_mnmajor(const GemmArgs& p) {
+  const int64_t v = p.dtype == MM_F32 ? 4 : 8;
+  if (p.b.cs != 1 || reinterpret_cast<uintptr_t>(p.b.ptr) % 16) return false;
+  if (p.K > 1 && p.b.rs % v) return false;
+  for (int d = 0; d < p.bm.nb; ++d)
+    if (p.bm.shape[d] > 1 && p.b.bstride[d] % v) return false;
+  return (p.N + 32 * v - 1) / (32 * v) <= 65535;   // column spans: grid y
+}
+
 template <typename T>
 mm_status launch_vec_t(const GemmArgs& p, cudaStream_t stream) {
-  if (p.M == 1) return launch_vec<T, 1>(p, stream);
-  if (p.M == 2) return launch_vec<T, 2>(p, stream);
-  return launch_vec<T, 4>(p, stream);
+  if (vec_kmajor(p)) {
+    if (p.M == 1) return launch_vec<T, 1>(p, stream);
+    if (p.M == 2) return launch_vec<T, 2>(p, stream);
+    return launch_vec<T, 4>(p, stream);
+  }
+  if (p.M == 1) return launch_vec_mn<T, 1>(p, stream);
+  if (p.M == 2) return launch_vec_mn<T, 2>(p, stream);
+  return launch_vec_mn<T, 4>(p, stream);
 }
 
 // ------------------------------------------------------------------ QLinear
@@ -576,14 +739,14 @@ mm_status launch_simt_gemm(const GemmArgs& p, cudaStream_t stream) {
 bool vec_gemm_supported(const GemmArgs& p) {
   if (p.dtype != MM_BF16 && p.dtype != MM_F16 && p.dtype != MM_F32) return false;
   if (p.M < 1 || p.M > kVecMaxRows || p.N < 1 || p.K < 1) return false;
-  // k contiguous in both operands; 16-byte aligned columns of B' and rows of A'.
-  const int64_t e = p.dtype == MM_F32 ? 4 : 2, v = 16 / e;
-  if (p.b.rs != 1 || p.a.cs != 1) return false;
-  if (reinterpret_cast<uintptr_t>(p.b.ptr) % 16 || reinterpret_cast<uintptr_t>(p.a.ptr) % 16) return false;
-  if ((p.N > 1 && p.b.cs % v) || (p.M > 1 && p.a.rs % v)) return false;
-  for (int d = 0; d < p.bm.nb; ++d)
-    if (p.bm.shape[d] > 1 && (p.b.bstride[d] % v || p.a.bstride[d] % v)) return false;
-  return p.N <= (int64_t(1) << 40) / (p.bm.count > 0 ? p.bm.count : 1);   // column groups x batches in range
+  return vec_kmajor(p) || vec_mnmajor(p);
+}
+
+// With 3 or 4 rows of 16-bit values against MN-major B' the tensor-core
+// kernel is as fast (8192 x 8192) or faster (4096 x 14336): the planner keeps
+// those there.
+bool vec_gemm_preferred(const GemmArgs& p) {
+  return vec_gemm_supported(p) && (vec_kmajor(p) || p.dtype == MM_F32 || p.M <= 2);
 }
 
 mm_status launch_vec_gemm(const GemmArgs& p, cudaStream_t stream) {

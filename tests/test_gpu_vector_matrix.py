@@ -6,12 +6,14 @@ take it as a 128-row tile whose other rows read the fill value and are never
 stored.  These tests cover both layouts of B', ragged N and K, every C
 broadcast shape, a broadcast batch and fp32 (three tf32 products) there.
 
-Products with 1 to 4 rows whose operands are contiguous along k also have a
-CUDA-core kernel that streams B' once (MM_PATH_VECTOR), which the planner
-prefers: the second half covers it with every row count, odd and ragged N,
-ragged K (padded views, so a last piece of fewer than 8 values), C shapes,
-broadcast batches, promoted vectors and the three float types, and checks
-which path the planner takes.
+Products with 1 to 4 rows of A' also have CUDA-core kernels that stream B'
+once (MM_PATH_VECTOR), which the planner prefers: one for K-major B' (k
+contiguous in A' and B') and one for MN-major B' (n contiguous; k split over a
+cluster of CTAs whose partial sums meet in distributed shared memory).  The
+second half covers both with every row count, odd and ragged N, ragged K
+(padded views, so a last piece of fewer than 8 values; K smaller than the
+cluster), C shapes, broadcast batches, promoted vectors, strided A' and the
+three float types, and checks which path the planner takes.
 """
 
 import contextlib
@@ -196,7 +198,7 @@ def test_vector_path_rejects_what_it_does_not_take():
     A = rand_tensor((5, 256), torch.bfloat16, 871, DEV)          # 5 rows
     B = rand_tensor((64, 256), torch.bfloat16, 872, DEV)
     A2 = rand_tensor((2, 256), torch.bfloat16, 873, DEV)
-    B2 = rand_tensor((256, 64), torch.bfloat16, 874, DEV)        # MN-major B' (transB = 0)
+    B2 = rand_tensor((256, 68), torch.bfloat16, 874, DEV)[:, :64]  # MN-major B', rows 136 bytes apart
     A3 = rand_tensor((2, 256), torch.float64, 875, DEV)
     B3 = rand_tensor((64, 256), torch.float64, 876, DEV)          # f64
     A4 = rand_tensor((2, 260), torch.bfloat16, 877, DEV)[:, 1:257]  # rows start off a 16-byte boundary
@@ -207,13 +209,60 @@ def test_vector_path_rejects_what_it_does_not_take():
         assert e.value.name == "MM_ERR_UNSUPPORTED"
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32], ids=str)
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("N,K", [(520, 64), (1037, 1096), (264, 5), (64, 8200)])
+def test_vector_gemm_mn_major(dtype, M, N, K):
+    # B stored [K, N] (transB = 0): MN-major B'.  N = 1037 ends in a lane with
+    # a partial piece; K = 5 leaves most CTAs of the cluster without rows;
+    # K = 1096 and 8200 give every warp full rounds and single rows.
+    A = rand_tensor((M, K), dtype, 880 + M, DEV)
+    B = rand_tensor((K, (N + 7) // 8 * 8), dtype, 885, DEV)[:, :N]   # rows 16-byte aligned
+    C = rand_tensor((N,), dtype, 886, DEV)
+    _vec_gemm_check(A, B, C, 0.5, 2.0, 0, 0)
+
+
+def test_vector_gemm_mn_major_strided_a_and_c_shapes():
+    # transA = 1 with A stored [K, 3]: A' has k stride 3; C per row.
+    K, N = 2000, 776
+    A = rand_tensor((K, 3), torch.bfloat16, 887, DEV)
+    B = rand_tensor((K, N), torch.bfloat16, 888, DEV)
+    for cshape in [None, (3, 1), (3, N)]:
+        C = None if cshape is None else rand_tensor(cshape, torch.bfloat16, 889, DEV)
+        _vec_gemm_check(A, B, C, 1.25, -0.5, 1, 0)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=str)
+def test_vector_matmul_mn_major_batched(dtype):
+    # a [K] @ B [5, K, N]; A [2, 3, K] @ B [2, 1, K, N] (B broadcast over dim 1).
+    K, N = 1500, 600
+    for a, B in ((rand_tensor((K,), dtype, 890, DEV), rand_tensor((5, K, N), dtype, 891, DEV)),
+                 (rand_tensor((2, 3, K), dtype, 892, DEV), rand_tensor((2, 1, K, N), dtype, 893, DEV))):
+        with vector_path():
+            Y = qg.mm_matmul(a, B)
+        assert qg.mm_last_path() == qg.MM_PATH_VECTOR
+        an, bn = to_np(a), to_np(B)
+        assert max_rel_err(to_np(Y), oracle.matmul(an, bn), oracle.matmul_abs_scale(an, bn)) <= TOL[dtype]
+
+
+def test_vector_gemm_mn_major_exact_on_integer_inputs():
+    # Small integers in fp32: exact sums, so bit for bit equal to the oracle.
+    g = torch.Generator().manual_seed(894)
+    A = torch.randint(-3, 4, (3, 8192), generator=g).to(torch.float32).to(DEV)
+    B = torch.randint(-3, 4, (8192, 4100), generator=g).to(torch.float32).to(DEV)
+    with vector_path():
+        Y = qg.mm_gemm(A, B, None, 1.0, 1.0, 0, 0)
+    assert qg.mm_last_path() == qg.MM_PATH_VECTOR
+    assert np.array_equal(to_np(Y), oracle.gemm(to_np(A), to_np(B), None))
+
+
 def test_planner_paths_for_few_row_products():
-    # K-major B' with 1-4 rows: the few-row kernel; MN-major B' and 5 or more
-    # rows: the tensor cores.
+    # 1-4 rows: the few-row kernels for both layouts of B'; 5 or more rows:
+    # the tensor cores.
     A = rand_tensor((1, 4096), torch.bfloat16, 813, DEV)
     B = rand_tensor((4096, 4096), torch.bfloat16, 814, DEV)
     a, b = to_np(A), to_np(B)
-    for tB, path in ((1, qg.MM_PATH_VECTOR), (0, qg.MM_PATH_TENSOR)):
+    for tB, path in ((1, qg.MM_PATH_VECTOR), (0, qg.MM_PATH_VECTOR)):
         Y = qg.mm_gemm(A, B, None, 1.0, 1.0, 0, tB)
         assert qg.mm_last_path() == path
         err = max_rel_err(to_np(Y), oracle.gemm(a, b, None, transB=tB), oracle.gemm_abs_scale(a, b, None, transB=tB))
@@ -221,3 +270,11 @@ def test_planner_paths_for_few_row_products():
     A8 = rand_tensor((8, 4096), torch.bfloat16, 815, DEV)
     qg.mm_gemm(A8, B, None, 1.0, 1.0, 0, 1)
     assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    # 3 rows of bf16: the few-row kernel for K-major B', the tensor cores
+    # (as fast there) for MN-major B'; fp32 takes the few-row kernel for both.
+    A3 = rand_tensor((3, 4096), torch.bfloat16, 816, DEV)
+    for tB, path in ((1, qg.MM_PATH_VECTOR), (0, qg.MM_PATH_TENSOR)):
+        qg.mm_gemm(A3, B, None, 1.0, 1.0, 0, tB)
+        assert qg.mm_last_path() == path
+    qg.mm_gemm(A3.float(), B.float(), None, 1.0, 1.0, 0, 0)
+    assert qg.mm_last_path() == qg.MM_PATH_VECTOR
