@@ -7,6 +7,10 @@
 // outputs each, strided by 16 so shared-memory reads are conflict-free and
 // global stores are coalesced along the row); K is staged through shared
 // memory 16 at a time with plain strided loads.
+//
+// Products with 1 to 4 rows of A' (bf16, f16, f32) have their own kernels,
+// which read B' once at memory speed: vec_gemm_kernel for K-major B' and
+// vec_mn_kernel for MN-major B' (see "few-row products" below).
 #include <atomic>
 #include <cstring>
 
