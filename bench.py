@@ -600,7 +600,11 @@ def run_ours(args, rank, world, local):
 
     extras = {}
     if not args.skip_extras:
-        extras = bench_extra_workloads(dev, world, stream, peaks, peak_kind)
+        # The headline line is printed even if one of the other workloads fails.
+        try:
+            extras = bench_extra_workloads(dev, world, stream, peaks, peak_kind)
+        except Exception as exc:  # noqa: BLE001 - reported in the JSON line
+            extras = {"error": "%s: %s" % (type(exc).__name__, exc)}
 
     traffic = stored_traffic("tc_gemm_kernel_gemm_bf16_8192")
     line = {
