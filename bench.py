@@ -628,7 +628,8 @@ def run_ours(args, rank, world, local):
         "device_status": status,
         "workloads": extras,
         "workloads_protocol": "each workload from %.0f s idle: 3-5 warm-up calls, then 10-20 calls back to back timed "
-                              "with CUDA events (matmul_f32: 50 calls, each after an L2 flush)" % EXTRA_IDLE_S,
+                              "with CUDA events (matmul_f32: 50 calls, each after an L2 flush; gemm_bf16_skinny_*: "
+                              "a CUDA graph of 10 calls over two copies of B, replayed 10 times)" % EXTRA_IDLE_S,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
