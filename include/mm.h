@@ -138,8 +138,13 @@ mm_status mm_matmul(const mm_tensor* A, const mm_tensor* B, const mm_tensor* Y, 
  * unidirectionally broadcastable to (M,N): rank <= 2, right-aligned, each
  * dimension equal to the target or 1.  ONNX defaults are alpha = beta = 1,
  * transA = transB = 0.  Float T: y = alpha*acc + beta*c evaluated in fp32
- * (fp64 for f64), rounded once to T.  Integer T: alpha and beta must be
- * integral (else MM_ERR_UNSUPPORTED) and Y is exact modulo 2^n. */
+ * (fp64 for f64), rounded once to T.  Integer T (the page does not say how
+ * a real-valued result becomes a T): with integral alpha and beta, Y is exact
+ * modulo 2^n; otherwise acc = A'B' wraps modulo 2^n to a T value, then
+ * r = alpha*acc + beta*C is evaluated in fp64 (each product rounded, then the
+ * sum) and truncated toward zero; results outside T's range are undefined
+ * (this library saturates them).  Non-finite alpha or beta with an integer T
+ * returns MM_ERR_UNSUPPORTED. */
 mm_status mm_gemm_output_shape(const mm_tensor* A, const mm_tensor* B, int64_t transA, int64_t transB,
                                int32_t* out_ndim, int64_t* out_shape /* [MM_MAX_DIMS] */);
 mm_status mm_gemm(const mm_tensor* A, const mm_tensor* B, const mm_tensor* C /* NULL = absent */,
@@ -243,9 +248,15 @@ mm_status mm_grouped_matmul_qweights(const mm_tensor* input, const mm_tensor* we
  *   (mm_grouped_matmul_workspace_size() under the tensor-core policy: the
  *   routing tables plus M*S rows of K elements) fits the array; larger
  *   problems return MM_ERR_WORKSPACE.
+ *   Path: always the tensor-core routing and GEMM kernels, whatever
+ *   mm_set_path_policy says (the CUDA-core path needs no scratch at all).
  *   The first call on a device looks up the array's device address (a CUDA
  *   runtime query, no allocation); make that first call before any stream
- *   capture.  Every call on a device shares the one array and each call resets
+ *   capture.  The address is then cached for the device's ordinal for the rest
+ *   of the process, so it does not survive cudaDeviceReset (nor does the
+ *   device-status word's, which every entry point caches the same way): do not
+ *   call the library on a device after resetting it.  Every call on a device
+ *   shares the one array and each call resets
  *   what it needs, so calls whose GPU work overlaps (different streams, or
  *   other host threads) race on it and must be ordered by the caller. */
 size_t mm_grouped_matmul_noalloc_max_scratch(void);

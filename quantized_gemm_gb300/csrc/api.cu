@@ -166,9 +166,11 @@ bool tensor_pays(int64_t M, int64_t N, int64_t K, int64_t batch) {
   return (double)M * (double)N * (double)K * (double)batch >= 2097152.0;
 }
 // fp32 runs as three tf32 products on the tensor cores: it needs 8x more work
-// than the 16-bit types before it beats the CUDA-core kernel.
+// than the 16-bit types (2^24 multiply-adds instead of 2^21) before it beats
+// the CUDA-core kernel.
 bool tensor_pays_dense(int dtype, int64_t M, int64_t N, int64_t K, int64_t batch) {
-  return dtype == MM_F32 ? tensor_pays(M, N, K, 8 * batch) : tensor_pays(M, N, K, batch);
+  if (dtype == MM_F32) return (double)M * (double)N * (double)K * (double)batch >= 8.0 * 2097152.0;
+  return tensor_pays(M, N, K, batch);
 }
 
 mm_status finish(mm_status s, int path) {

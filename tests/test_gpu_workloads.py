@@ -28,9 +28,13 @@ def _rows(n, extra, seed):
 
 
 def test_matmul_f32_full():
+    """The small f32 workload runs on the CUDA cores (FFMA): the [4,128,64] @
+    [64,96] product on the tiled kernel (3.1 M multiply-adds, below the 2^24 at
+    which three tf32 products pay), the promoted 1-D one on the few-row kernel."""
     d = workloads.matmul_f32(device=DEV)
-    for a, b in ((d["A"], d["B"]), (d["A1"], d["B1"])):
+    for (a, b), path in (((d["A"], d["B"]), qg.MM_PATH_SIMT), ((d["A1"], d["B1"]), qg.MM_PATH_VECTOR)):
         y = qg.mm_matmul(a, b)
+        assert qg.mm_last_path() == path
         an, bn = to_np(a), to_np(b)
         assert max_rel_err(to_np(y), oracle.matmul(an, bn), oracle.matmul_abs_scale(an, bn)) <= 1e-5
 

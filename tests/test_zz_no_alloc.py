@@ -7,8 +7,8 @@ by taking its scratch from a fixed array the library keeps on each device.
 These tests call it directly through ctypes on preallocated tensors, twice in
 a row with different problems (the array keeps the previous call's contents,
 so stale routing state must not leak into the second result), and compare each
-result with the existing workspace-taking entry point, within the per-element
-bf16/f16 bound used by every float test.  A problem whose scratch exceeds the
+result with the existing workspace-taking entry point and with the oracle,
+within the per-element bf16/f16 bound used by every float test.  A problem whose scratch exceeds the
 array is rejected with MM_ERR_WORKSPACE.
 
 The file name makes pytest collect it last.
@@ -46,11 +46,18 @@ def _case(M, K, N, G, S, dtype, ind, with_bias, seed):
 def _check_against_existing(x, w, gi, bias):
     out = torch.empty((x.shape[0], gi.shape[1], w.shape[2]), dtype=x.dtype, device=DEV)
     assert _noalloc(x, w, gi, bias, out) == 0
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
     assert qg.mm_get_device_status() == "MM_OK"
     ref = qg.mm_grouped_matmul(x, w, gi, bias)        # the existing entry point (caller workspace)
     torch.cuda.synchronize()
-    scale = oracle.grouped_abs_scale(to_np(x), to_np(w), gi.cpu().numpy(), None if bias is None else to_np(bias))
+    hx, hw, hg = to_np(x), to_np(w), gi.cpu().numpy()
+    hb = None if bias is None else to_np(bias)
+    scale = oracle.grouped_abs_scale(hx, hw, hg, hb)
+    # Against the existing entry point, and against the oracle (which shares
+    # no code with either, so a fault in the kernels both entry points run
+    # cannot pass unseen).
     assert max_rel_err(to_np(out), to_np(ref), scale) <= TOL[x.dtype]
+    assert max_rel_err(to_np(out), oracle.grouped_matmul(hx, hw, hg, hb), scale) <= TOL[x.dtype]
 
 
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
