@@ -26,9 +26,18 @@ Each module cites the page and section it follows:
 * ``dequantize_linear`` -- GroupedMatMul - 29, Summary: weight-only quantized
   experts (DequantizeLinear of the weights, then GroupedMatMul)
 
-Parity status: every function here is pinned by tests in
+A second, independent oracle restates the same pages as plain C++ loops
+(``csrc/oracle.cpp``: double accumulation in k order without fused
+multiply-adds, exact integers, the same float32 requantisation), bound by
+``oracle.native`` with the same function names; it is what the benchmark's CPU
+baseline times and what the full-size GPU parity tests use.  The two share no
+code.
+
+Parity status: every function of both oracles is pinned by tests in
 ``tests/test_oracle_pins.py`` (printed worked examples, brute force on tiny
-inputs, closed forms and identities); none is "parity unpinned".
+inputs, closed forms, identities and hand-computed error-bound denominators),
+and ``tests/test_oracle_native.py`` checks that the two agree on random
+inputs; none is "parity unpinned".
 """
 
 from .matmul import matmul, matmul_output_shape, matmul_abs_scale

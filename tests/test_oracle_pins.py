@@ -11,6 +11,11 @@
 * Identities: (A B)^T = B^T A^T through transA/transB; GroupedMatMul with one
   group and one selection equals Gemm with a (1, N) bias; identity and
   permutation weights.
+* The error-bound denominators (the *_abs_scale functions) by hand values
+  with negative entries, a negative alpha and a broadcast C.
+
+Every pin runs against both oracles: the numpy one (``oracle``) and the plain
+C++ loops (``oracle.native``), which share no code with each other.
 """
 
 import itertools
@@ -22,8 +27,20 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle.native
 
 GOLDEN = pathlib.Path(__file__).parent / "golden"
+
+# The oracle under test; the fixture below runs every pin once per oracle.
+ORC = oracle
+
+
+@pytest.fixture(autouse=True, params=["numpy", "cpp"])
+def _which_oracle(request):
+    global ORC
+    ORC = oracle if request.param == "numpy" else oracle.native
+    yield
+    ORC = oracle
 
 
 def _load(name):
@@ -48,9 +65,9 @@ PRINT_TOL = 1e-6
 def test_matmul_page_examples(ex):
     A, B = _arr(ex["inputs"]["A"]), _arr(ex["inputs"]["B"])
     want = _arr(ex["outputs"]["Y"]).astype(np.float64)
-    got = oracle.matmul(A, B)
+    got = ORC.matmul(A, B)
     assert got.shape == want.shape
-    scale = oracle.matmul_abs_scale(A, B)
+    scale = ORC.matmul_abs_scale(A, B)
     assert np.all(np.abs(got - want) <= PRINT_TOL * (scale + np.abs(want)))
 
 
@@ -62,9 +79,9 @@ def test_gemm_page_examples(ex):
     A, B = _arr(ex["inputs"]["A"]), _arr(ex["inputs"]["B"])
     C = _arr(ex["inputs"]["C"]) if "C" in ex["inputs"] else None
     want = _arr(ex["outputs"]["Y"]).astype(np.float64)
-    got = oracle.gemm(A, B, C, **kw)
+    got = ORC.gemm(A, B, C, **kw)
     assert got.shape == want.shape
-    scale = oracle.gemm_abs_scale(A, B, C, **kw)
+    scale = ORC.gemm_abs_scale(A, B, C, **kw)
     assert np.all(np.abs(got - want) <= PRINT_TOL * (scale + np.abs(want)))
 
 
@@ -74,7 +91,7 @@ def test_qlinear_page_examples_bit_exact(ex):
     args = [_arr(i[k]) for k in ("a", "a_scale", "a_zero_point", "b", "b_scale",
                                  "b_zero_point", "y_scale", "y_zero_point")]
     want = _arr(ex["outputs"]["y"])
-    got = oracle.qlinear_matmul(*args)
+    got = ORC.qlinear_matmul(*args)
     assert got.dtype == want.dtype and got.shape == want.shape
     assert np.array_equal(got, want)
 
@@ -82,7 +99,7 @@ def test_qlinear_page_examples_bit_exact(ex):
 # ---------------------------------------------------------------- QLinear closed forms
 
 def _ql(a, b, sa=1.0, za=0, sb=1.0, zb=0, ys=1.0, yz=0, t_in=np.int8, t_out=np.int8):
-    return oracle.qlinear_matmul(np.asarray(a, t_in), np.float32(sa), t_in(za),
+    return ORC.qlinear_matmul(np.asarray(a, t_in), np.float32(sa), t_in(za),
                                  np.asarray(b, t_in), np.float32(sb), t_in(zb),
                                  np.float32(ys), t_out(yz))
 
@@ -110,7 +127,7 @@ def test_qlinear_per_row_and_per_column_parameters():
     a = np.array([[1, 2], [3, 4]], np.int8)
     b = np.array([[1, 0], [0, 1]], np.int8)
     for shape_a, shape_b in (((2,), (2,)), ((2, 1), (1, 2))):
-        y = oracle.qlinear_matmul(
+        y = ORC.qlinear_matmul(
             a, np.array([1.0, 2.0], np.float32).reshape(shape_a), np.array([0, 1], np.int8).reshape(shape_a),
             b, np.array([1.0, 0.5], np.float32).reshape(shape_b), np.array([0, 0], np.int8).reshape(shape_b),
             np.float32(1.0), np.int8(0))
@@ -124,7 +141,7 @@ def test_qlinear_accumulator_wraps_in_32_bits():
     K = 33026
     a = np.full((1, K), 255, np.uint8)
     b = np.full((K, 1), 255, np.uint8)
-    y = oracle.qlinear_matmul(a, np.float32(1), np.uint8(0), b, np.float32(1), np.uint8(0),
+    y = ORC.qlinear_matmul(a, np.float32(1), np.uint8(0), b, np.float32(1), np.uint8(0),
                               np.float32(2.0 ** 24), np.int8(0))
     assert y.item() == -128
 
@@ -134,7 +151,7 @@ def test_requantize_is_float32_sequence():
     s = np.float32(0.0066) * np.float32(0.00705)
     v = np.float32(1000) * s
     q = v / np.float32(0.0107)
-    assert oracle.requantize(np.int32(1000), np.float32(0.0066), np.float32(0.00705),
+    assert ORC.requantize(np.int32(1000), np.float32(0.0066), np.float32(0.00705),
                              np.float32(0.0107), np.int8(0), np.int8) == np.int8(round(float(q)))
 
 
@@ -147,17 +164,17 @@ def test_integer_matmul_wraps_modulo_2n(dt, bits):
     h = 1 << (bits - 2)
     A = np.array([[h, h]], dtype=np.uint64).astype(dt)
     B = np.array([[2], [2]], dtype=dt)
-    assert oracle.matmul(A, B).item() == 0
+    assert ORC.matmul(A, B).item() == 0
     A2 = np.array([[1 << (bits - 1)]], dtype=np.uint64).astype(dt)
     B2 = np.array([[3]], dtype=dt)
     want = np.array([1 << (bits - 1)], dtype=np.uint64).astype(dt).item()
-    assert oracle.matmul(A2, B2).item() == want
+    assert ORC.matmul(A2, B2).item() == want
 
 
 def test_signed_integer_matmul_negative_values():
     A = np.array([[-3, 4]], np.int32)
     B = np.array([[5], [-6]], np.int32)
-    assert oracle.matmul(A, B).item() == -39
+    assert ORC.matmul(A, B).item() == -39
 
 
 # ---------------------------------------------------------------- brute force
@@ -216,7 +233,7 @@ def test_matmul_brute_force_float(sa, sb):
     rng = np.random.default_rng(7)
     A = rng.integers(-9, 10, size=sa).astype(np.float32) / 4
     B = rng.integers(-9, 10, size=sb).astype(np.float32) / 8
-    got = oracle.matmul(A, B)
+    got = ORC.matmul(A, B)
     want = _bf_matmul(A.astype(np.float64), B.astype(np.float64)).astype(np.float64)
     assert got.shape == want.shape
     assert np.array_equal(got, want)  # small dyadic values: every sum is exact
@@ -229,7 +246,7 @@ def test_matmul_brute_force_integer(dt):
     for sa, sb in MATMUL_SHAPES[:6]:
         A = rng.integers(info.min, info.max, size=sa, dtype=dt, endpoint=True)
         B = rng.integers(info.min, info.max, size=sb, dtype=dt, endpoint=True)
-        got = oracle.matmul(A, B)
+        got = ORC.matmul(A, B)
         bf = _bf_matmul(A.astype(object), B.astype(object))
         mod = 1 << (8 * np.dtype(dt).itemsize)
         want = [int(v) % mod for v in np.asarray(bf, dtype=object).reshape(-1)]
@@ -280,7 +297,7 @@ def test_qlinear_brute_force(t_in, t_out):
     sb = rng.uniform(0.003, 0.01, size=(N,)).astype(np.float32)
     ys = np.float32(0.05)
     yz = t_out(rng.integers(np.iinfo(t_out).min, np.iinfo(t_out).max))
-    got = oracle.qlinear_matmul(a, sa, za, b, sb, zb, ys, yz)
+    got = ORC.qlinear_matmul(a, sa, za, b, sb, zb, ys, yz)
     want = _bf_qlinear_2d(a.astype(int).tolist(), za.astype(int).tolist(), sa.tolist(),
                           b.astype(int).tolist(), zb.astype(int).tolist(), sb.tolist(),
                           ys, int(yz), lo, hi)
@@ -296,7 +313,7 @@ def test_qlinear_batched_per_row_column_brute_force():
     zb = rng.integers(-20, 20, size=(2, 1, 5), endpoint=True).astype(np.int8)
     sa = rng.uniform(0.003, 0.01, size=(2, 3, 1)).astype(np.float32)
     sb = rng.uniform(0.003, 0.01, size=(2, 1, 5)).astype(np.float32)
-    got = oracle.qlinear_matmul(a, sa, za, b, sb, zb, np.float32(0.02), np.int8(-9))
+    got = ORC.qlinear_matmul(a, sa, za, b, sb, zb, np.float32(0.02), np.int8(-9))
     for d in range(2):
         want = _bf_qlinear_2d(a[d].astype(int).tolist(), za[d, :, 0].astype(int).tolist(),
                               sa[d, :, 0].tolist(), b[d].astype(int).tolist(),
@@ -340,7 +357,7 @@ def test_gemm_brute_force(tA, tB, c_shape):
     A = rng.integers(-8, 9, size=(K, M) if tA else (M, K)).astype(np.float32) / 2
     B = rng.integers(-8, 9, size=(N, K) if tB else (K, N)).astype(np.float32) / 4
     C = None if c_shape is None else (rng.integers(-8, 9, size=c_shape).astype(np.float32) / 8)
-    got = oracle.gemm(A, B, C, alpha=0.5, beta=-2.0, transA=tA, transB=tB)
+    got = ORC.gemm(A, B, C, alpha=0.5, beta=-2.0, transA=tA, transB=tB)
     want = _bf_gemm(A.astype(np.float64), B.astype(np.float64), C, 0.5, -2.0, tA, tB)
     assert np.array_equal(got, want)
 
@@ -350,7 +367,7 @@ def test_gemm_integer_exact():
     B = np.array([[1], [1]], np.int32)
     C = np.array([[5]], np.int32)
     # A @ B = 2^31; 3 * 2^31 + (-1) * 5 = 2^31 - 5 (mod 2^32), which is the int32 2147483643.
-    got = oracle.gemm(A, B, C, alpha=3.0, beta=-1.0)
+    got = ORC.gemm(A, B, C, alpha=3.0, beta=-1.0)
     want = ((3 * 2 ** 31 - 5) + 2 ** 31) % 2 ** 32 - 2 ** 31
     assert got.item() == want
 
@@ -361,22 +378,22 @@ def test_gemm_integer_non_integral_alpha_beta():
     A = np.array([[2 ** 31 - 1, 1]], np.int32)
     B = np.array([[1], [1]], np.int32)
     C = np.array([[5]], np.int32)
-    assert oracle.gemm(A, B, C, alpha=0.5, beta=-1.0).item() == -(2 ** 30) - 5
+    assert ORC.gemm(A, B, C, alpha=0.5, beta=-1.0).item() == -(2 ** 30) - 5
     # truncation toward zero: acc = +-3, alpha 0.5 -> +-1.5; with beta 0.25 and C = +-7 -> +-3.25
     A2 = np.array([[1, 2], [-1, -2]], np.int32)
     B2 = np.array([[1], [1]], np.int32)
-    assert oracle.gemm(A2, B2, None, alpha=0.5).ravel().tolist() == [1, -1]
+    assert ORC.gemm(A2, B2, None, alpha=0.5).ravel().tolist() == [1, -1]
     C2 = np.array([[7], [-7]], np.int32)
-    assert oracle.gemm(A2, B2, C2, alpha=0.5, beta=0.25).ravel().tolist() == [3, -3]
+    assert ORC.gemm(A2, B2, C2, alpha=0.5, beta=0.25).ravel().tolist() == [3, -3]
     # unsigned: 5 * float32(0.3) = 1.50000006 -> 1
     U = np.array([[5]], np.uint32)
-    assert oracle.gemm(U, np.array([[1]], np.uint32), None, alpha=0.3).item() == 1
+    assert ORC.gemm(U, np.array([[1]], np.uint32), None, alpha=0.3).item() == 1
     # int64: the accumulator is rounded to float64 first: 2^54 + 3 -> 2^54 + 4, times 0.5
     L = np.array([[2 ** 54 + 3]], np.int64)
-    assert oracle.gemm(L, np.array([[1]], np.int64), None, alpha=0.5).item() == 2 ** 53 + 2
+    assert ORC.gemm(L, np.array([[1]], np.int64), None, alpha=0.5).item() == 2 ** 53 + 2
     # results outside T's range are undefined: rejected
     with pytest.raises(ValueError):
-        oracle.gemm(np.array([[2 ** 31 - 1]], np.int32), np.array([[1]], np.int32), None, alpha=1.5)
+        ORC.gemm(np.array([[2 ** 31 - 1]], np.int32), np.array([[1]], np.int32), None, alpha=1.5)
 
 
 def test_gemm_transpose_identity():
@@ -384,12 +401,12 @@ def test_gemm_transpose_identity():
     rng = np.random.default_rng(1)
     A = rng.standard_normal((6, 5))
     B = rng.standard_normal((5, 7))
-    Y = oracle.gemm(A, B)
-    Yt = oracle.gemm(B, A, transA=1, transB=1)
+    Y = ORC.gemm(A, B)
+    Yt = ORC.gemm(B, A, transA=1, transB=1)
     assert np.allclose(Y.T, Yt, rtol=0, atol=1e-12)
     Ai = rng.integers(-100, 100, size=(6, 5)).astype(np.int64)
     Bi = rng.integers(-100, 100, size=(5, 7)).astype(np.int64)
-    assert np.array_equal(oracle.gemm(Ai, Bi).T, oracle.gemm(Bi, Ai, transA=1, transB=1))
+    assert np.array_equal(ORC.gemm(Ai, Bi).T, ORC.gemm(Bi, Ai, transA=1, transB=1))
 
 
 def test_gemm_empty_k_and_column_broadcast():
@@ -398,19 +415,19 @@ def test_gemm_empty_k_and_column_broadcast():
     A = np.zeros((3, 0), np.float32)
     B = np.zeros((0, 4), np.float32)
     C = np.array([[1.0], [2.0], [3.0]], np.float32)
-    Y = oracle.gemm(A, B, C, beta=2.0)
+    Y = ORC.gemm(A, B, C, beta=2.0)
     assert np.array_equal(Y, np.repeat(np.array([[2.0], [4.0], [6.0]]), 4, axis=1))
     with pytest.raises(ValueError):
-        oracle.gemm(A, B, np.zeros((2, 4), np.float32))
+        ORC.gemm(A, B, np.zeros((2, 4), np.float32))
 
 
 def test_matmul_shape_errors():
     with pytest.raises(ValueError):
-        oracle.matmul(np.zeros((2, 3)), np.zeros((4, 2)))
+        ORC.matmul(np.zeros((2, 3)), np.zeros((4, 2)))
     with pytest.raises(ValueError):
-        oracle.matmul(np.zeros((2, 2, 3)), np.zeros((3, 3, 2)))
+        ORC.matmul(np.zeros((2, 2, 3)), np.zeros((3, 3, 2)))
     with pytest.raises(ValueError):
-        oracle.matmul(np.zeros(()), np.zeros((3,)))
+        ORC.matmul(np.zeros(()), np.zeros((3,)))
 
 
 # ---------------------------------------------------------------- GroupedMatMul
@@ -458,7 +475,7 @@ def _grouped_examples():
 def test_grouped_page_examples_hand_derived(name, dtype):
     x, w, gi, bias, want = _grouped_examples()[name]
     b = None if bias is None else bias.astype(dtype)
-    got = oracle.grouped_matmul(x.astype(dtype), w.astype(dtype), gi, b)
+    got = ORC.grouped_matmul(x.astype(dtype), w.astype(dtype), gi, b)
     want = np.array(want, np.float64)
     # Every term is a small integer; the only inexact values are the bias
     # entries, which are exact as the float of type `dtype` widened to float64.
@@ -469,11 +486,11 @@ def test_grouped_page_examples_hand_derived(name, dtype):
 def test_grouped_empty_shapes_and_invalid_index():
     x = np.arange(6, dtype=np.float32).reshape(2, 3)
     w = np.arange(24, dtype=np.float32).reshape(2, 3, 4)
-    assert oracle.grouped_matmul(x, w, np.empty((2, 0), np.int64)).shape == (2, 0, 4)
-    assert oracle.grouped_matmul(np.empty((0, 3), np.float32), w, np.empty((0, 2), np.int64)).shape == (0, 2, 4)
+    assert ORC.grouped_matmul(x, w, np.empty((2, 0), np.int64)).shape == (2, 0, 4)
+    assert ORC.grouped_matmul(np.empty((0, 3), np.float32), w, np.empty((0, 2), np.int64)).shape == (0, 2, 4)
     for bad in (-1, 2):
         with pytest.raises(IndexError):
-            oracle.grouped_matmul(x, w, np.array([[0], [bad]], np.int64))
+            ORC.grouped_matmul(x, w, np.array([[0], [bad]], np.int64))
 
 
 def test_grouped_one_group_equals_gemm_with_bias():
@@ -481,8 +498,8 @@ def test_grouped_one_group_equals_gemm_with_bias():
     x = rng.standard_normal((7, 5))
     w = rng.standard_normal((1, 5, 6))
     bias = rng.standard_normal((1, 6))
-    got = oracle.grouped_matmul(x, w, np.zeros((7, 1), np.int32), bias)[:, 0, :]
-    want = oracle.gemm(x, w[0], bias)
+    got = ORC.grouped_matmul(x, w, np.zeros((7, 1), np.int32), bias)[:, 0, :]
+    want = ORC.gemm(x, w[0], bias)
     assert np.allclose(got, want, rtol=0, atol=1e-12)
 
 
@@ -493,7 +510,7 @@ def test_grouped_identity_and_permutation_weights():
     perms = [np.eye(K)[list(p)] for p in ((0, 1, 2, 3), (3, 2, 1, 0), (1, 0, 3, 2))]
     w = np.stack(perms).astype(np.float32)   # weights[g] is a permutation matrix
     gi = rng.integers(0, G, size=(M, S)).astype(np.int64)
-    out = oracle.grouped_matmul(x, w, gi)
+    out = ORC.grouped_matmul(x, w, gi)
     for m in range(M):
         for i in range(S):
             assert np.array_equal(out[m, i], x[m] @ perms[gi[m, i]])
@@ -508,7 +525,7 @@ def test_grouped_brute_force():
     w = rng.integers(-4, 5, size=(G, K, N)).astype(np.float32)
     bias = rng.integers(-4, 5, size=(G, N)).astype(np.float32)
     gi = rng.integers(0, G, size=(M, S)).astype(np.int32)
-    got = oracle.grouped_matmul(x, w, gi, bias)
+    got = ORC.grouped_matmul(x, w, gi, bias)
     for m in range(M):
         for i in range(S):
             g = int(gi[m, i])
@@ -528,11 +545,11 @@ def test_dequantize_worked_values():
     q = np.array([[[-128, 127], [5, -5]]], dtype=np.int8)
     zp = np.array([[[3, -1]]], dtype=np.int8)
     scale = np.array([[[0.5, 1.5]]])
-    got = oracle.dequantize_linear(q, scale, zp, None, "bf16")
+    got = ORC.dequantize_linear(q, scale, zp, None, "bf16")
     assert got.tolist() == [[[-65.5, 192.0], [1.0, -6.0]]]
     # uint8 with the default zero point 0
     qu = np.array([[[0, 255]]], dtype=np.uint8)
-    assert oracle.dequantize_linear(qu, np.array([[[2.0, 0.25]]]), None, 1, "f16").tolist() == [[[0.0, 63.75]]]
+    assert ORC.dequantize_linear(qu, np.array([[[2.0, 0.25]]]), None, 1, "f16").tolist() == [[[0.0, 63.75]]]
 
 
 def test_dequantize_rounds_once_to_the_scale_type():
@@ -540,13 +557,13 @@ def test_dequantize_rounds_once_to_the_scale_type():
     q = np.array([[[127]]], dtype=np.int8)
     zp = np.array([[[-128]]], dtype=np.int8)
     s = np.array([[[1.5]]])
-    assert oracle.dequantize_linear(q, s, zp, None, "bf16").item() == 382.0
-    assert oracle.dequantize_linear(q, s, zp, None, "f16").item() == 382.5
+    assert ORC.dequantize_linear(q, s, zp, None, "bf16").item() == 382.0
+    assert ORC.dequantize_linear(q, s, zp, None, "f16").item() == 382.5
     # ties go to the even neighbour: 174 * 1.5 = 261 -> 260, 178 * 1.5 = 267 -> 268
     for diff, want in ((174, 260.0), (178, 268.0), (-174, -260.0)):
         qq = np.array([[[diff - 128 if diff > 0 else diff + 127]]], dtype=np.int8)
         zz = np.array([[[-128 if diff > 0 else 127]]], dtype=np.int8)
-        assert oracle.dequantize_linear(qq, s, zz, None, "bf16").item() == want
+        assert ORC.dequantize_linear(qq, s, zz, None, "bf16").item() == want
 
 
 def test_bf16_rounding_matches_torch_conversion():
@@ -558,7 +575,7 @@ def test_bf16_rounding_matches_torch_conversion():
     scales = torch.tensor(np.random.default_rng(40).uniform(-3, 3, 64), dtype=torch.float32).to(torch.bfloat16)
     scales = scales.double().numpy()
     prod = np.multiply.outer(diffs, scales)            # exact in float32 (<= 17 significant bits)
-    ours = oracle.round_to_bf16(prod)
+    ours = ORC.round_to_bf16(prod)
     ref = torch.from_numpy(prod.astype(np.float32)).to(torch.bfloat16).double().numpy()
     assert np.array_equal(ours, ref)
 
@@ -569,7 +586,7 @@ def test_dequantize_blocks_brute_force():
     q = rng.integers(-128, 128, size=(G, K, N)).astype(np.int8)
     zp = rng.integers(-20, 21, size=(G, 3, N)).astype(np.int8)
     scale = rng.integers(1, 9, size=(G, 3, N)) / 8.0   # exact, products exact in every type
-    got = oracle.dequantize_linear(q, scale, zp, block, "f32")
+    got = ORC.dequantize_linear(q, scale, zp, block, "f32")
     for g in range(G):
         for k in range(K):
             for n in range(N):
@@ -585,13 +602,13 @@ def test_grouped_qweights_reduces_to_grouped_matmul():
     q = rng.integers(-128, 128, size=(G, K, N)).astype(np.int8)
     gi = rng.integers(0, G, size=(M, S)).astype(np.int32)
     bias = rng.integers(-4, 5, size=(G, N)).astype(np.float32)
-    got = oracle.grouped_matmul_qweights(x, q, np.ones((G, 1, N)), None, K, gi, bias, "bf16")
-    assert np.array_equal(got, oracle.grouped_matmul(x, q.astype(np.float32), gi, bias))
+    got = ORC.grouped_matmul_qweights(x, q, np.ones((G, 1, N)), None, K, gi, bias, "bf16")
+    assert np.array_equal(got, ORC.grouped_matmul(x, q.astype(np.float32), gi, bias))
     # a per-column scale of 2**-3 scales every output of that column (bias excluded)
     s = np.ones((G, 1, N))
     s[:, :, 1] = 0.125
-    got2 = oracle.grouped_matmul_qweights(x, q, s, None, K, gi, None, "bf16")
-    ref2 = oracle.grouped_matmul(x, q.astype(np.float32), gi, None)
+    got2 = ORC.grouped_matmul_qweights(x, q, s, None, K, gi, None, "bf16")
+    ref2 = ORC.grouped_matmul(x, q.astype(np.float32), gi, None)
     assert np.array_equal(got2[:, :, 1], ref2[:, :, 1] * 0.125)
     assert np.array_equal(got2[:, :, 0], ref2[:, :, 0])
 
@@ -604,7 +621,7 @@ def test_grouped_qweights_uses_each_groups_parameters():
     zp = np.array([[[1, 1]], [[4, 4]]], dtype=np.int8)
     s = np.full((2, 1, 2), 0.5)
     gi = np.array([[0, 1]], dtype=np.int64)
-    out = oracle.grouped_matmul_qweights(x, q, s, zp, None, gi, None, "f16")
+    out = ORC.grouped_matmul_qweights(x, q, s, zp, None, gi, None, "f16")
     assert out[0, 0].tolist() == [-3.0, -3.0]          # (0 - 1) * 0.5 * 6
     assert out[0, 1].tolist() == [-12.0, -12.0]        # (0 - 4) * 0.5 * 6
 
@@ -612,8 +629,61 @@ def test_grouped_qweights_uses_each_groups_parameters():
 def test_dequantize_rejects_bad_shapes():
     q = np.zeros((1, 4, 2), dtype=np.int8)
     with pytest.raises(ValueError):
-        oracle.dequantize_linear(q, np.ones((1, 1, 2)), None, 2, "bf16")      # needs [1, 2, 2]
+        ORC.dequantize_linear(q, np.ones((1, 1, 2)), None, 2, "bf16")      # needs [1, 2, 2]
     with pytest.raises(TypeError):
-        oracle.dequantize_linear(q, np.ones((1, 1, 2)), np.zeros((1, 1, 2), dtype=np.uint8), None, "bf16")
+        ORC.dequantize_linear(q, np.ones((1, 1, 2)), np.zeros((1, 1, 2), dtype=np.uint8), None, "bf16")
     with pytest.raises(TypeError):
-        oracle.dequantize_linear(q.astype(np.int16), np.ones((1, 1, 2)), None, None, "bf16")
+        ORC.dequantize_linear(q.astype(np.int16), np.ones((1, 1, 2)), None, None, "bf16")
+
+
+# ------------------------------------------------------------------ error-bound denominators
+# Hand values chosen so that each plausible slip changes the result: a
+# negative alpha (|alpha| dropped -> negative values), a row whose terms
+# cancel (|A @ B| instead of |A| @ |B| -> 0 there), and a broadcast C with
+# negative entries (the |beta * C| term dropped or taken without abs).
+
+def test_gemm_abs_scale_hand_values():
+    A = np.array([[1.0, -2.0], [3.0, -4.0]])
+    B = np.array([[-1.0, 2.0], [-0.5, -3.0]])
+    # |A| @ |B| = [[2, 8], [5, 18]] while A @ B = [[0, 8], [-1, 18]].
+    # |alpha| = 0.5, |beta| = 2, C = [[1, -1]] stretched over the rows:
+    want = np.array([[3.0, 6.0], [4.5, 11.0]])
+    C = np.array([[1.0, -1.0]])
+    got = ORC.gemm_abs_scale(A, B, C, alpha=-0.5, beta=-2.0)
+    assert np.array_equal(got, want)
+    # the same through the transposition attributes
+    assert np.array_equal(ORC.gemm_abs_scale(A.T.copy(), B.T.copy(), C, alpha=-0.5, beta=-2.0, transA=1, transB=1),
+                          want)
+    # C of shape (M, 1) stretched along the columns: + 2 * [[1], [3]]
+    got = ORC.gemm_abs_scale(A, B, np.array([[1.0], [-3.0]]), alpha=-0.5, beta=-2.0)
+    assert np.array_equal(got, np.array([[3.0, 6.0], [8.5, 15.0]]))
+    # C absent: the product term alone
+    assert np.array_equal(ORC.gemm_abs_scale(A, B, None, alpha=-0.5), np.array([[1.0, 4.0], [2.5, 9.0]]))
+    # and the value itself has the cancellation: Y[0, 0] = -0.5 * 0 - 2 * 1
+    assert ORC.gemm(A, B, C, alpha=-0.5, beta=-2.0)[0, 0] == -2.0
+
+
+def test_matmul_abs_scale_hand_values():
+    # A [2, 1, 2] against B [2, 1] (1-D promotion of neither; batch of A only):
+    # batch 0: |1|*|-1| + |-2|*|-0.5| = 2 (the product is -1 + 1 = 0);
+    # batch 1: |-3|*|-1| + |4|*|-0.5| = 5 (the product is 3 - 2 = 1).
+    A = np.array([[[1.0, -2.0]], [[-3.0, 4.0]]])
+    B = np.array([[-1.0], [-0.5]])
+    assert np.array_equal(ORC.matmul_abs_scale(A, B), np.array([[[2.0]], [[5.0]]]))
+    assert np.array_equal(ORC.matmul(A, B), np.array([[[0.0]], [[1.0]]]))
+    # 1-D operands: |[1, -2]| . |[-1, -0.5]| = 2 with the promoted dims removed
+    assert ORC.matmul_abs_scale(np.array([1.0, -2.0]), np.array([-1.0, -0.5])).shape == ()
+    assert float(ORC.matmul_abs_scale(np.array([1.0, -2.0]), np.array([-1.0, -0.5]))) == 2.0
+
+
+def test_grouped_abs_scale_hand_values():
+    # x = [1, -1]; W0 = [[2], [3]], W1 = [[-1], [1]]; bias = [-0.5, 0.25].
+    # (m=0, i=0) picks group 0: |1*2| + |-1*3| + |-0.5| = 5.5 (the value is -1.5);
+    # (m=0, i=1) picks group 1: |1*-1| + |-1*1| + |0.25| = 2.25 (the value is -1.75).
+    x = np.array([[1.0, -1.0]])
+    w = np.array([[[2.0], [3.0]], [[-1.0], [1.0]]])
+    gi = np.array([[0, 1]], np.int64)
+    bias = np.array([[-0.5], [0.25]])
+    assert np.array_equal(ORC.grouped_abs_scale(x, w, gi, bias), np.array([[[5.5], [2.25]]]))
+    assert np.array_equal(ORC.grouped_matmul(x, w, gi, bias), np.array([[[-1.5], [-1.75]]]))
+    assert np.array_equal(ORC.grouped_abs_scale(x, w, gi), np.array([[[5.0], [2.0]]]))
