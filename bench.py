@@ -3,12 +3,16 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line.  The headline workload is the bf16 Gemm M=N=K=8192,
-transB=1, alpha=0.5, beta=2.0, C[1,8192] (one step = one mm_gemm call = one
-tcgen05 kernel launch); the metric is achieved TFLOP/s (2*M*N*K per step) and
-its fraction of the measured dense bf16 peak.  The other four workloads
-(f32 MatMul, batched broadcast bf16 MatMul, int8 QLinearMatMul, bf16
-GroupedMatMul) are timed the same way and reported under "workloads".
+Prints ONE JSON line on stdout.  The headline workload is the bf16 Gemm
+M=N=K=8192, transB=1, alpha=0.5, beta=2.0, C[1,8192] (one step = one mm_gemm
+call = one tcgen05 kernel launch); the metric is achieved TFLOP/s (2*M*N*K per
+step) and its fraction of the measured dense bf16 peak.  The line's
+"per_config" object holds the same metric for each of the five workloads (f32
+MatMul, the Gemm, batched broadcast bf16 MatMul, int8 QLinearMatMul, bf16
+GroupedMatMul) and for their type variants, each with its roofline fraction and,
+for the five, the C++ oracle's throughput on a stated sample of the same
+workload timed on this host's cores.  The full per-workload detail goes to
+stderr as one JSON line.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize(), timed with CUDA events on the stream the library
@@ -258,9 +262,40 @@ def gemm_case(dev, M=8192, N=8192, K=8192):
     return d, Y, step
 
 
-def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
-    """The four other workloads and their type variants: one call of the public API per step."""
+def stream_peaks(dev, world, stream):
+    """Write-only and copy bandwidth of the library's streaming kernels over
+    2 GiB (best of 10 calls, CUDA events): the HBM roofline of a product whose
+    traffic is nearly all output (the batched MatMul writes 2.15 GB and reads
+    0.15 GB)."""
     import quantized_gemm_gb300 as qg
+    nbytes = 2 << 30
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    src.fill_(1)
+    out = {}
+    for name, mode, traffic in (("write", 0, nbytes), ("write_bulk", 2, nbytes), ("copy", 1, 2 * nbytes)):
+        best = None
+        for _ in range(3):
+            qg.mm_stream_probe(dst, src if mode == 1 else None, mode)
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            qg.mm_stream_probe(dst, src if mode == 1 else None, mode)
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name + "_gbs"] = traffic / best / 1e6
+    del dst, src
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=True):
+    """The four other workloads and their type variants: one call of the public API per step.
+    With cpu, the C++ oracle is also timed on a sample of each of the four."""
+    import quantized_gemm_gb300 as qg
+    import oracle.native as orc
     out = {}
     bf16_peak = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
@@ -275,6 +310,11 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
         qg.mm_matmul(d["A1"], d["B1"], out=Y2)
     flush = l2_flusher(dev)
     ms, _ = time_loop(s1, 50, 5, world, stream, flush=flush, idle_s=EXTRA_IDLE_S)
+    paths = []
+    for a, b, y in ((d["A"], d["B"], Y1), (d["A1"], d["B1"], Y2)):
+        qg.mm_matmul(a, b, out=y)
+        paths.append({qg.MM_PATH_SIMT: "simt", qg.MM_PATH_VECTOR: "vector", qg.MM_PATH_TENSOR: "tensor"}.get(
+            qg.mm_last_path(), "?"))
     # The same two calls captured once in a CUDA graph and replayed: the
     # GPU-side latency without the per-call host work of the binding.
     graph = torch.cuda.CUDAGraph()
@@ -286,8 +326,12 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     flops = 2 * 4 * 128 * 64 * 96 + 2 * 4 * 64 * 96
     nbytes = 4 * (4 * 128 * 64 + 64 * 96 + 4 * 128 * 96 + 64 + 4 * 64 * 96 + 4 * 96)
     out["matmul_f32"] = {"value": flops / ms / 1e9, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
-                         "us_per_graph_replay": ms_graph * 1e3, "bound": "latency",
+                         "us_per_graph_replay": ms_graph * 1e3, "bound": "latency", "paths": "+".join(paths),
                          "hbm_gbs": nbytes / ms / 1e6, "kernels_per_call": 2, "l2": "flushed between iterations"}
+    if cpu:
+        h = {k: d[k].cpu().numpy() for k in ("A", "B", "A1", "B1")}
+        rate, _ = oracle_rate(lambda: (orc.matmul(h["A"], h["B"]), orc.matmul(h["A1"], h["B1"])), flops)
+        out["matmul_f32"]["cpu_baseline"] = cpu_entry(rate, "whole")
     del d, Y1, Y2, graph
 
     # 2a. Skinny products of the headline Gemm's B (stored [N, K], transB = 1):
@@ -346,29 +390,60 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     del d, Yf
     torch.cuda.empty_cache()
 
-    # 3. bf16 batched MatMul A[8,32,2048,128] @ B[1,32,128,2048]: HBM-bound (2.15 GB output).
+    # 2c. The CUDA-core kernel on the types without a tensor-core path:
+    # f64 and int32 Gemm, 4096^3 (FFMA/DFMA/IMAD throughput).
+    for name, dt in (("gemm_f64_simt", torch.float64), ("gemm_i32_simt", torch.int32)):
+        g = torch.Generator(device=dev).manual_seed(5)
+        if dt.is_floating_point:
+            A = torch.randn((4096, 4096), generator=g, device=dev, dtype=dt)
+            B = torch.randn((4096, 4096), generator=g, device=dev, dtype=dt)
+        else:
+            A = torch.randint(-100, 100, (4096, 4096), generator=g, device=dev, dtype=dt)
+            B = torch.randint(-100, 100, (4096, 4096), generator=g, device=dev, dtype=dt)
+        Yx = torch.empty((4096, 4096), dtype=dt, device=dev)
+        ms, _ = time_loop(lambda: qg.mm_gemm(A, B, None, 1.0, 0.0, 0, 0, out=Yx), 5, 2, world, stream,
+                          idle_s=EXTRA_IDLE_S)
+        assert qg.mm_last_path() == qg.MM_PATH_SIMT
+        out[name] = {"value": 2 * 4096 ** 3 / ms / 1e9, "unit": "TFLOP/s" if dt.is_floating_point else "TOP/s",
+                     "ms_per_call": ms, "bound": "alu", "kernel": "simt_gemm_kernel", "shape": "4096^3"}
+        del A, B, Yx
+    torch.cuda.empty_cache()
+
+    # 3. bf16 batched MatMul A[8,32,2048,128] @ B[1,32,128,2048]: HBM-bound
+    #    (2.15 GB output), compared with the copy bandwidth and with the
+    #    write-only stream measured here.
+    sp = stream_peaks(dev, world, stream)
     d = workloads.matmul_bf16_bcast(device=dev)
     Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
     ms, _ = time_loop(lambda: qg.mm_matmul(d["A"], d["B"], out=Y), 20, 3, world, stream, idle_s=EXTRA_IDLE_S)
     flops = 2 * 256 * 2048 * 2048 * 128
     nbytes = (d["A"].numel() + d["B"].numel() + Y.numel()) * 2
     gbs = nbytes / ms / 1e6
+    wpeak = max(sp["write_gbs"], sp["write_bulk_gbs"])
     out["matmul_bf16_bcast"] = {"value": flops / ms / 1e9, "unit": "TFLOP/s", "ms_per_call": ms,
                                 "bound": "hbm", "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
+                                "write_gbs": Y.numel() * 2 / ms / 1e6, "write_peak_gbs": wpeak,
+                                "frac_of_write_peak": Y.numel() * 2 / ms / 1e6 / wpeak, "stream_probe": sp,
                                 "kernels_per_call": 1, "l2": "inputs+output larger than L2"}
+    if cpu:
+        A = d["A"][0, :8].double().cpu().numpy()
+        B = d["B"][0, :8].double().cpu().numpy()
+        rate, _ = oracle_rate(lambda: orc.matmul(A, B), 2 * 8 * 2048 * 2048 * 128)
+        out["matmul_bf16_bcast"]["cpu_baseline"] = cpu_entry(rate, "8 of 256 batches")
+        del A, B
     del d, Y
     torch.cuda.empty_cache()
 
     # 4. int8 QLinearMatMul 16384 x 4096 x 4096 (runs on the f16 tensor pipe),
     #    then the same product with uint8 / mixed operands, float16 scales and
     #    batch-indexed quantisation parameters.
-    out["qlinear_s8"] = bench_qlinear(workloads.qlinear_s8(device=dev), world, stream, bf16_peak)
+    out["qlinear_s8"] = bench_qlinear(workloads.qlinear_s8(device=dev), world, stream, bf16_peak, cpu=cpu)
     for name, kw in sorted(workloads.QLINEAR_VARIANTS.items()):
         out[name] = bench_qlinear(workloads.qlinear(device=dev, **kw), world, stream, bf16_peak)
 
     # 5. GroupedMatMul M=16384, S=2, G=64, K=4096, N=14336: bf16 with int32
     #    indices, then float16 with int64 indices.
-    out["grouped_bf16"] = bench_grouped(workloads.grouped_bf16(device=dev), world, stream, bf16_peak)
+    out["grouped_bf16"] = bench_grouped(workloads.grouped_bf16(device=dev), world, stream, bf16_peak, cpu=cpu)
     out["grouped_f16_i64"] = bench_grouped(
         workloads.grouped_bf16(device=dev, dtype=torch.float16, index_dtype=torch.int64), world, stream, bf16_peak)
     # The same sizes with 8 groups (4096 rows each on average): CTA-pair tiles.
@@ -381,7 +456,7 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind):
     return out
 
 
-def bench_qlinear(d, world, stream, peak):
+def bench_qlinear(d, world, stream, peak, cpu=False):
     import quantized_gemm_gb300 as qg
     keys = ("a", "a_scale", "a_zero_point", "b", "b_scale", "b_zero_point", "y_scale", "y_zero_point")
     a, b = d["a"], d["b"]
@@ -400,12 +475,21 @@ def bench_qlinear(d, world, stream, peak):
            "kernels_per_call": 3, "saturated_fraction": sat, "l2": "inputs+workspace larger than L2",
            "types": "a %s, b %s, y %s, scales %s" % (a.dtype, b.dtype, y.dtype, d["a_scale"].dtype),
            "shape": "a %s, b %s" % (list(a.shape), list(b.shape))}
+    if cpu:
+        import oracle.native as orc
+        rows = 256
+        h = {k: d[k].cpu().numpy() for k in keys}
+        for k in ("a", "a_scale", "a_zero_point"):
+            h[k] = h[k][:rows]
+        rate, _ = oracle_rate(lambda: orc.qlinear_matmul(*[h[k] for k in keys]), 2 * rows * b.shape[-1] * a.shape[-1])
+        res["cpu_baseline"] = cpu_entry(rate, "%d of %d rows" % (rows, a.shape[0]))
+        res["cpu_baseline"]["unit"] = "TOP/s"
     del d, y, ws
     torch.cuda.empty_cache()
     return res
 
 
-def bench_grouped(d, world, stream, peak):
+def bench_grouped(d, world, stream, peak, cpu=False):
     import quantized_gemm_gb300 as qg
     x, w, gi = d["input"], d["weights"], d["group_indices"]
     M, K = x.shape
@@ -419,6 +503,16 @@ def bench_grouped(d, world, stream, peak):
     res = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor", "peak_tflops": peak,
            "frac": tf / peak, "kernels_per_call": 4, "l2": "weights (7.5 GB) larger than L2",
            "types": "%s, indices %s" % (x.dtype, gi.dtype)}
+    if cpu:
+        import oracle.native as orc
+        toks, cols = 512, 512
+        hx = x[:toks].double().cpu().numpy()
+        hw = w[:, :, :cols].double().cpu().numpy()
+        hb = d["bias"][:, :cols].double().cpu().numpy()
+        hg = gi[:toks].cpu().numpy()
+        rate, _ = oracle_rate(lambda: orc.grouped_matmul(hx, hw, hg, hb), 2 * toks * S * K * cols)
+        res["cpu_baseline"] = cpu_entry(rate, "%d tokens x %d cols" % (toks, cols))
+        del hx, hw
     del d, x, w, gi, yo, ws
     torch.cuda.empty_cache()
     return res
@@ -445,16 +539,14 @@ def bench_grouped_q(d, world, stream, peak):
 
 
 def cpu_baseline_gemm(d, rows):
-    """The oracle (numpy float64, BLAS threads) on the first `rows` rows of the Gemm workload."""
-    import oracle
+    """The C++ oracle on the first `rows` rows of the Gemm workload: (TFLOP/s, seconds)."""
+    import oracle.native as orc
     A = d["A"][:rows].double().cpu().numpy()
     B = d["B"].double().cpu().numpy()
     C = d["C"].double().cpu().numpy()
-    t0 = time.perf_counter()
-    oracle.gemm(A, B, C, alpha=d["alpha"], beta=d["beta"], transA=d["transA"], transB=d["transB"])
-    dt = time.perf_counter() - t0
     flops = 2.0 * rows * B.shape[0] * B.shape[1]
-    return flops / dt / 1e12, dt
+    return oracle_rate(lambda: orc.gemm(A, B, C, alpha=d["alpha"], beta=d["beta"], transA=d["transA"],
+                                        transB=d["transB"]), flops)
 
 
 def e2e_gemm(d, flops, world, steps, warmup=3):
@@ -503,54 +595,118 @@ def e2e_gemm(d, flops, world, steps, warmup=3):
     e1.record(s_out)
     e1.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
-    return {"value": flops / ms / 1e9 * world, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
-            "d2h_bytes_per_step": hys[0].numel() * hys[0].element_size(),
-            "pipelined": "3 streams, 2 buffer sets",
-            "bound": "host link: copy engines and SM copies both measured at 210 GB/s host->device, "
-                     "193 GB/s device->host, 257 GB/s in both directions at once on this box"}
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = hys[0].numel() * hys[0].element_size()
+    return {"value": _r(flops / ms / 1e9 * world), "unit": "TFLOP/s", "ms_per_step": _r(ms),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "host_link_gbs": _r((h2d + d2h) / ms / 1e6)}
 
 
-def blas_threads():
-    try:
-        return int(os.environ.get("OPENBLAS_NUM_THREADS", "0")) or (os.cpu_count() or 1)
-    except ValueError:
-        return os.cpu_count() or 1
+def oracle_rate(fn, ops, min_s=0.5):
+    """The C++ oracle's throughput on one sample: fn (one oracle call on it)
+    repeated until min_s of wall time has passed; returns (T ops/s, seconds)."""
+    fn()                                     # builds/loads the library, warms the caches
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_s:
+            return ops * n / dt / 1e12, dt
+
+
+def cpu_entry(rate, sample):
+    import oracle.native
+    return {"value": rate, "unit": "TFLOP/s", "cores": oracle.native.num_threads(), "kind": "oracle",
+            "sample": sample}
 
 
 # ------------------------------------------------------------------ arms
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is a bounded row sample of the Gemm."""
+    """The C++ oracle as the reference arm: each step is a bounded row sample of the Gemm."""
     if rank != 0:
         return
-    dev = "cpu"
-    d = workloads.gemm_bf16(device=dev)
+    import oracle.native as orc
+    d = workloads.gemm_bf16(device="cpu")
     A = d["A"].double().numpy()
     B = d["B"].double().numpy()
     C = d["C"].double().numpy()
-    import oracle
+
+    def gemm_rows(r0, rows):
+        orc.gemm(A[r0:r0 + rows], B, C, alpha=d["alpha"], beta=d["beta"], transB=1)
+    # Rows per step from a timed probe of 8 rows, so that the whole
+    # warm-up + timed run takes about 40 s of CPU time.
+    t0 = time.perf_counter()
+    gemm_rows(0, 8)
+    per_row = (time.perf_counter() - t0) / 8
     total_steps = args.steps + args.warmup
-    rows = int(max(8, min(512, 60.0 / max(1, total_steps) / 2e-3)))
+    rows = int(max(8, min(1024, 40.0 / max(1, total_steps) / max(per_row, 1e-6))))
     for i in range(args.warmup):
-        oracle.gemm(A[:rows], B, C, alpha=d["alpha"], beta=d["beta"], transB=1)
+        gemm_rows(0, rows)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        r0 = (i * rows) % (A.shape[0] - rows + 1)
-        oracle.gemm(A[r0:r0 + rows], B, C, alpha=d["alpha"], beta=d["beta"], transB=1)
+        gemm_rows((i * rows) % (A.shape[0] - rows + 1), rows)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
     tflops = 2.0 * rows * 8192 * 8192 / dt / 1e12
+    sample = "%d rows of the 8192^3 Gemm per step (C++ oracle: plain double loops)" % rows
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "gemm_bf16", "M": 8192, "N": 8192, "K": 8192, "transB": 1,
                    "alpha": 0.5, "beta": 2.0, "sample_rows_per_step": rows},
-        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": "%d rows of the 8192^3 Gemm per step (numpy float64)" % rows},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def _r(x, sig=4):
+    """x rounded to `sig` significant digits (None, integers and text unchanged)."""
+    if not isinstance(x, float) or x == 0 or not math.isfinite(x):
+        return x
+    return float("%.*g" % (sig, x))
+
+
+SHORT_KEYS = {"us_per_graph_replay": "us_graph", "achieved_gbs": "gbs", "frac_of_write_peak": "frac_write",
+              "write_peak_gbs": "write_peak_gbs"}
+
+
+def compact(entry, keys):
+    """The listed keys of a workload's detail, numbers rounded, some keys
+    shortened (SHORT_KEYS); a cpu_baseline keeps its value, core count and
+    sample (its unit is the entry's)."""
+    out = {}
+    for k in keys:
+        v = entry.get(k)
+        if v is None:
+            continue
+        if isinstance(v, dict):
+            v = {kk: _r(vv) for kk, vv in v.items() if kk in ("value", "cores", "sample")}
+        out[SHORT_KEYS.get(k, k)] = _r(v)
+    return out
+
+
+# Workload name in the detail -> key in per_config: the five configurations,
+# then the type variants (SURVEY rows f1-f4) at the same sizes.
+PER_CONFIG = (
+    ("1_matmul_f32", "matmul_f32", ("value", "unit", "us_per_call", "us_per_graph_replay", "bound", "paths",
+                                    "cpu_baseline")),
+    ("3_matmul_bf16_bcast", "matmul_bf16_bcast", ("value", "unit", "ms_per_call", "achieved_gbs", "frac",
+                                                 "peak_gbs", "frac_of_write_peak", "write_peak_gbs",
+                                                 "cpu_baseline")),
+    ("4_qlinear_s8", "qlinear_s8", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
+    ("5_grouped_bf16", "grouped_bf16", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
+    ("f1_qlinear_u8", "qlinear_u8", ("value", "unit", "ms_per_call", "frac")),
+    ("f1_qlinear_u8s8_f16scales", "qlinear_u8s8_f16scales", ("value", "unit", "ms_per_call", "frac")),
+    ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "unit", "ms_per_call", "frac")),
+    ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "unit", "ms_per_call", "frac")),
+    ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "unit", "ms_per_call", "frac")),
+    ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "unit", "ms_per_call", "frac")),
+    ("f4_gemm_f32", "gemm_f32", ("value", "unit", "ms_per_call", "frac", "peak_tflops")),
+)
 
 
 def run_ours(args, rank, world, local):
@@ -590,11 +746,11 @@ def run_ours(args, rank, world, local):
         e2e = e2e_gemm(d, flops, world, min(max(args.steps, 3), 40))
 
     cpu = None
-    if rank == 0 and world == 1 and not args.skip_cpu:
-        rows = 2048
-        cpu_tf, cpu_s = cpu_baseline_gemm(d, rows)
-        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": "first %d of 8192 rows of the Gemm (numpy float64 BLAS), %.1f s" % (rows, cpu_s)}
+    want_cpu = rank == 0 and world == 1 and not args.skip_cpu
+    if want_cpu:
+        rows = 256
+        cpu_tf, _ = cpu_baseline_gemm(d, rows)
+        cpu = cpu_entry(_r(cpu_tf), "%d of 8192 rows, C++ oracle (plain double loops)" % rows)
     del d, Y
     torch.cuda.empty_cache()
 
@@ -602,36 +758,44 @@ def run_ours(args, rank, world, local):
     if not args.skip_extras:
         # The headline line is printed even if one of the other workloads fails.
         try:
-            extras = bench_extra_workloads(dev, world, stream, peaks, peak_kind)
+            extras = bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=want_cpu)
         except Exception as exc:  # noqa: BLE001 - reported in the JSON line
             extras = {"error": "%s: %s" % (type(exc).__name__, exc)}
 
+    per_config = {"2_gemm_bf16": {"value": _r(tflops_rank), "unit": "TFLOP/s", "ms_per_call": _r(ms),
+                                  "frac": _r(tflops_rank / peak), "peak_tflops": peak,
+                                  "cpu_baseline": dict(compact({"c": cpu}, ("c",))["c"], sample="%d of 8192 rows" % 256)
+                                  if cpu else None}}
+    for key, name, keys in PER_CONFIG:
+        if name in extras:
+            per_config[key] = compact(extras[name], keys)
+    if "error" in extras:
+        per_config["error"] = extras["error"][:200]
+    per_config = dict(sorted(per_config.items()))
+
     traffic = stored_traffic("tc_gemm_kernel_gemm_bf16_8192")
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "per_config": per_config,
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded N(0,1)/sqrt(8192) A, B and N(0,1) C, rounded to bf16",
-        "config": {"workload": "gemm_bf16", "M": M, "N": N, "K": K, "transA": 0, "transB": 1, "alpha": 0.5,
-                   "beta": 2.0, "C": [1, N], "parallelism": "independent replicas x%d" % world,
-                   "l2": "inputs larger than L2 (A+B = 256 MiB > 129 MB)"},
-        "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops_rank / peak, "traffic": traffic,
-                     "peak_source": "%s %s (MEASURED_PEAKS.json)%s" % (
-                         peak_src, peak_kind, ": sw_power_cap active during the timed loop" if capped else ""),
-                     "frac_of_burst": tflops_rank / burst_peak, "burst_peak": burst_peak,
-                     "kernel": "tc_gemm_kernel<kDense>", "algorithmic": "2*M*N*K = %.4g FLOP per launch" % flops},
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic, seeded (workloads.py)",
+        "config": {"workload": "gemm_bf16", "M": M, "N": N, "K": K, "transB": 1, "alpha": 0.5,
+                   "beta": 2.0, "C": [1, N], "parallelism": "replicas x%d" % world, "l2": "A+B 256 MiB > L2"},
+        "roofline": {"bound": "tensor", "achieved": _r(tflops_rank), "peak": peak, "unit": "TFLOP/s",
+                     "frac": _r(tflops_rank / peak), "traffic": traffic, "peak_kind": "%s %s" % (peak_src, peak_kind),
+                     "frac_of_burst": _r(tflops_rank / burst_peak)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "device_status": status,
-        "workloads": extras,
-        "workloads_protocol": "each workload from %.0f s idle: 3-5 warm-up calls, then 10-20 calls back to back timed "
-                              "with CUDA events (matmul_f32: 50 calls, each after an L2 flush; gemm_bf16_skinny_*: "
-                              "a CUDA graph of 10 calls over two copies of B, replayed 10 times)" % EXTRA_IDLE_S,
     }
     if rank == 0:
+        # The detail of every workload, for the record, on stderr; stdout holds
+        # only the one JSON line.
+        sys.stderr.write("bench detail: " + json.dumps({"workloads": extras}) + "\n")
+        sys.stderr.flush()
         print(json.dumps(line), flush=True)
 
 
@@ -644,6 +808,17 @@ def run_profile_workload(args):
     name = args.profile_workload
     if name == "gemm_bf16":
         _, _, step = gemm_case(dev)
+    elif name == "matmul_f32":
+        d = workloads.matmul_f32(device=dev)
+        Y1 = torch.empty((4, 128, 96), dtype=torch.float32, device=dev)
+        Y2 = torch.empty((4, 96), dtype=torch.float32, device=dev)
+        step = lambda: (qg.mm_matmul(d["A"], d["B"], out=Y1), qg.mm_matmul(d["A1"], d["B1"], out=Y2))
+    elif name in ("gemm_f64_simt", "gemm_i32_simt"):
+        dt = torch.float64 if name == "gemm_f64_simt" else torch.int32
+        A = torch.ones((4096, 4096), dtype=dt, device=dev)
+        B = torch.ones((4096, 4096), dtype=dt, device=dev)
+        Yx = torch.empty((4096, 4096), dtype=dt, device=dev)
+        step = lambda: qg.mm_gemm(A, B, None, 1.0, 0.0, 0, 0, out=Yx)
     elif name == "gemm_f32":
         d = workloads.gemm_bf16(device=dev, dtype=torch.float32)
         Yf = torch.empty((8192, 8192), dtype=torch.float32, device=dev)
@@ -704,7 +879,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--profile-workload", default=None,
-                    help="run only this workload (gemm_bf16, gemm_bf16_skinny_mR[_tensor], matmul_bf16_bcast, qlinear_s8 or a "
+                    help="run only this workload (gemm_bf16, matmul_f32, gemm_f64_simt, gemm_i32_simt, "
+                         "gemm_bf16_skinny_mR[_tensor], matmul_bf16_bcast, qlinear_s8 or a "
                          "QLinear variant, "
                          "grouped_bf16[_gG][_nN])")
     args = ap.parse_args()

@@ -264,6 +264,17 @@ mm_status mm_grouped_matmul_noalloc(const mm_tensor* input, const mm_tensor* wei
                                     const mm_tensor* group_indices, const mm_tensor* bias /* NULL = absent */,
                                     const mm_tensor* output, void* stream);
 
+/* ---------------------------------------------------------------- memory-stream measurement
+ * Not an operator (the pages have no counterpart): the streaming kernels that
+ * measure the HBM roofline a memory-bound product is compared with.
+ *   mode 0: write `bytes` of a constant to dst (16-byte vector stores);
+ *   mode 1: copy `bytes` from src to dst (16-byte vector loads and stores);
+ *   mode 2: write `bytes` with bulk (TMA) stores from shared memory.
+ * dst (and src for mode 1) are device memory owned by the caller, 16-byte
+ * aligned; bytes is a multiple of 16 (otherwise MM_ERR_INVALID_ARG).  The
+ * call is asynchronous on `stream`; time it with events on that stream. */
+mm_status mm_stream_probe(void* dst, const void* src, size_t bytes, int32_t mode, void* stream);
+
 /* ---------------------------------------------------------------- device status
  * Synchronises `stream`, then returns and clears the device-side status of the
  * current device: MM_OK, MM_ERR_INDEX_RANGE or MM_ERR_TIMEOUT (the first set,

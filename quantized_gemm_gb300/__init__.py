@@ -20,7 +20,7 @@ __all__ = [
     "library_path",
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "mm_grouped_matmul_qweights", "mm_grouped_matmul_qweights_workspace_size",
-    "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE", "MM_PATH_VECTOR",
+    "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE", "MM_PATH_VECTOR", "mm_stream_probe",
 ]
 
 MM_MAX_DIMS = 8
@@ -83,6 +83,7 @@ def _lib():
             "mm_grouped_matmul_noalloc": ([T, T, T, T, T, P], I32),
             "mm_grouped_matmul_qweights_workspace_size": ([T, T, T, T, I64, T, ctypes.POINTER(SZ)], I32),
             "mm_grouped_matmul_qweights": ([T, T, T, T, I64, T, T, T, P, SZ, P], I32),
+            "mm_stream_probe": ([P, P, SZ, I32, P], I32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -173,6 +174,17 @@ def mm_last_path():
 def mm_set_wait_limit_ns(ns):
     """Limit of each tensor-core pipeline wait, in ns (0 = default 2 s)."""
     _check(_lib().mm_set_wait_limit_ns(int(ns)), "mm_set_wait_limit_ns")
+
+
+def mm_stream_probe(dst, src=None, mode=0, stream=None):
+    """Memory-stream measurement kernel on the bytes of ``dst``: mode 0 writes
+    them, 1 copies ``src`` into them (same size), 2 writes them with bulk (TMA)
+    stores."""
+    nbytes = dst.numel() * dst.element_size()
+    if src is not None and src.numel() * src.element_size() != nbytes:
+        raise ValueError("src and dst must have the same size in bytes")
+    _check(_lib().mm_stream_probe(dst.data_ptr(), None if src is None else src.data_ptr(), nbytes, int(mode),
+                                  _stream(dst, stream)), "mm_stream_probe")
 
 
 def mm_matmul(A, B, out=None, stream=None):

@@ -662,6 +662,17 @@ mm_status mm_grouped_matmul_noalloc(const mm_tensor* input, const mm_tensor* wei
   return finish(launch_tc_grouped(g, scratch, status, static_cast<cudaStream_t>(stream)), MM_PATH_TENSOR);
 }
 
+// ------------------------------------------------------------------ memory-stream measurement
+
+mm_status mm_stream_probe(void* dst, const void* src, size_t bytes, int32_t mode, void* stream) {
+  if (mode != kStreamWrite && mode != kStreamCopy && mode != kStreamWriteBulk) return MM_ERR_INVALID_ARG;
+  if (bytes == 0) return MM_OK;
+  if (!dst || (bytes & 15) || (reinterpret_cast<uintptr_t>(dst) & 15)) return MM_ERR_INVALID_ARG;
+  if (mode == kStreamCopy && (!src || (reinterpret_cast<uintptr_t>(src) & 15))) return MM_ERR_INVALID_ARG;
+  if (bytes > (size_t)INT64_MAX) return MM_ERR_INVALID_ARG;
+  return launch_stream_probe(dst, src, (int64_t)bytes, mode, static_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ device status
 
 mm_status mm_get_device_status(void* stream) {

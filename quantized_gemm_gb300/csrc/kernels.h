@@ -71,4 +71,9 @@ mm_status launch_vec_gemm(const GemmArgs& args, cudaStream_t stream);
 mm_status launch_simt_qlinear(const QLinearArgs& args, cudaStream_t stream);
 mm_status launch_simt_grouped(const GroupedArgs& args, unsigned* status, cudaStream_t stream);
 
+// Streaming measurement kernels (stream.cu): bytes is a multiple of 16 and the
+// buffers are 16-byte aligned (checked by the caller).
+enum { kStreamWrite = 0, kStreamCopy = 1, kStreamWriteBulk = 2 };
+mm_status launch_stream_probe(void* dst, const void* src, int64_t bytes, int mode, cudaStream_t stream);
+
 }  // namespace qg

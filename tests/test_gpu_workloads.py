@@ -1,11 +1,21 @@
 """Parity at the benchmark sizes, in the launch configuration bench.py times.
 
 Each workload runs once at full size through the public API (auto planner,
-which must choose the tensor-core kernels for the four large workloads); the
-oracle then recomputes sampled output rows from the same inputs (rows of a
-matmul depend only on the matching rows of A, so the oracle is given those
-rows): tile-boundary rows plus seeded random ones.  Float rows are held to the
-per-element bound, QLinearMatMul rows must be bit-exact.
+which must choose the tensor-core kernels for the four large workloads).  Two
+checks then cover its output:
+
+* every column of sampled rows: the numpy oracle recomputes tile-boundary and
+  seeded random rows (a row of a product depends only on the matching row of
+  A, so the oracle is given those rows);
+* every row of sampled columns: the C++ oracle recomputes the whole output on
+  a column subset (a column depends only on the matching column of B' and of
+  the per-column parameters) that holds the first and last columns and one
+  column of every 128-wide column block.  Every row tile of the persistent
+  raster, every (row tile, column tile) pair of the subset and, for
+  GroupedMatMul, every routed row of every group is checked.
+
+Float results are held to the per-element bound, QLinearMatMul results must
+be bit-exact.
 """
 
 import numpy as np
@@ -13,6 +23,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.native
 import quantized_gemm_gb300 as qg
 import workloads
 from helpers import max_rel_err, to_np
@@ -25,6 +36,18 @@ def _rows(n, extra, seed):
     fixed = [0, 1, 127, 128, 255, 256, n // 2, n - 129, n - 128, n - 1]
     rnd = np.random.default_rng(seed).choice(n, size=extra, replace=False)
     return sorted(set(int(r) for r in fixed + list(rnd) if 0 <= r < n))
+
+
+def _cols(n, seed, least=64):
+    """Column subset: both ends, the edges around column 128 and 256, one seeded
+    column in every 128-wide block, and seeded extras up to `least` columns."""
+    g = np.random.default_rng(seed)
+    cols = {0, 1, 127, 128, 255, 256, n - 2, n - 1}
+    cols |= {int(b + g.integers(0, min(128, n - b))) for b in range(0, n, 128)}
+    rest = np.setdiff1d(np.arange(n), np.fromiter(cols, dtype=np.int64))
+    if len(cols) < least and rest.size:
+        cols |= set(int(c) for c in g.choice(rest, size=min(least - len(cols), rest.size), replace=False))
+    return np.array(sorted(c for c in cols if 0 <= c < n), dtype=np.int64)
 
 
 def test_matmul_f32_full():
@@ -52,6 +75,14 @@ def test_gemm_bf16_8192_sampled_rows():
     ref = oracle.gemm(A, B, C, **kw)
     assert max_rel_err(to_np(Y[rows]), ref, oracle.gemm_abs_scale(A, B, C, **kw)) <= 1e-2
     assert torch.isfinite(Y.float()).all()
+    # every row, on a column subset (transB = 1: output column j is row j of B)
+    cols = _cols(8192, 21)
+    ct = torch.from_numpy(cols).to(DEV)
+    A = to_np(d["A"])
+    Bs = to_np(d["B"][ct])
+    Cs = to_np(d["C"][:, ct])
+    ref = oracle.native.gemm(A, Bs, Cs, **kw)
+    assert max_rel_err(to_np(Y[:, ct]), ref, oracle.native.gemm_abs_scale(A, Bs, Cs, **kw)) <= 1e-2
 
 
 def test_gemm_f32_8192_sampled_rows():
@@ -67,6 +98,13 @@ def test_gemm_f32_8192_sampled_rows():
     kw = dict(alpha=d["alpha"], beta=d["beta"], transA=0, transB=1)
     ref = oracle.gemm(A, B, C, **kw)
     assert max_rel_err(to_np(Y[rows]), ref, oracle.gemm_abs_scale(A, B, C, **kw)) <= 1e-5
+    cols = _cols(8192, 22)
+    ct = torch.from_numpy(cols).to(DEV)
+    A = to_np(d["A"])
+    Bs = to_np(d["B"][ct])
+    Cs = to_np(d["C"][:, ct])
+    ref = oracle.native.gemm(A, Bs, Cs, **kw)
+    assert max_rel_err(to_np(Y[:, ct]), ref, oracle.native.gemm_abs_scale(A, Bs, Cs, **kw)) <= 1e-5
 
 
 def test_matmul_bf16_bcast_sampled():
@@ -81,6 +119,13 @@ def test_matmul_bf16_bcast_sampled():
         B = to_np(d["B"][0, b1])
         ref = oracle.matmul(A, B)
         assert max_rel_err(to_np(Y[b0, b1][rows]), ref, oracle.matmul_abs_scale(A, B)) <= 1e-2
+    # every row of every batch index, on a column subset
+    cols = _cols(2048, 23)
+    ct = torch.from_numpy(cols).to(DEV)
+    A = to_np(d["A"])
+    Bs = to_np(d["B"][..., ct])
+    ref = oracle.native.matmul(A, Bs)
+    assert max_rel_err(to_np(Y[..., ct]), ref, oracle.native.matmul_abs_scale(A, Bs)) <= 1e-2
 
 
 def test_qlinear_s8_sampled_rows_bit_exact():
@@ -97,6 +142,20 @@ def test_qlinear_s8_sampled_rows_bit_exact():
     assert np.array_equal(got, ref), "%d mismatching outputs" % int((got != ref).sum())
     sat = float(((y == 127) | (y == -128)).float().mean())
     assert 0.001 < sat < 0.05      # the workload's y_scale saturates about 1% of outputs
+    _qlinear_all_rows(h, y.cpu().numpy(), 24)
+
+
+def _qlinear_all_rows(h, yh, seed):
+    """Every row against the C++ oracle on a column subset of b and its per-column parameters."""
+    cols = _cols(h["b"].shape[-1], seed)
+
+    def colsel(x):
+        x = np.asarray(x)
+        return x[..., cols] if x.ndim >= 1 and x.shape[-1] == h["b"].shape[-1] and x.size > 1 else x
+    ref = oracle.native.qlinear_matmul(h["a"], h["a_scale"], h["a_zero_point"], colsel(h["b"]), colsel(h["b_scale"]),
+                                       colsel(h["b_zero_point"]), h["y_scale"], h["y_zero_point"])
+    got = yh[..., cols]
+    assert np.array_equal(got, ref), "%d mismatching outputs" % int((got != ref).sum())
 
 
 @pytest.mark.parametrize("name", sorted(workloads.QLINEAR_VARIANTS))
@@ -118,6 +177,7 @@ def test_qlinear_variants_sampled_rows_bit_exact(name):
                                     h["y_zero_point"])
         got = sel(yh)[rows]
         assert np.array_equal(got, ref), "%d mismatching outputs" % int((got != ref).sum())
+    _qlinear_all_rows(h, yh, 25)
     info = np.iinfo(yh.dtype)
     sat = float(((yh == info.max) | (yh == info.min)).mean())
     assert 0.001 < sat < 0.05
@@ -158,6 +218,16 @@ def _grouped_check(d, seed):
     scale = oracle.grouped_abs_scale(x, w, gi_local, bias)
     got = to_np(out[toks][:, :, cols_t])
     assert max_rel_err(got, ref, scale) <= 1e-2
+    # every routed row of every group, on a column subset
+    cols = _cols(d["weights"].shape[2], seed + 2)
+    ct = torch.from_numpy(cols).to(DEV)
+    x = to_np(d["input"])
+    w = to_np(d["weights"][:, :, ct])
+    bias = to_np(d["bias"][:, ct])
+    gi = d["group_indices"].cpu().numpy()
+    ref = oracle.native.grouped_matmul(x, w, gi, bias)
+    scale = oracle.native.grouped_abs_scale(x, w, gi, bias)
+    assert max_rel_err(to_np(out[:, :, ct]), ref, scale) <= 1e-2
 
 
 @pytest.mark.parametrize("block", [0, 128])
@@ -185,4 +255,13 @@ def test_grouped_qweights_sampled_tokens_and_columns(block):
     scale = oracle.grouped_qweights_abs_scale(*args)
     got = to_np(out[toks][:, :, cols_t])
     assert max_rel_err(got, ref, scale) <= 1e-2
+    # every routed row of every group, on a column subset
+    cols = _cols(14336, 26)
+    ct = torch.from_numpy(cols).to(DEV)
+    args = (to_np(d["input"]), d["weights_q"][:, :, ct].cpu().numpy(), to_np(d["w_scale"][:, :, ct]),
+            d["w_zero_point"][:, :, ct].cpu().numpy(), block, d["group_indices"].cpu().numpy(),
+            to_np(d["bias"][:, ct]), "bf16")
+    ref = oracle.native.grouped_matmul_qweights(*args)
+    scale = oracle.native.grouped_qweights_abs_scale(*args)
+    assert max_rel_err(to_np(out[:, :, ct]), ref, scale) <= 1e-2
 
