@@ -165,10 +165,15 @@ class ClockSampler:
 
 
 def l2_flusher(device):
-    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    """Evicts L2 by reading a buffer twice its size.  The buffer is written
+    once here; the flush itself only reads, so it leaves no dirty lines whose
+    write-back the next timed kernel would pay."""
+    buf = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
+    torch.cuda.synchronize(device)
 
     def flush():
-        buf.fill_(1.0)
+        torch.sum(buf, out=sink)
     return flush
 
 
@@ -833,9 +838,12 @@ def run_profile_workload(args):
         As = (torch.randn((rows, 8192), device=dev) / math.sqrt(8192)).to(torch.bfloat16)
         Ys = torch.empty((rows, 8192), dtype=torch.bfloat16, device=dev)
         step = lambda: qg.mm_gemm(As, Bs, None, 1.0, 1.0, 0, 1, out=Ys)
-    elif name == "matmul_bf16_bcast":
-        d = workloads.matmul_bf16_bcast(device=dev)
-        Y = torch.empty((8, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
+    elif name.startswith("matmul_bf16_bcast"):
+        # a _bN suffix: N leading batches instead of 8 (a smaller case of the
+        # same product, for full ncu captures)
+        nb = int(name.split("_b")[-1]) if name.startswith("matmul_bf16_bcast_b") else 8
+        d = workloads.matmul_bf16_bcast(device=dev, batch=(nb, 32))
+        Y = torch.empty((nb, 32, 2048, 2048), dtype=torch.bfloat16, device=dev)
         step = lambda: qg.mm_matmul(d["A"], d["B"], out=Y)
     elif name == "qlinear_s8" or name in workloads.QLINEAR_VARIANTS:
         d = workloads.qlinear(device=dev, **workloads.QLINEAR_VARIANTS.get(name, {}))
@@ -880,7 +888,7 @@ def main():
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--profile-workload", default=None,
                     help="run only this workload (gemm_bf16, matmul_f32, gemm_f64_simt, gemm_i32_simt, "
-                         "gemm_bf16_skinny_mR[_tensor], matmul_bf16_bcast, qlinear_s8 or a "
+                         "gemm_bf16_skinny_mR[_tensor], matmul_bf16_bcast[_bN], qlinear_s8 or a "
                          "QLinear variant, "
                          "grouped_bf16[_gG][_nN])")
     args = ap.parse_args()

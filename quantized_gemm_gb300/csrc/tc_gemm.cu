@@ -109,9 +109,14 @@ constexpr int kSignalOff = 240;                  // 16 spare bytes of the contro
 
 __host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedQ; }
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
+// TMA-store epilogue for products of at most this many k-blocks (output-bound
+// ones): its box buffers cost a ring stage, which long-K products need more
+// (8192^3 Gemm: 0.610 -> 0.620 ms with it; batched K = 128 MatMul 0.494 -> 0.452 ms).
+constexpr int kYTmaMaxKb = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
 constexpr int kStageWords = 32 * 16;             // float per-warp output staging: 32 rows x 64 bytes
+constexpr int kYBoxBytes = 32 * 128;             // TMA-store box per warp: 32 rows x 64 16-bit columns
 
 // Shape of the CTA: 16 epilogue warps of 64 columns each, enough warps to hide
 // the epilogue's latency (short-K float products, the QLinear requantisation).
@@ -328,7 +333,7 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
       }
       pending |= 1u << stage;
       pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == G::kStages) { stage = 0; phase ^= 1; }
+      if (++stage == (uint32_t)p.stages) { stage = 0; phase ^= 1; }
     }
   }
 done:
@@ -412,7 +417,7 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
         }
         if (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
         else tc_commit(empty0 + 8 * stage);
-        if (++stage == G::kStages) { stage = 0; phase ^= 1; }
+        if (++stage == (uint32_t)p.stages) { stage = 0; phase ^= 1; }
       }
       if (PAIR) tc_commit_pair(accf0 + 8 * buf, 0x3);
       else tc_commit(accf0 + 8 * buf);
@@ -776,8 +781,8 @@ __device__ void run_split(const TcParams& p, uint8_t* smem, uint32_t sbase, uint
 // ------------------------------------------------------------------ epilogue
 
 template <int MODE, bool PAIR>
-__device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, uint32_t acce0, volatile int* abort,
-                             uint32_t* stage) {
+__device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t tmem, uint32_t accf0, uint32_t acce0,
+                             volatile int* abort, uint32_t* stage, uint32_t ybox) {
   // Warp-private shared memory: QLinear column data (kQColWords) or the
   // output staging rows (kStageWords).
   int32_t* qcol = reinterpret_cast<int32_t*>(stage);
@@ -955,6 +960,49 @@ __device__ void run_epilogue(const TcParams& p, uint32_t tmem, uint32_t accf0, u
         if (p.c && rok)
           crow = static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs;
       }
+      if constexpr (MODE == kDense || MODE == kSkinny) {
+        if (p.y_tma) {
+          // The warp's 32 rows x 64 columns: into registers, release the
+          // accumulator, then alpha/beta/C and the rounding to 16 bits into
+          // the warp's box buffer in the 128-byte swizzled layout of the
+          // output's tensor map (row r's 16-byte chunk c at c ^ (r % 8): the
+          // row-wise writes are conflict-free), and one tensor store of the
+          // box.  The store's clipping drops rows and columns past M and N.
+          uint32_t r[2][32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld32(taddr0 + c * 32, r[c]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          release(buf);
+          // The buffer is reused once the previous tile's store has read it.
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
+            if (crow) add_c32(p, crow, ncol + 32 * h, v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t chunk = (uint32_t)(4 * h + q);
+              sts128(ybox + (uint32_t)lane * 128 + ((chunk ^ (uint32_t)(lane & 7)) << 4),
+                     make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16), pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
+                                pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16),
+                                pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16)));
+            }
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0 && rbase < rows_t) {
+            tma_store_3d(tmY, ybox, (int32_t)ncol, (int32_t)(ti.m0 + roff + rbase),
+                         (int32_t)batch_off(p, p.y_bc, ti.batch));
+            bulk_commit();
+          }
+          continue;
+        }
+      }
       // The warp's columns, 64 at a time (two tcgen05.ld of 32); the
       // accumulator is released once its last columns are in registers.
 #pragma unroll 1
@@ -1050,8 +1098,9 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* ctrl = smem_raw + (sbase - raw) + G::kRingBytes;
-  const uint32_t cbase = sbase + G::kRingBytes;
+  // [ring][epilogue slices][control block][kGroupedQ staging ring]
+  uint8_t* ctrl = smem_raw + (sbase - raw) + G::kRingBytes + Cfg<MODE, PAIR>::kEpiBytes;
+  const uint32_t cbase = sbase + G::kRingBytes + Cfg<MODE, PAIR>::kEpiBytes;
   const uint32_t full0 = cbase, empty0 = cbase + 8 * S, accf0 = cbase + 16 * S;
   const uint32_t acce0 = accf0 + 16, drain = acce0 + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 16 * S + 40);
@@ -1110,9 +1159,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
       else mbar_wait_teardown(drain, 0, p.teardown_ns);   // the leader's last commit reaches this CTA too
     }
   } else if (warp < Cfg<MODE, PAIR>::kConvWarp0) {
-    uint32_t* stage = reinterpret_cast<uint32_t*>(ctrl + kCtrlBytes) +
+    uint32_t* stage = reinterpret_cast<uint32_t*>(smem_raw + (sbase - raw) + G::kRingBytes) +
                       (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
-    run_epilogue<MODE, PAIR>(p, tmem, accf0, acce0, abort, stage);
+    // TMA-store epilogue: a 4 KB box buffer per warp from the end of the
+    // stages in use (the unused stages and the slices above).
+    const uint32_t ybox = sbase + (uint32_t)p.stages * G::kStageBytes + (uint32_t)(warp - kEpiWarp0) * kYBoxBytes;
+    run_epilogue<MODE, PAIR>(p, &tmZ, tmem, accf0, acce0, abort, stage, ybox);
+    // Every tensor store has read its box before the CTA can exit.
+    if (p.y_tma && lane == 0) bulk_wait_all();
   } else if (MODE == kGroupedQ) {
     run_convert<MODE, PAIR>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
   } else if (MODE == kTF32) {
@@ -1339,10 +1393,29 @@ int max_pair_clusters() {
   }
 }
 
+// Ring stages for a launch: all of them, except that a TMA-store epilogue
+// (kDense / kSkinny) gives up whole stages until the box buffers of its
+// storing warps (4 KB each) fit in the freed stages plus the epilogue slices.
+template <int MODE, bool PAIR>
+void choose_stages(TcParams& p) {
+  using G = Geo<MODE, PAIR>;
+  p.stages = G::kStages;
+  if (MODE != kDense && MODE != kSkinny) p.y_tma = 0;
+  if (!p.y_tma) return;
+  const int need = (G::kTileN / Cfg<MODE, PAIR>::kCols) * 4 * kYBoxBytes;
+  while (p.stages > 2 && (G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) --p.stages;
+  if ((G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) {
+    p.y_tma = 0;
+    p.stages = G::kStages;
+  }
+}
+
 template <int MODE, bool PAIR>
 mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtensorMap& ms, const CUtensorMap& mz,
-                        const TcParams& p, int64_t work, cudaStream_t stream) {
+                        const TcParams& p_in, int64_t work, cudaStream_t stream) {
   constexpr int kSmem = Cfg<MODE, PAIR>::kSmem, kThreadsM = Cfg<MODE, PAIR>::kThreads;
+  TcParams p = p_in;
+  choose_stages<MODE, PAIR>(p);
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MM_ERR_CUDA;
@@ -1454,6 +1527,20 @@ int sm_count_public() { return sm_count(); }
 
 namespace {
 
+// The 16-bit output Y [batch.., M, N] (row stride y.rs, unit column stride) as
+// a tensor map of 32-row x 64-column boxes, 128-byte swizzled, for the
+// TMA-store epilogue: sets p->y_tma and p->y_bc when Y's layout fits TMA.
+void plan_output(const GemmArgs& g, TcParams* p, OperandPlan* y) {
+  p->y_tma = 0;
+  if (g.dtype != MM_BF16 && g.dtype != MM_F16) return;
+  if ((g.K + BK - 1) / BK > kYTmaMaxKb) return;
+  if (g.y.cs != 1 || g.y.rs < g.N) return;
+  if (!plan_operand(g.y.ptr, g.dtype, g.M, g.N, g.M == 1 ? (g.N + 7) / 8 * 8 : g.y.rs, 1, g.bm, g.y.bstride, 32, y))
+    return;
+  p->y_tma = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) p->y_bc[d] = y->bc[d];
+}
+
 bool plan_dense(const GemmArgs& g, bool pair, OperandPlan* a, OperandPlan* b) {
   if (g.dtype != MM_BF16 && g.dtype != MM_F16 && g.dtype != MM_F32) return false;
   if (g.M < 1 || g.N < 2 || g.K < 1) return false;
@@ -1513,7 +1600,9 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
         plan_operand(g.a.ptr, g.dtype, g.M, g.K, a_rs, g.a.cs, g.bm, g.a.bstride, BM / 2, &a) && !a.mn_major &&
         plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, 64, &b)) {
       p.idesc = make_idesc_mn(p.out_f16, 0, b.mn_major, BM, 64);
-      return launch_tc(kSkinny, false, a, b, p, stream);
+      OperandPlan ymap;
+      plan_output(g, &p, &ymap);
+      return launch_tc(kSkinny, false, a, b, p, stream, nullptr, p.y_tma ? &ymap : nullptr);
     }
   }
   // CTA pairs (256-row tiles) for long-K products with more than one row tile;
@@ -1528,7 +1617,10 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
     p.pair_tail = pair && !p.out_f32 && !a.mn_major &&
                   plan_operand(g.a.ptr, g.dtype, g.M, g.K, g.a.rs, g.a.cs, g.bm, g.a.bstride, BM / 2, &a_tail);
     if (p.pair_tail) p.idesc_tail = make_idesc_rows(p.out_f16, 0, b.mn_major, BM);
-    const mm_status st = launch_tc(p.out_f32 ? kTF32 : kDense, pair, a, b, p, stream, p.pair_tail ? &a_tail : nullptr);
+    OperandPlan ymap;
+    plan_output(g, &p, &ymap);
+    const mm_status st = launch_tc(p.out_f32 ? kTF32 : kDense, pair, a, b, p, stream,
+                                   p.pair_tail ? &a_tail : nullptr, p.y_tma ? &ymap : nullptr);
     if (st != MM_ERR_UNSUPPORTED || !pair) return st;
   }
   return MM_ERR_UNSUPPORTED;
