@@ -51,6 +51,10 @@ import workloads  # noqa: E402
 
 METRIC = "achieved TFLOPS/TOPS and % of GB300 dense tensor peak, per config"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# CUDA-core peaks (nominal, not measured): the fp64 rate of the part, and
+# 152 SMs x 64 integer multiply-adds per SM and clock x 2 ops x 2.07 GHz.
+ALU_PEAKS = {"gemm_f64_simt": (1.25, "nominal GB300 fp64, TFLOP/s"),
+             "gemm_i32_simt": (152 * 64 * 2 * 2.07e9 / 1e12, "152 SMs x 64 IMAD/clk x 2 ops x 2.07 GHz, TOP/s")}
 L2_BYTES = 129 * 10 ** 6
 # The other workloads' short loops (compared with the burst peak, itself a
 # short best-of-10 measurement) each start after this much idle time, so
@@ -409,8 +413,10 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=True):
         ms, _ = time_loop(lambda: qg.mm_gemm(A, B, None, 1.0, 0.0, 0, 0, out=Yx), 5, 2, world, stream,
                           idle_s=EXTRA_IDLE_S)
         assert qg.mm_last_path() == qg.MM_PATH_SIMT
-        out[name] = {"value": 2 * 4096 ** 3 / ms / 1e9, "unit": "TFLOP/s" if dt.is_floating_point else "TOP/s",
-                     "ms_per_call": ms, "bound": "alu", "kernel": "simt_gemm_kernel", "shape": "4096^3"}
+        val = 2 * 4096 ** 3 / ms / 1e9
+        out[name] = {"value": val, "unit": "TFLOP/s" if dt.is_floating_point else "TOP/s",
+                     "ms_per_call": ms, "bound": "alu", "kernel": "simt_gemm_kernel", "shape": "4096^3",
+                     "peak": ALU_PEAKS[name][0], "frac": val / ALU_PEAKS[name][0], "peak_note": ALU_PEAKS[name][1]}
         del A, B, Yx
     torch.cuda.empty_cache()
 
@@ -697,20 +703,21 @@ def compact(entry, keys):
 # Workload name in the detail -> key in per_config: the five configurations,
 # then the type variants at the same sizes.
 PER_CONFIG = (
-    ("1_matmul_f32", "matmul_f32", ("value", "unit", "us_per_call", "us_per_graph_replay", "bound", "paths",
+    ("1_matmul_f32", "matmul_f32", ("value", "unit", "us_per_call", "us_per_graph_replay", "paths",
                                     "cpu_baseline")),
     ("3_matmul_bf16_bcast", "matmul_bf16_bcast", ("value", "unit", "ms_per_call", "achieved_gbs", "frac",
-                                                 "peak_gbs", "frac_of_write_peak", "write_peak_gbs",
-                                                 "cpu_baseline")),
+                                                 "frac_of_write_peak", "write_peak_gbs", "cpu_baseline")),
     ("4_qlinear_s8", "qlinear_s8", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
     ("5_grouped_bf16", "grouped_bf16", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
-    ("f1_qlinear_u8", "qlinear_u8", ("value", "unit", "ms_per_call", "frac")),
-    ("f1_qlinear_u8s8_f16scales", "qlinear_u8s8_f16scales", ("value", "unit", "ms_per_call", "frac")),
-    ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "unit", "ms_per_call", "frac")),
-    ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "unit", "ms_per_call", "frac")),
-    ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "unit", "ms_per_call", "frac")),
-    ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "unit", "ms_per_call", "frac")),
-    ("f4_gemm_f32", "gemm_f32", ("value", "unit", "ms_per_call", "frac", "peak_tflops")),
+    ("f1_qlinear_u8", "qlinear_u8", ("value", "ms_per_call", "frac")),
+    ("f1_qlinear_u8s8_f16scales", "qlinear_u8s8_f16scales", ("value", "ms_per_call", "frac")),
+    ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "ms_per_call", "frac")),
+    ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "ms_per_call", "frac")),
+    ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "ms_per_call", "frac")),
+    ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "ms_per_call", "frac")),
+    ("f4_gemm_f32", "gemm_f32", ("value", "ms_per_call", "frac")),
+    ("a13_gemm_f64_simt", "gemm_f64_simt", ("value", "ms_per_call", "frac")),
+    ("a13_gemm_i32_simt", "gemm_i32_simt", ("value", "ms_per_call", "frac")),
 )
 
 
@@ -767,10 +774,9 @@ def run_ours(args, rank, world, local):
         except Exception as exc:  # noqa: BLE001 - reported in the JSON line
             extras = {"error": "%s: %s" % (type(exc).__name__, exc)}
 
+    # (the headline's roofline and CPU baseline are in the line itself)
     per_config = {"2_gemm_bf16": {"value": _r(tflops_rank), "unit": "TFLOP/s", "ms_per_call": _r(ms),
-                                  "frac": _r(tflops_rank / peak), "peak_tflops": peak,
-                                  "cpu_baseline": dict(compact({"c": cpu}, ("c",))["c"], sample="%d of 8192 rows" % 256)
-                                  if cpu else None}}
+                                  "frac": _r(tflops_rank / peak)}}
     for key, name, keys in PER_CONFIG:
         if name in extras:
             per_config[key] = compact(extras[name], keys)

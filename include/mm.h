@@ -93,9 +93,10 @@ const char* mm_version(void);
  * makes calls they cannot run return MM_ERR_UNSUPPORTED.  MM_PATH_VECTOR forces
  * the few-row kernel for MatMul and Gemm (MM_ERR_UNSUPPORTED where it does not
  * apply) and acts as MM_PATH_AUTO for the other operators.  Under
- * MM_PATH_AUTO the few-row kernels take every MatMul/Gemm call they can run,
- * except 3 or 4 rows of bf16/f16 against MN-major B' (the tensor cores are as
- * fast there).
+ * MM_PATH_AUTO the few-row kernels take every MatMul/Gemm call they can run
+ * that streams at least 2^17 elements of B' (N * K * batch), except 3 or 4
+ * rows of bf16/f16 against MN-major B' (the tensor cores are as fast there);
+ * smaller ones run on the CUDA-core tiles.
  * Meant for tests and measurements.  Returns MM_ERR_INVALID_ARG for an unknown
  * value. */
 mm_status mm_set_path_policy(int32_t policy);

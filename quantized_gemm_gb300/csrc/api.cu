@@ -181,9 +181,14 @@ mm_status finish(mm_status s, int path) {
 // MatMul and Gemm after validation: the few-row kernel where it applies (policy
 // MM_PATH_AUTO, or forced by MM_PATH_VECTOR), else the tensor-core or the
 // CUDA-core tiles.
+// The few-row kernels pay when they stream at least 2^17 elements of B'
+// (their k split and cross-CTA reduction cost a few microseconds); smaller
+// products take one pass of the CUDA-core tiles.
+bool few_row_pays(const GemmArgs& g) { return (double)g.N * (double)g.K * (double)g.bm.count >= 131072.0; }
+
 mm_status run_dense(const GemmArgs& g, bool pays, cudaStream_t st) {
   const int pol = g_policy.load();
-  if (pol == MM_PATH_VECTOR || (pol == MM_PATH_AUTO && vec_gemm_preferred(g))) {
+  if (pol == MM_PATH_VECTOR || (pol == MM_PATH_AUTO && vec_gemm_preferred(g) && few_row_pays(g))) {
     if (!vec_gemm_supported(g)) return MM_ERR_UNSUPPORTED;
     return finish(launch_vec_gemm(g, st), MM_PATH_VECTOR);
   }

@@ -58,6 +58,8 @@ struct GroupedArgs {
 };
 
 mm_status launch_simt_gemm(const GemmArgs& args, cudaStream_t stream);
+// Multiprocessors of the current device (cached per device).
+int sm_count_public();
 // Products with at most kVecMaxRows rows of A' (bf16, f16, f32): one pass over
 // B' on the CUDA cores, for K-major B' (k contiguous in A' and B', 16-byte
 // aligned rows of A' and columns of B') and for MN-major B' (n contiguous,

@@ -124,19 +124,158 @@ template <> struct Epi<uint32_t> : EpiInt<uint32_t, uint32_t> {};
 template <> struct Epi<int64_t> : EpiInt<int64_t, uint64_t> {};
 template <> struct Epi<uint64_t> : EpiInt<uint64_t, uint64_t> {};
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmArgs p) {
+// ------------------------------------------------------------------ tiled CUDA-core GEMM
+
+// A block of 256 threads (16 x 16) computes a (16*TM) x (16*TN) output tile,
+// TM x TN outputs per thread.  A thread's rows are ty*RM + i in each of the
+// tile's TM/RM row bands (RM = 16 bytes of accumulators), and likewise its
+// columns, so that each step over k reads its A and B values from shared
+// memory as 16-byte vectors (conflict-free: the 16 threads of a half-warp read
+// 256 consecutive bytes of B, the two halves the same words of A) and the
+// output rows are written 16 bytes per thread, 256 bytes per half-warp.
+//
+// K goes through shared memory in slabs of kSlab, double-buffered: the global
+// loads of slab s+1 are issued before slab s is multiplied, so a small product
+// pays the memory latency about once instead of once per slab.  An operand
+// that is contiguous along one of its dimensions, with 16-byte aligned rows and
+// batches, is read 16 bytes per thread (along k, or along m / n); any other
+// layout element by element with its strides.
+constexpr int kSlab = 16;
+
+enum SimtLoad { kLoadScalar = 0, kLoadVecK = 1, kLoadVecMN = 2 };
+
+// One operand of the tile as the kernel reads it: R "rows" (m of A, n of B),
+// row stride rs and k stride ks (elements), the load mode, and for the
+// element-by-element mode whether consecutive threads go along k (k is the
+// smaller stride) or along the rows.
+struct SimtOperand {
+  int mode, along_k;
+};
+
+template <typename T, int R>
+struct SlabLoad {
   using Acc = typename Arith<T>::acc;
-  __shared__ Acc As[kTk][kTile + 1];
-  __shared__ Acc Bs[kTk][kTile + 1];
+  static constexpr int V = 16 / (int)sizeof(T);               // elements per 16-byte vector
+  static constexpr int NE = R * kSlab / kThreads;              // elements per thread (scalar mode)
+  static constexpr int NV = R * kSlab / V;                     // vectors per slab
+  static constexpr int NVT = (NV + kThreads - 1) / kThreads;   // vectors per thread
+  static_assert(NE * sizeof(T) <= NVT * 16, "scalar-mode elements fit the vector registers");
+  // The loaded values as stored in memory: NVT vectors, or (scalar mode) NE
+  // elements packed in the same registers; converted when written to shared memory.
+  uint4 v[NVT];
+
+  // Global -> registers for the slab at k0 of the operand at `base` (rows r0..).
+  __device__ __forceinline__ void load(const T* base, int64_t rs, int64_t ks, int64_t r0, int64_t rows, int64_t k0,
+                                       int64_t K, SimtOperand op, int tid) {
+    if (op.mode == kLoadScalar) {
+#pragma unroll
+      for (int u = 0; u < NE; ++u) {
+        const int idx = tid + u * kThreads;
+        const int r = op.along_k ? idx / kSlab : idx % R, k = op.along_k ? idx % kSlab : idx / R;
+        const int64_t gr = r0 + r, gk = k0 + k;
+        reinterpret_cast<T*>(v)[u] = (gr < rows && gk < K) ? base[gr * rs + gk * ks] : T(0);
+      }
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < NVT; ++u) {
+      const int idx = tid + u * kThreads;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx >= NV) continue;
+      int64_t gr, gk;
+      bool full;
+      if (op.mode == kLoadVecK) {
+        gr = r0 + idx / (kSlab / V);
+        gk = k0 + (int64_t)(idx % (kSlab / V)) * V;
+        full = gr < rows && gk + V <= K;
+        if (!full && gr < rows) {        // the k tail: element by element
+          T* t = reinterpret_cast<T*>(&v[u]);
+          for (int c = 0; c < V; ++c)
+            if (gk + c < K) t[c] = base[gr * rs + (gk + c) * ks];
+        }
+      } else {
+        gk = k0 + idx / (R / V);
+        gr = r0 + (int64_t)(idx % (R / V)) * V;
+        full = gk < K && gr + V <= rows;
+        if (!full && gk < K) {           // the row tail
+          T* t = reinterpret_cast<T*>(&v[u]);
+          for (int c = 0; c < V; ++c)
+            if (gr + c < rows) t[c] = base[(gr + c) * rs + gk * ks];
+        }
+      }
+      if (full) v[u] = __ldg(reinterpret_cast<const uint4*>(base + gr * rs + gk * ks));
+    }
+  }
+
+  // Registers -> shared memory slab S[k][r] (row pitch P).
+  template <int P>
+  __device__ __forceinline__ void store(Acc (*S)[P], SimtOperand op, int tid) const {
+    if (op.mode == kLoadScalar) {
+#pragma unroll
+      for (int u = 0; u < NE; ++u) {
+        const int idx = tid + u * kThreads;
+        const int r = op.along_k ? idx / kSlab : idx % R, k = op.along_k ? idx % kSlab : idx / R;
+        S[k][r] = Arith<T>::load(reinterpret_cast<const T*>(v) + u);
+      }
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < NVT; ++u) {
+      const int idx = tid + u * kThreads;
+      if (idx >= NV) continue;
+      const T* t = reinterpret_cast<const T*>(&v[u]);
+      if (op.mode == kLoadVecK) {
+        const int r = idx / (kSlab / V), k = (idx % (kSlab / V)) * V;
+#pragma unroll
+        for (int c = 0; c < V; ++c) S[k + c][r] = Arith<T>::load(t + c);
+      } else {
+        const int k = idx / (R / V), r = (idx % (R / V)) * V;
+#pragma unroll
+        for (int c = 0; c < V; ++c) S[k][r + c] = Arith<T>::load(t + c);
+      }
+    }
+  }
+};
+
+// RM consecutive accumulators from shared memory (RM * sizeof(Acc) = 16 bytes,
+// or fewer for small tiles).
+template <typename Acc, int RM>
+__device__ __forceinline__ void lds_vec(const Acc* src, Acc (&dst)[RM]) {
+  if constexpr (RM * sizeof(Acc) == 16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    memcpy(dst, &u, 16);
+  } else if constexpr (RM * sizeof(Acc) == 8) {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    memcpy(dst, &u, 8);
+  } else {
+#pragma unroll
+    for (int i = 0; i < RM; ++i) dst[i] = src[i];
+  }
+}
+
+// Two blocks per SM (at most 128 registers a thread) except for the 8 x 8
+// tiles, whose 64 accumulators would then spill.
+template <typename T, int TM, int TN>
+__global__ void __launch_bounds__(kThreads, TM == 8 ? 1 : 2)
+    simt_gemm_kernel(const GemmArgs p, SimtOperand opa, SimtOperand opb) {
+  using Acc = typename Arith<T>::acc;
+  constexpr int RM = (16 / (int)sizeof(Acc)) < TM ? 16 / (int)sizeof(Acc) : TM;   // rows per band
+  constexpr int RN = (16 / (int)sizeof(Acc)) < TN ? 16 / (int)sizeof(Acc) : TN;
+  constexpr int BMt = 16 * TM, BNt = 16 * TN;
+  constexpr int PA = BMt + 16 / (int)sizeof(Acc), PB = BNt + 16 / (int)sizeof(Acc);   // padded row pitch
+  __shared__ __align__(16) Acc As[2][kSlab][PA];
+  __shared__ __align__(16) Acc Bs[2][kSlab][PB];
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;
-  const int64_t n0 = (int64_t)blockIdx.x * kTile;
-  const int64_t mtiles = (p.M + kTile - 1) / kTile;
+  const int64_t n0 = (int64_t)blockIdx.x * BNt;
+  const int64_t mtiles = (p.M + BMt - 1) / BMt;
   const T* A = static_cast<const T*>(p.a.ptr);
   const T* B = static_cast<const T*>(p.b.ptr);
   const T* C = static_cast<const T*>(p.c.ptr);
   T* Y = static_cast<T*>(const_cast<void*>(p.y.ptr));
+  const int nslab = (int)((p.K + kSlab - 1) / kSlab);
+  SlabLoad<T, BMt> la;
+  SlabLoad<T, BNt> lb;
 
   for (int64_t bt = blockIdx.z; bt < p.bm.count; bt += gridDim.z) {
     const T* Ab = A + batch_offset(p.bm, p.a.bstride, bt);
@@ -144,46 +283,61 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmArgs p) {
     const T* Cb = C ? C + batch_offset(p.bm, p.c.bstride, bt) : nullptr;
     T* Yb = Y + batch_offset(p.bm, p.y.bstride, bt);
     for (int64_t mt = blockIdx.y; mt < mtiles; mt += gridDim.y) {
-      const int64_t m0 = mt * kTile;
-      Acc acc[4][4];
+      const int64_t m0 = mt * BMt;
+      Acc acc[TM][TN];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = Acc(0);
-
-      for (int64_t k0 = 0; k0 < p.K; k0 += kTk) {
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          const int e = tid + e4 * kThreads;
-          const int ar = e / kTk, ak = e % kTk;        // A tile: 64 rows x 16 k
-          const int64_t gm = m0 + ar, gk = k0 + ak;
-          As[ak][ar] = (gm < p.M && gk < p.K) ? Arith<T>::load(Ab + gm * p.a.rs + gk * p.a.cs) : Acc(0);
-          const int bk = e / kTile, bn = e % kTile;    // B tile: 16 k x 64 cols
-          const int64_t hk = k0 + bk, hn = n0 + bn;
-          Bs[bk][bn] = (hk < p.K && hn < p.N) ? Arith<T>::load(Bb + hk * p.b.rs + hn * p.b.cs) : Acc(0);
-        }
+        for (int j = 0; j < TN; ++j) acc[i][j] = Acc(0);
+      if (nslab > 0) {
+        la.load(Ab, p.a.rs, p.a.cs, m0, p.M, 0, p.K, opa, tid);
+        lb.load(Bb, p.b.cs, p.b.rs, n0, p.N, 0, p.K, opb, tid);
+        __syncthreads();   // the previous tile's last reads of buffer 0 are done
+        la.store(As[0], opa, tid);
+        lb.store(Bs[0], opb, tid);
         __syncthreads();
+      }
+      for (int s = 0; s < nslab; ++s) {
+        const int buf = s & 1;
+        if (s + 1 < nslab) {
+          la.load(Ab, p.a.rs, p.a.cs, m0, p.M, (int64_t)(s + 1) * kSlab, p.K, opa, tid);
+          lb.load(Bb, p.b.cs, p.b.rs, n0, p.N, (int64_t)(s + 1) * kSlab, p.K, opb, tid);
+        }
 #pragma unroll
-        for (int kk = 0; kk < kTk; ++kk) {
-          Acc av[4], bv[4];
+        for (int kk = 0; kk < kSlab; ++kk) {
+          Acc av[TM], bv[TN];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) av[i] = As[kk][ty + 16 * i];
+          for (int g = 0; g < TM / RM; ++g) {
+            Acc t[RM];
+            lds_vec<Acc, RM>(&As[buf][kk][g * 16 * RM + ty * RM], t);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx + 16 * j];
+            for (int i = 0; i < RM; ++i) av[g * RM + i] = t[i];
+          }
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int g = 0; g < TN / RN; ++g) {
+            Acc t[RN];
+            lds_vec<Acc, RN>(&Bs[buf][kk][g * 16 * RN + tx * RN], t);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = mac<Acc>(acc[i][j], av[i], bv[j]);
+            for (int j = 0; j < RN; ++j) bv[g * RN + j] = t[j];
+          }
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = mac<Acc>(acc[i][j], av[i], bv[j]);
+        }
+        if (s + 1 < nslab) {
+          la.store(As[buf ^ 1], opa, tid);
+          lb.store(Bs[buf ^ 1], opb, tid);
         }
         __syncthreads();
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t gm = m0 + ty + 16 * i;
+      for (int i = 0; i < TM; ++i) {
+        const int64_t gm = m0 + (i / RM) * 16 * RM + ty * RM + (i % RM);
         if (gm >= p.M) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t gn = n0 + tx + 16 * j;
+        for (int j = 0; j < TN; ++j) {
+          const int64_t gn = n0 + (j / RN) * 16 * RN + tx * RN + (j % RN);
           if (gn >= p.N) continue;
           const T* c = Cb ? Cb + gm * p.c.rs + gn * p.c.cs : nullptr;
           Yb[gm * p.y.rs + gn * p.y.cs] = Arith<T>::store(Epi<T>::apply(p, acc[i][j], c));
@@ -720,24 +874,68 @@ dim3 tile_grid(int64_t M, int64_t N, int64_t batch) {
   return dim3((unsigned)nt, (unsigned)(mt < 65535 ? mt : 65535), (unsigned)(batch < 65535 ? batch : 65535));
 }
 
+// How the tiled kernel reads an operand with `rows` rows (stride rs) and k
+// stride ks: 16-byte vectors along whichever dimension is contiguous when the
+// base, the other stride and every batch stride keep the vectors aligned;
+// otherwise element by element, consecutive threads along the smaller stride.
+SimtOperand simt_operand(const void* ptr, int elem, int64_t rs, int64_t ks, const BatchMap& bm,
+                         const int64_t* bstride) {
+  const int64_t v = 16 / elem;
+  bool aligned = (reinterpret_cast<uintptr_t>(ptr) % 16) == 0;
+  for (int d = 0; d < bm.nb; ++d) aligned = aligned && (bm.shape[d] <= 1 || bstride[d] % v == 0);
+  SimtOperand op;
+  op.along_k = (ks < 0 ? -ks : ks) <= (rs < 0 ? -rs : rs);
+  if (aligned && ks == 1 && rs % v == 0) op.mode = kLoadVecK;
+  else if (aligned && rs == 1 && ks % v == 0) op.mode = kLoadVecMN;
+  else op.mode = kLoadScalar;
+  return op;
+}
+
+template <typename T, int TM>
+mm_status launch_tile_cfg(const GemmArgs& p, cudaStream_t stream) {
+  constexpr int BT = 16 * TM;
+  const int64_t nt = (p.N + BT - 1) / BT, mt = (p.M + BT - 1) / BT;
+  if (nt > 0x7fffffff) return MM_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)nt, (unsigned)(mt < 65535 ? mt : 65535),
+                  (unsigned)(p.bm.count < 65535 ? p.bm.count : 65535));
+  const SimtOperand oa = simt_operand(p.a.ptr, (int)sizeof(T), p.a.rs, p.a.cs, p.bm, p.a.bstride);
+  const SimtOperand ob = simt_operand(p.b.ptr, (int)sizeof(T), p.b.cs, p.b.rs, p.bm, p.b.bstride);
+  simt_gemm_kernel<T, TM, TM><<<grid, kThreads, 0, stream>>>(p, oa, ob);
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+// The largest tile that still gives every SM a block: 128 x 128 (8 x 8 per
+// thread) for 32- and 16-bit types, 64 x 64 for 64-bit ones, down to 32 x 32
+// for small products, which are bound by latency rather than arithmetic.
+template <typename T>
+mm_status launch_tiles(const GemmArgs& p, cudaStream_t stream) {
+  const int64_t sms = sm_count_public();
+  auto tiles = [&](int64_t bt) { return ((p.M + bt - 1) / bt) * ((p.N + bt - 1) / bt) * p.bm.count; };
+  if constexpr (sizeof(typename Arith<T>::acc) == 8) {
+    if (tiles(64) >= sms) return launch_tile_cfg<T, 4>(p, stream);
+    return launch_tile_cfg<T, 2>(p, stream);
+  } else {
+    if (tiles(128) >= sms) return launch_tile_cfg<T, 8>(p, stream);
+    if (tiles(64) >= sms) return launch_tile_cfg<T, 4>(p, stream);
+    return launch_tile_cfg<T, 2>(p, stream);
+  }
+}
+
 }  // namespace
 
 mm_status launch_simt_gemm(const GemmArgs& p, cudaStream_t stream) {
   if (p.M == 0 || p.N == 0 || p.bm.count == 0) return MM_OK;
-  if ((p.N + kTile - 1) / kTile > 0x7fffffff) return MM_ERR_UNSUPPORTED;
-  const dim3 grid = tile_grid(p.M, p.N, p.bm.count);
   switch (p.dtype) {
-    case MM_BF16: simt_gemm_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_F16: simt_gemm_kernel<__half><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_F32: simt_gemm_kernel<float><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_F64: simt_gemm_kernel<double><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_I32: simt_gemm_kernel<int32_t><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_I64: simt_gemm_kernel<int64_t><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_U32: simt_gemm_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(p); break;
-    case MM_U64: simt_gemm_kernel<uint64_t><<<grid, kThreads, 0, stream>>>(p); break;
+    case MM_BF16: return launch_tiles<__nv_bfloat16>(p, stream);
+    case MM_F16: return launch_tiles<__half>(p, stream);
+    case MM_F32: return launch_tiles<float>(p, stream);
+    case MM_F64: return launch_tiles<double>(p, stream);
+    case MM_I32: return launch_tiles<int32_t>(p, stream);
+    case MM_I64: return launch_tiles<int64_t>(p, stream);
+    case MM_U32: return launch_tiles<uint32_t>(p, stream);
+    case MM_U64: return launch_tiles<uint64_t>(p, stream);
     default: return MM_ERR_DTYPE;
   }
-  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
 bool vec_gemm_supported(const GemmArgs& p) {

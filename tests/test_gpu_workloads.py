@@ -51,11 +51,12 @@ def _cols(n, seed, least=64):
 
 
 def test_matmul_f32_full():
-    """The small f32 workload runs on the CUDA cores (FFMA): the [4,128,64] @
-    [64,96] product on the tiled kernel (3.1 M multiply-adds, below the 2^24 at
-    which three tf32 products pay), the promoted 1-D one on the few-row kernel."""
+    """The small f32 workload runs on the CUDA cores (FFMA) in the tiled
+    kernel: the [4,128,64] @ [64,96] product (3.1 M multiply-adds, below the
+    2^24 at which three tf32 products pay) and the promoted 1-D one (24576
+    elements of B', below the 2^17 at which the few-row kernel pays)."""
     d = workloads.matmul_f32(device=DEV)
-    for (a, b), path in (((d["A"], d["B"]), qg.MM_PATH_SIMT), ((d["A1"], d["B1"]), qg.MM_PATH_VECTOR)):
+    for (a, b), path in (((d["A"], d["B"]), qg.MM_PATH_SIMT), ((d["A1"], d["B1"]), qg.MM_PATH_SIMT)):
         y = qg.mm_matmul(a, b)
         assert qg.mm_last_path() == path
         an, bn = to_np(a), to_np(b)
