@@ -51,10 +51,9 @@ import workloads  # noqa: E402
 
 METRIC = "achieved TFLOPS/TOPS and % of GB300 dense tensor peak, per config"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# CUDA-core peaks (nominal, not measured): the fp64 rate of the part, and
-# 152 SMs x 64 integer multiply-adds per SM and clock x 2 ops x 2.07 GHz.
-ALU_PEAKS = {"gemm_f64_simt": (1.25, "nominal GB300 fp64, TFLOP/s"),
-             "gemm_i32_simt": (152 * 64 * 2 * 2.07e9 / 1e12, "152 SMs x 64 IMAD/clk x 2 ops x 2.07 GHz, TOP/s")}
+# CUDA-core peak probes (mm_alu_probe op, dependent steps per chain): int32
+# multiply-add for the int32 GEMM, fp64 FMA for the f64 one.
+ALU_PROBES = {"gemm_i32_simt": (0, 100000), "gemm_f64_simt": (1, 4000)}
 L2_BYTES = 129 * 10 ** 6
 # The other workloads' short loops (compared with the burst peak, itself a
 # short best-of-10 measurement) each start after this much idle time, so
@@ -177,7 +176,7 @@ def l2_flusher(device):
     torch.cuda.synchronize(device)
 
     def flush():
-        torch.sum(buf, out=sink)
+        sink.copy_(buf.sum())
     return flush
 
 
@@ -300,6 +299,25 @@ def stream_peaks(dev, world, stream):
     return out
 
 
+def alu_peak(dev, stream, op, iters):
+    """Peak multiply-add rate of one CUDA-core instruction (2 ops each), in
+    T ops/s: best of 3 launches of the library's arithmetic-rate probe."""
+    import quantized_gemm_gb300 as qg
+    macs = qg.mm_alu_probe(op, iters)
+    out = torch.empty(macs // (8 * iters), dtype=torch.float64, device=dev)
+    qg.mm_alu_probe(op, iters, out=out)
+    best = None
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        qg.mm_alu_probe(op, iters, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    return 2.0 * macs / best / 1e9
+
+
 def bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=True):
     """The four other workloads and their type variants: one call of the public API per step.
     With cpu, the C++ oracle is also timed on a sample of each of the four."""
@@ -414,9 +432,11 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=True):
                           idle_s=EXTRA_IDLE_S)
         assert qg.mm_last_path() == qg.MM_PATH_SIMT
         val = 2 * 4096 ** 3 / ms / 1e9
+        apeak = alu_peak(dev, stream, *ALU_PROBES[name])
         out[name] = {"value": val, "unit": "TFLOP/s" if dt.is_floating_point else "TOP/s",
                      "ms_per_call": ms, "bound": "alu", "kernel": "simt_gemm_kernel", "shape": "4096^3",
-                     "peak": ALU_PEAKS[name][0], "frac": val / ALU_PEAKS[name][0], "peak_note": ALU_PEAKS[name][1]}
+                     "peak": apeak, "frac": val / apeak,
+                     "peak_note": "measured: mm_alu_probe %s chains" % ("int32 mad" if dt == torch.int32 else "fp64 fma")}
         del A, B, Yx
     torch.cuda.empty_cache()
 
@@ -716,8 +736,8 @@ PER_CONFIG = (
     ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "ms_per_call", "frac")),
     ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "ms_per_call", "frac")),
     ("f4_gemm_f32", "gemm_f32", ("value", "ms_per_call", "frac")),
-    ("a13_gemm_f64_simt", "gemm_f64_simt", ("value", "ms_per_call", "frac")),
-    ("a13_gemm_i32_simt", "gemm_i32_simt", ("value", "ms_per_call", "frac")),
+    ("a13_gemm_f64_simt", "gemm_f64_simt", ("value", "ms_per_call", "frac", "peak")),
+    ("a13_gemm_i32_simt", "gemm_i32_simt", ("value", "ms_per_call", "frac", "peak")),
 )
 
 

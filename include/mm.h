@@ -276,6 +276,21 @@ mm_status mm_grouped_matmul_noalloc(const mm_tensor* input, const mm_tensor* wei
  * call is asynchronous on `stream`; time it with events on that stream. */
 mm_status mm_stream_probe(void* dst, const void* src, size_t bytes, int32_t mode, void* stream);
 
+/* ---------------------------------------------------------------- arithmetic-rate measurement
+ * Not an operator (the pages have no counterpart): the peak rate of the
+ * CUDA-core multiply-add that the tiled kernels use for the types without a
+ * tensor-core path, against which they are compared.
+ *   op 0: mad.lo.u32 (int32 / uint32 GEMMs), op 1: fma.rn.f64 (f64),
+ *   op 2: fma.rn.f32 (f32 on the CUDA cores).
+ * Every thread of a grid of 4 blocks of 256 threads per SM runs 8 independent
+ * chains of `iters` dependent multiply-adds.  *multiply_adds (if not NULL)
+ * receives the total count (ops = 2 x that); out, device memory owned by the
+ * caller, 8-byte aligned, must hold one 8-byte value per thread (at most
+ * 4 * 256 * SMs values); with out NULL only the count is returned.  The call
+ * is asynchronous on `stream`; time it with events on that stream.
+ * Returns MM_ERR_INVALID_ARG for an unknown op, iters < 0 or a misaligned out. */
+mm_status mm_alu_probe(int32_t op, void* out, int64_t iters, int64_t* multiply_adds, void* stream);
+
 /* ---------------------------------------------------------------- device status
  * Synchronises `stream`, then returns and clears the device-side status of the
  * current device: MM_OK, MM_ERR_INDEX_RANGE or MM_ERR_TIMEOUT (the first set,

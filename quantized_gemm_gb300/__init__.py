@@ -21,6 +21,7 @@ __all__ = [
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "mm_grouped_matmul_qweights", "mm_grouped_matmul_qweights_workspace_size",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE", "MM_PATH_VECTOR", "mm_stream_probe",
+    "mm_alu_probe",
 ]
 
 MM_MAX_DIMS = 8
@@ -84,6 +85,7 @@ def _lib():
             "mm_grouped_matmul_qweights_workspace_size": ([T, T, T, T, I64, T, ctypes.POINTER(SZ)], I32),
             "mm_grouped_matmul_qweights": ([T, T, T, T, I64, T, T, T, P, SZ, P], I32),
             "mm_stream_probe": ([P, P, SZ, I32, P], I32),
+            "mm_alu_probe": ([I32, P, I64, P, P], I32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -185,6 +187,18 @@ def mm_stream_probe(dst, src=None, mode=0, stream=None):
         raise ValueError("src and dst must have the same size in bytes")
     _check(_lib().mm_stream_probe(dst.data_ptr(), None if src is None else src.data_ptr(), nbytes, int(mode),
                                   _stream(dst, stream)), "mm_stream_probe")
+
+
+def mm_alu_probe(op, iters, out=None, stream=None):
+    """Arithmetic-rate probe (op 0 int32 multiply-add, 1 fp64 FMA, 2 fp32 FMA):
+    returns the number of multiply-adds the launch performs; with ``out`` (a
+    device tensor of at least that many / (8 * iters) 8-byte elements) it also
+    launches the probe on the current stream."""
+    n = ctypes.c_int64(0)
+    ptr = None if out is None else out.data_ptr()
+    st = None if out is None else _stream(out, stream)
+    _check(_lib().mm_alu_probe(int(op), ptr, int(iters), ctypes.byref(n), st), "mm_alu_probe")
+    return n.value
 
 
 def mm_matmul(A, B, out=None, stream=None):

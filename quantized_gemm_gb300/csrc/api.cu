@@ -678,6 +678,18 @@ mm_status mm_stream_probe(void* dst, const void* src, size_t bytes, int32_t mode
   return launch_stream_probe(dst, src, (int64_t)bytes, mode, static_cast<cudaStream_t>(stream));
 }
 
+mm_status mm_alu_probe(int32_t op, void* out, int64_t iters, int64_t* multiply_adds, void* stream) {
+  if (op != kAluImad && op != kAluDfma && op != kAluFfma) return MM_ERR_INVALID_ARG;
+  if (iters < 0) return MM_ERR_INVALID_ARG;
+  int threads = 0;
+  const mm_status st = launch_alu_probe(op, nullptr, iters, &threads, static_cast<cudaStream_t>(stream));
+  if (st != MM_OK) return st;
+  if (multiply_adds) *multiply_adds = (int64_t)threads * kAluChains * iters;
+  if (!out) return MM_OK;
+  if (reinterpret_cast<uintptr_t>(out) & 7) return MM_ERR_INVALID_ARG;
+  return launch_alu_probe(op, out, iters, nullptr, static_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ device status
 
 mm_status mm_get_device_status(void* stream) {

@@ -134,13 +134,17 @@ template <> struct Epi<uint64_t> : EpiInt<uint64_t, uint64_t> {};
 // 256 consecutive bytes of B, the two halves the same words of A) and the
 // output rows are written 16 bytes per thread, 256 bytes per half-warp.
 //
-// K goes through shared memory in slabs of kSlab, double-buffered: the global
+// K goes through shared memory in slabs of KS, double-buffered: the global
 // loads of slab s+1 are issued before slab s is multiplied, so a small product
 // pays the memory latency about once instead of once per slab.  An operand
 // that is contiguous along one of its dimensions, with 16-byte aligned rows and
 // batches, is read 16 bytes per thread (along k, or along m / n); any other
 // layout element by element with its strides.
-constexpr int kSlab = 16;
+// Slab depth: 16 for the 8 x 8 tiles, deeper for the small tiles (every
+// thread still loads 8 32-bit or 4 64-bit values a slab), so that a small
+// product (K = 64 for 2 x 2 tiles) is a single slab: one memory latency.
+template <int TM, int ACC_BYTES>
+constexpr int slab_depth() { return TM >= 8 ? 16 : TM == 4 ? (ACC_BYTES == 8 ? 16 : 32) : (ACC_BYTES == 8 ? 32 : 64); }
 
 enum SimtLoad { kLoadScalar = 0, kLoadVecK = 1, kLoadVecMN = 2 };
 
@@ -152,7 +156,7 @@ struct SimtOperand {
   int mode, along_k;
 };
 
-template <typename T, int R>
+template <typename T, int R, int kSlab>
 struct SlabLoad {
   using Acc = typename Arith<T>::acc;
   static constexpr int V = 16 / (int)sizeof(T);               // elements per 16-byte vector
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, TM == 8 ? 1 : 2)
   constexpr int RN = (16 / (int)sizeof(Acc)) < TN ? 16 / (int)sizeof(Acc) : TN;
   constexpr int BMt = 16 * TM, BNt = 16 * TN;
   constexpr int PA = BMt + 16 / (int)sizeof(Acc), PB = BNt + 16 / (int)sizeof(Acc);   // padded row pitch
+  constexpr int kSlab = slab_depth<TM, (int)sizeof(Acc)>();
   __shared__ __align__(16) Acc As[2][kSlab][PA];
   __shared__ __align__(16) Acc Bs[2][kSlab][PB];
   const int tid = threadIdx.x;
@@ -274,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, TM == 8 ? 1 : 2)
   const T* C = static_cast<const T*>(p.c.ptr);
   T* Y = static_cast<T*>(const_cast<void*>(p.y.ptr));
   const int nslab = (int)((p.K + kSlab - 1) / kSlab);
-  SlabLoad<T, BMt> la;
-  SlabLoad<T, BNt> lb;
+  SlabLoad<T, BMt, kSlab> la;
+  SlabLoad<T, BNt, kSlab> lb;
 
   for (int64_t bt = blockIdx.z; bt < p.bm.count; bt += gridDim.z) {
     const T* Ab = A + batch_offset(p.bm, p.a.bstride, bt);

@@ -1,5 +1,6 @@
 // Streaming kernels that measure the memory roofline this library's kernels
-// are judged against: a write-only stream (the bound of a product whose
+// are judged against (and, at the end, the arithmetic-rate probe of the
+// CUDA-core instructions the tiled GEMM uses): a write-only stream (the bound of a product whose
 // traffic is almost all output, such as a batched product with a 128-deep k)
 // and a copy.  They are measurement helpers, not operator steps.
 //
@@ -70,6 +71,52 @@ __global__ void __launch_bounds__(32) write_bulk_kernel(char* dst, int64_t bytes
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// kAluChains independent chains x = x * a + c per thread, `iters` steps each,
+// in the instruction being measured (inline PTX, so each step is one
+// mad.lo.u32 / fma.rn.f64 / fma.rn.f32); the chains' sum is stored so that
+// nothing is dead.  a and c come from the caller's arguments.
+template <int OP>
+__global__ void __launch_bounds__(kAluThreads) alu_probe_kernel(void* out, int64_t iters, uint32_t seed) {
+  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+  if constexpr (OP == kAluImad) {
+    uint32_t x[kAluChains];
+    const uint32_t a = seed | 1u, c = seed ^ 0x9e3779b9u;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) x[j] = tid + j;
+    for (int64_t i = 0; i < iters; ++i)
+#pragma unroll
+      for (int j = 0; j < kAluChains; ++j) asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(x[j]) : "r"(a), "r"(c));
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) s += x[j];
+    static_cast<uint32_t*>(out)[tid] = s;
+  } else if constexpr (OP == kAluDfma) {
+    double x[kAluChains];
+    const double a = 1.0 - (double)(seed & 0xff) * 0x1p-40, c = 0x1p-30;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) x[j] = (double)(tid + j);
+    for (int64_t i = 0; i < iters; ++i)
+#pragma unroll
+      for (int j = 0; j < kAluChains; ++j) asm volatile("fma.rn.f64 %0, %0, %1, %2;" : "+d"(x[j]) : "d"(a), "d"(c));
+    double s = 0;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) s += x[j];
+    static_cast<double*>(out)[tid] = s;
+  } else {
+    float x[kAluChains];
+    const float a = 1.0f - (float)(seed & 0xff) * 0x1p-20f, c = 0x1p-12f;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) x[j] = (float)(tid + j);
+    for (int64_t i = 0; i < iters; ++i)
+#pragma unroll
+      for (int j = 0; j < kAluChains; ++j) asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+f"(x[j]) : "f"(a), "f"(c));
+    float s = 0;
+#pragma unroll
+    for (int j = 0; j < kAluChains; ++j) s += x[j];
+    static_cast<float*>(out)[tid] = s;
+  }
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -96,6 +143,22 @@ mm_status launch_stream_probe(void* dst, const void* src, int64_t bytes, int mod
       break;
     default:
       return MM_ERR_INVALID_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+}
+
+mm_status launch_alu_probe(int op, void* out, int64_t iters, int* threads_out, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return MM_ERR_CUDA;
+  const int blocks = sms * kAluBlocksPerSm;
+  if (threads_out) *threads_out = blocks * kAluThreads;
+  if (!out) return MM_OK;
+  const uint32_t seed = (uint32_t)(iters * 2654435761u);
+  switch (op) {
+    case kAluImad: alu_probe_kernel<kAluImad><<<blocks, kAluThreads, 0, stream>>>(out, iters, seed); break;
+    case kAluDfma: alu_probe_kernel<kAluDfma><<<blocks, kAluThreads, 0, stream>>>(out, iters, seed); break;
+    case kAluFfma: alu_probe_kernel<kAluFfma><<<blocks, kAluThreads, 0, stream>>>(out, iters, seed); break;
+    default: return MM_ERR_INVALID_ARG;
   }
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }

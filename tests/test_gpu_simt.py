@@ -308,3 +308,55 @@ def test_gemm_integer_non_integral_saturates():
     assert Y.item() == 0
     Y = qg.mm_gemm(A[:, :1], B[:1], None, 1.5, 1.0, 0, 0)          # 1.5 * (2^31 - 1) > 2^31 - 1
     assert Y.item() == 2 ** 31 - 1
+
+
+# Shapes that select each register tile of the tiled CUDA-core kernel (8 x 8
+# threads' outputs in 128 x 128 blocks when there are at least as many such
+# blocks as SMs, 4 x 4 in 64 x 64 blocks, else 2 x 2), with ragged M, N and K
+# tails, in every layout its loads distinguish: 16-byte vectors along k (A
+# row-major, B stored [N, K]), along m / n (A stored [K, M], B row-major) and
+# element by element (an odd row stride).
+TILE_CASES = [
+    (torch.float32, 1300, 1800, 97),    # 8 x 8 (165 blocks of 128 x 128)
+    (torch.int32, 1300, 1800, 97),
+    (torch.bfloat16, 1300, 1800, 97),
+    (torch.float32, 900, 700, 200),     # 4 x 4
+    (torch.uint32, 900, 700, 200),
+    (torch.float64, 700, 900, 61),      # 64-bit: 4 x 4 (165 blocks of 64 x 64)
+    (torch.int64, 700, 900, 61),
+    (torch.float64, 100, 90, 150),      # 2 x 2
+]
+
+
+@pytest.mark.parametrize("dtype,M,N,K", TILE_CASES, ids=lambda v: str(v))
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1), (0, 1)])
+def test_gemm_simt_register_tiles(dtype, M, N, K, tA, tB):
+    A = rand_tensor((K, M) if tA else (M, K), dtype, 41, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), dtype, 42, DEV)
+    alpha, beta = (1.0, 0.0)
+    with policy(qg.MM_PATH_SIMT):
+        Y = qg.mm_gemm(A, B, None, alpha, beta, tA, tB)
+    assert qg.mm_last_path() == qg.MM_PATH_SIMT
+    ref, scale = _gemm_ref(A, B, None, alpha, beta, tA, tB)
+    if dtype in TOL:
+        assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
+    else:
+        assert np.array_equal(to_np(Y), ref)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int32, torch.float64], ids=str)
+def test_gemm_simt_register_tiles_scalar_loads(dtype):
+    # Row strides of 1301 / 1803 elements: no 16-byte alignment, so both
+    # operands take the element-by-element loads, with a C broadcast row.
+    M, N, K = 1300, 1800, 70
+    Ab = rand_tensor((M, K + 1), dtype, 43, DEV)[:, 1:]
+    Bb = rand_tensor((K, N + 3), dtype, 44, DEV)[:, 3:]
+    C = rand_tensor((N,), dtype, 45, DEV)
+    alpha, beta = (0.5, 2.0) if dtype in TOL else (3.0, -2.0)
+    with policy(qg.MM_PATH_SIMT):
+        Y = qg.mm_gemm(Ab, Bb, C, alpha, beta, 0, 0)
+    ref, scale = _gemm_ref(Ab, Bb, C, alpha, beta, 0, 0)
+    if dtype in TOL:
+        assert max_rel_err(to_np(Y), ref, scale) <= TOL[dtype]
+    else:
+        assert np.array_equal(to_np(Y), ref)
