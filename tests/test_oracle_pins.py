@@ -363,13 +363,20 @@ def test_gemm_brute_force(tA, tB, c_shape):
 
 
 def test_gemm_integer_exact():
-    A = np.array([[2 ** 31 - 1, 1]], np.int32)
+    A = np.array([[2 ** 31 - 1, 2]], np.int32)
     B = np.array([[1], [1]], np.int32)
     C = np.array([[5]], np.int32)
-    # A @ B = 2^31; 3 * 2^31 + (-1) * 5 = 2^31 - 5 (mod 2^32), which is the int32 2147483643.
+    # A @ B = 2^31 + 1, which wraps to the int32 -2^31 + 1; then
+    # 3 * (2^31 + 1) + (-1) * 5 = 3 * 2^31 - 2, which is 2^31 - 2 modulo 2^32:
+    # the int32 2147483646 (alpha taken as 1 would give 2^31 - 4).
     got = ORC.gemm(A, B, C, alpha=3.0, beta=-1.0)
-    want = ((3 * 2 ** 31 - 5) + 2 ** 31) % 2 ** 32 - 2 ** 31
+    want = ((3 * (2 ** 31 + 1) - 5) + 2 ** 31) % 2 ** 32 - 2 ** 31
+    assert want == 2 ** 31 - 2
     assert got.item() == want
+    # uint32, alpha 5, beta 7: 5 * (2^32 - 1) + 7 * 3 = 16 (mod 2^32)
+    U = np.array([[2 ** 32 - 1]], np.uint32)
+    got = ORC.gemm(U, np.array([[1]], np.uint32), np.array([[3]], np.uint32), alpha=5.0, beta=7.0)
+    assert got.item() == 16
 
 
 def test_gemm_integer_non_integral_alpha_beta():
