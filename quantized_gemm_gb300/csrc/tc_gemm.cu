@@ -109,9 +109,11 @@ constexpr int kSignalOff = 240;                  // 16 spare bytes of the contro
 
 __host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedQ; }
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
-// TMA-store epilogue for products of at most this many k-blocks (output-bound
-// ones): its box buffers cost a ring stage, which long-K products need more
-// (8192^3 Gemm: 0.610 -> 0.620 ms with it; batched K = 128 MatMul 0.494 -> 0.452 ms).
+// TMA-store epilogue: products of at most this many k-blocks (output-bound
+// ones) store 32 x 64 boxes from 4 KB buffers that cost a ring stage (batched
+// K = 128 MatMul 0.494 -> 0.452 ms); longer ones, which need every stage
+// (8192^3 Gemm 0.610 -> 0.620 ms with wide boxes), store 32 x 32 boxes from
+// the 2 KB staging slices (0.603 -> 0.601 ms).
 constexpr int kYTmaMaxKb = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
@@ -975,6 +977,37 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
           tc_fence_before();
           __syncwarp();
           release(buf);
+          const int32_t yrow0 = (int32_t)(ti.m0 + roff + rbase), yb = (int32_t)batch_off(p, p.y_bc, ti.batch);
+          if (p.y_tma == 2) {
+            // Narrow boxes (32 rows x 32 columns, 64-byte swizzle: row r's
+            // chunk c at c ^ ((r / 2) % 4)) in the warp's 2 KB staging slice,
+            // which needs no ring stage: two stores per tile, each waiting for
+            // the previous one to have read the slice.
+            const uint32_t sbox = smem_u32(stage);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
+              if (crow) add_c32(p, crow, ncol + 32 * h, v);
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                sts128(sbox + (uint32_t)lane * 64 + (((uint32_t)q ^ ((uint32_t)(lane >> 1) & 3u)) << 4),
+                       make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16),
+                                  pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
+                                  pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16),
+                                  pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16)));
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0 && rbase < rows_t) {
+                tma_store_3d(tmY, sbox, (int32_t)(ncol + 32 * h), yrow0, yb);
+                bulk_commit();
+              }
+            }
+            continue;
+          }
           // The buffer is reused once the previous tile's store has read it.
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
@@ -996,8 +1029,7 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0 && rbase < rows_t) {
-            tma_store_3d(tmY, ybox, (int32_t)ncol, (int32_t)(ti.m0 + roff + rbase),
-                         (int32_t)batch_off(p, p.y_bc, ti.batch));
+            tma_store_3d(tmY, ybox, (int32_t)ncol, yrow0, yb);
             bulk_commit();
           }
           continue;
@@ -1401,7 +1433,7 @@ void choose_stages(TcParams& p) {
   using G = Geo<MODE, PAIR>;
   p.stages = G::kStages;
   if (MODE != kDense && MODE != kSkinny) p.y_tma = 0;
-  if (!p.y_tma) return;
+  if (p.y_tma != 1) return;   // narrow boxes use the staging slices
   const int need = (G::kTileN / Cfg<MODE, PAIR>::kCols) * 4 * kYBoxBytes;
   while (p.stages > 2 && (G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) --p.stages;
   if ((G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) {
@@ -1533,11 +1565,41 @@ namespace {
 void plan_output(const GemmArgs& g, TcParams* p, OperandPlan* y) {
   p->y_tma = 0;
   if (g.dtype != MM_BF16 && g.dtype != MM_F16) return;
-  if ((g.K + BK - 1) / BK > kYTmaMaxKb) return;
-  if (g.y.cs != 1 || g.y.rs < g.N) return;
-  if (!plan_operand(g.y.ptr, g.dtype, g.M, g.N, g.M == 1 ? (g.N + 7) / 8 * 8 : g.y.rs, 1, g.bm, g.y.bstride, 32, y))
+  if (g.y.cs != 1 || g.y.rs < g.N || g.M < 1 || g.N < 1) return;
+  const bool wide = (g.K + BK - 1) / BK <= kYTmaMaxKb;   // wide boxes cost a ring stage
+  auto encode = encode_fn();
+  if (!encode || (reinterpret_cast<uintptr_t>(g.y.ptr) & 15)) return;
+  const int64_t pitch = g.M == 1 ? (g.N + 7) / 8 * 8 : g.y.rs;   // one row: any valid pitch
+  if (pitch % 8 || g.M > 0x7fffffffLL || g.N > 0x7fffffffLL) return;
+  int64_t unit = 0;
+  for (int d = 0; d < g.bm.nb; ++d)
+    if (g.bm.shape[d] > 1 && g.y.bstride[d] != 0) unit = gcd64(unit, g.y.bstride[d]);
+  int64_t nbat = 1;
+  for (int d = 0; d < kMaxBatchDims; ++d) y->bc[d] = 0;
+  if (unit != 0) {
+    if (unit % 8) return;
+    int64_t maxc = 0;
+    for (int d = 0; d < g.bm.nb; ++d)
+      if (g.bm.shape[d] > 1 && g.y.bstride[d] != 0) {
+        y->bc[d] = g.y.bstride[d] / unit;
+        maxc += (g.bm.shape[d] - 1) * y->bc[d];
+      }
+    nbat = maxc + 1;
+    if (nbat > 0x7fffffffLL) return;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)g.N, (cuuint64_t)g.M, (cuuint64_t)nbat};
+  const cuuint64_t strides[2] = {(cuuint64_t)pitch * 2,
+                                 unit != 0 ? (cuuint64_t)unit * 2 : (cuuint64_t)((pitch * 2 * g.M + 15) & ~15ll)};
+  if (strides[0] >= (1ull << 40) || strides[1] >= (1ull << 40)) return;
+  const cuuint32_t box[3] = {wide ? 64u : 32u, 32u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = g.dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (encode(&y->map, dt, 3, const_cast<void*>(g.y.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return;
-  p->y_tma = 1;
+  y->mn_major = 0;
+  p->y_tma = wide ? 1 : 2;
   for (int d = 0; d < kMaxBatchDims; ++d) p->y_bc[d] = y->bc[d];
 }
 
