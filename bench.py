@@ -304,7 +304,7 @@ def alu_peak(dev, stream, op, iters):
     T ops/s: best of 3 launches of the library's arithmetic-rate probe."""
     import quantized_gemm_gb300 as qg
     macs = qg.mm_alu_probe(op, iters)
-    out = torch.empty(macs // (8 * iters), dtype=torch.float64, device=dev)
+    out = torch.empty(macs // (qg.MM_ALU_CHAINS * iters), dtype=torch.float64, device=dev)
     qg.mm_alu_probe(op, iters, out=out)
     best = None
     for _ in range(3):

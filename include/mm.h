@@ -282,8 +282,8 @@ mm_status mm_stream_probe(void* dst, const void* src, size_t bytes, int32_t mode
  * tensor-core path, against which they are compared.
  *   op 0: mad.lo.u32 (int32 / uint32 GEMMs), op 1: fma.rn.f64 (f64),
  *   op 2: fma.rn.f32 (f32 on the CUDA cores).
- * Every thread of a grid of 4 blocks of 256 threads per SM runs 8 independent
- * chains of `iters` dependent multiply-adds.  *multiply_adds (if not NULL)
+ * Every thread of a grid of 4 blocks of 256 threads per SM runs 16
+ * independent chains of `iters` dependent multiply-adds.  *multiply_adds (if not NULL)
  * receives the total count (ops = 2 x that); out, device memory owned by the
  * caller, 8-byte aligned, must hold one 8-byte value per thread (at most
  * 4 * 256 * SMs values); with out NULL only the count is returned.  The call

@@ -21,7 +21,7 @@ __all__ = [
     "mm_qlinear_matmul_workspace_size", "mm_grouped_matmul_workspace_size", "mm_grouped_matmul_noalloc",
     "mm_grouped_matmul_qweights", "mm_grouped_matmul_qweights_workspace_size",
     "MM_PATH_AUTO", "MM_PATH_SIMT", "MM_PATH_TENSOR", "MM_PATH_NONE", "MM_PATH_VECTOR", "mm_stream_probe",
-    "mm_alu_probe",
+    "mm_alu_probe", "MM_ALU_CHAINS",
 ]
 
 MM_MAX_DIMS = 8
@@ -189,11 +189,15 @@ def mm_stream_probe(dst, src=None, mode=0, stream=None):
                                   _stream(dst, stream)), "mm_stream_probe")
 
 
+# Independent multiply-add chains per thread of mm_alu_probe (include/mm.h).
+MM_ALU_CHAINS = 16
+
+
 def mm_alu_probe(op, iters, out=None, stream=None):
     """Arithmetic-rate probe (op 0 int32 multiply-add, 1 fp64 FMA, 2 fp32 FMA):
     returns the number of multiply-adds the launch performs; with ``out`` (a
-    device tensor of at least that many / (8 * iters) 8-byte elements) it also
-    launches the probe on the current stream."""
+    device tensor of at least that many / (MM_ALU_CHAINS * iters) 8-byte
+    elements, one per thread) it also launches the probe on the current stream."""
     n = ctypes.c_int64(0)
     ptr = None if out is None else out.data_ptr()
     st = None if out is None else _stream(out, stream)

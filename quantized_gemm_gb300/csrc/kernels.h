@@ -78,7 +78,7 @@ mm_status launch_simt_grouped(const GroupedArgs& args, unsigned* status, cudaStr
 enum { kStreamWrite = 0, kStreamCopy = 1, kStreamWriteBulk = 2 };
 // Arithmetic-rate probe: dependent multiply-add chains of one instruction.
 enum { kAluImad = 0, kAluDfma = 1, kAluFfma = 2 };
-constexpr int kAluChains = 8;      // independent chains per thread
+constexpr int kAluChains = 16;     // independent chains per thread
 constexpr int kAluThreads = 256;   // threads per block
 constexpr int kAluBlocksPerSm = 4;
 mm_status launch_alu_probe(int op, void* out, int64_t iters, int* threads_out, cudaStream_t stream);

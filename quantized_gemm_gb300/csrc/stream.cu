@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kAluThreads) alu_probe_kernel(void* out, int64
     const uint32_t a = seed | 1u, c = seed ^ 0x9e3779b9u;
 #pragma unroll
     for (int j = 0; j < kAluChains; ++j) x[j] = tid + j;
+#pragma unroll 4
     for (int64_t i = 0; i < iters; ++i)
 #pragma unroll
       for (int j = 0; j < kAluChains; ++j) asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(x[j]) : "r"(a), "r"(c));
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kAluThreads) alu_probe_kernel(void* out, int64
     const double a = 1.0 - (double)(seed & 0xff) * 0x1p-40, c = 0x1p-30;
 #pragma unroll
     for (int j = 0; j < kAluChains; ++j) x[j] = (double)(tid + j);
+#pragma unroll 4
     for (int64_t i = 0; i < iters; ++i)
 #pragma unroll
       for (int j = 0; j < kAluChains; ++j) asm volatile("fma.rn.f64 %0, %0, %1, %2;" : "+d"(x[j]) : "d"(a), "d"(c));
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(kAluThreads) alu_probe_kernel(void* out, int64
     const float a = 1.0f - (float)(seed & 0xff) * 0x1p-20f, c = 0x1p-12f;
 #pragma unroll
     for (int j = 0; j < kAluChains; ++j) x[j] = (float)(tid + j);
+#pragma unroll 4
     for (int64_t i = 0; i < iters; ++i)
 #pragma unroll
       for (int j = 0; j < kAluChains; ++j) asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+f"(x[j]) : "f"(a), "f"(c));

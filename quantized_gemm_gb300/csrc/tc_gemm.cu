@@ -109,16 +109,9 @@ constexpr int kSignalOff = 240;                  // 16 spare bytes of the contro
 
 __host__ __device__ constexpr bool is_grouped(int mode) { return mode == kGrouped || mode == kGroupedQ; }
 constexpr int64_t kPairMinK = 1024;              // CTA pairs for K >= this
-// TMA-store epilogue: products of at most this many k-blocks (output-bound
-// ones) store 32 x 64 boxes from 4 KB buffers that cost a ring stage (batched
-// K = 128 MatMul 0.494 -> 0.452 ms); longer ones, which need every stage
-// (8192^3 Gemm 0.610 -> 0.620 ms with wide boxes), store 32 x 32 boxes from
-// the 2 KB staging slices (0.603 -> 0.601 ms).
-constexpr int kYTmaMaxKb = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kCtrlBytes = 256;                  // mbarriers, TMEM slot, abort flag
 constexpr int kStageWords = 32 * 16;             // float per-warp output staging: 32 rows x 64 bytes
-constexpr int kYBoxBytes = 32 * 128;             // TMA-store box per warp: 32 rows x 64 16-bit columns
 
 // Shape of the CTA: 16 epilogue warps of 64 columns each, enough warps to hide
 // the epilogue's latency (short-K float products, the QLinear requantisation).
@@ -335,7 +328,7 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
       }
       pending |= 1u << stage;
       pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == (uint32_t)p.stages) { stage = 0; phase ^= 1; }
+      if (++stage == G::kStages) { stage = 0; phase ^= 1; }
     }
   }
 done:
@@ -419,7 +412,7 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
         }
         if (PAIR) tc_commit_pair(empty0 + 8 * stage, 0x3);
         else tc_commit(empty0 + 8 * stage);
-        if (++stage == (uint32_t)p.stages) { stage = 0; phase ^= 1; }
+        if (++stage == G::kStages) { stage = 0; phase ^= 1; }
       }
       if (PAIR) tc_commit_pair(accf0 + 8 * buf, 0x3);
       else tc_commit(accf0 + 8 * buf);
@@ -784,7 +777,7 @@ __device__ void run_split(const TcParams& p, uint8_t* smem, uint32_t sbase, uint
 
 template <int MODE, bool PAIR>
 __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t tmem, uint32_t accf0, uint32_t acce0,
-                             volatile int* abort, uint32_t* stage, uint32_t ybox) {
+                             volatile int* abort, uint32_t* stage) {
   // Warp-private shared memory: QLinear column data (kQColWords) or the
   // output staging rows (kStageWords).
   int32_t* qcol = reinterpret_cast<int32_t*>(stage);
@@ -965,11 +958,7 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
       if constexpr (MODE == kDense || MODE == kSkinny) {
         if (p.y_tma) {
           // The warp's 32 rows x 64 columns: into registers, release the
-          // accumulator, then alpha/beta/C and the rounding to 16 bits into
-          // the warp's box buffer in the 128-byte swizzled layout of the
-          // output's tensor map (row r's 16-byte chunk c at c ^ (r % 8): the
-          // row-wise writes are conflict-free), and one tensor store of the
-          // box.  The store's clipping drops rows and columns past M and N.
+          // accumulator, then alpha/beta/C and the rounding to 16 bits.
           uint32_t r[2][32];
 #pragma unroll
           for (int c = 0; c < 2; ++c) tmem_ld32(taddr0 + c * 32, r[c]);
@@ -978,59 +967,33 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
           __syncwarp();
           release(buf);
           const int32_t yrow0 = (int32_t)(ti.m0 + roff + rbase), yb = (int32_t)batch_off(p, p.y_bc, ti.batch);
-          if (p.y_tma == 2) {
-            // Narrow boxes (32 rows x 32 columns, 64-byte swizzle: row r's
-            // chunk c at c ^ ((r / 2) % 4)) in the warp's 2 KB staging slice,
-            // which needs no ring stage: two stores per tile, each waiting for
-            // the previous one to have read the slice.
-            const uint32_t sbox = smem_u32(stage);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float v[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
-              if (crow) add_c32(p, crow, ncol + 32 * h, v);
-              if (lane == 0) bulk_wait_read_all();
-              __syncwarp();
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                sts128(sbox + (uint32_t)lane * 64 + (((uint32_t)q ^ ((uint32_t)(lane >> 1) & 3u)) << 4),
-                       make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16),
-                                  pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
-                                  pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16),
-                                  pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16)));
-              fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0 && rbase < rows_t) {
-                tma_store_3d(tmY, sbox, (int32_t)(ncol + 32 * h), yrow0, yb);
-                bulk_commit();
-              }
-            }
-            continue;
-          }
-          // The buffer is reused once the previous tile's store has read it.
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
+          // 32 columns at a time into the warp's 2 KB staging slice in the
+          // 64-byte swizzled layout of the output's tensor map (row r's 16-byte
+          // chunk c at c ^ ((r / 2) % 4): conflict-free row-wise writes), then
+          // one tensor store of the 32 x 32 box; before the slice is written
+          // again the previous store must have read it.  The store clips rows
+          // and columns past M and N.
+          const uint32_t sbox = smem_u32(stage);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[h][j]);
             if (crow) add_c32(p, crow, ncol + 32 * h, v);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t chunk = (uint32_t)(4 * h + q);
-              sts128(ybox + (uint32_t)lane * 128 + ((chunk ^ (uint32_t)(lane & 7)) << 4),
+            for (int q = 0; q < 4; ++q)
+              sts128(sbox + (uint32_t)lane * 64 + (((uint32_t)q ^ ((uint32_t)(lane >> 1) & 3u)) << 4),
                      make_uint4(pack2(v[8 * q], v[8 * q + 1], p.out_f16), pack2(v[8 * q + 2], v[8 * q + 3], p.out_f16),
                                 pack2(v[8 * q + 4], v[8 * q + 5], p.out_f16),
                                 pack2(v[8 * q + 6], v[8 * q + 7], p.out_f16)));
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && rbase < rows_t) {
+              tma_store_3d(tmY, sbox, (int32_t)(ncol + 32 * h), yrow0, yb);
+              bulk_commit();
             }
-          }
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0 && rbase < rows_t) {
-            tma_store_3d(tmY, ybox, (int32_t)ncol, yrow0, yb);
-            bulk_commit();
           }
           continue;
         }
@@ -1193,10 +1156,7 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   } else if (warp < Cfg<MODE, PAIR>::kConvWarp0) {
     uint32_t* stage = reinterpret_cast<uint32_t*>(smem_raw + (sbase - raw) + G::kRingBytes) +
                       (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
-    // TMA-store epilogue: a 4 KB box buffer per warp from the end of the
-    // stages in use (the unused stages and the slices above).
-    const uint32_t ybox = sbase + (uint32_t)p.stages * G::kStageBytes + (uint32_t)(warp - kEpiWarp0) * kYBoxBytes;
-    run_epilogue<MODE, PAIR>(p, &tmZ, tmem, accf0, acce0, abort, stage, ybox);
+    run_epilogue<MODE, PAIR>(p, &tmZ, tmem, accf0, acce0, abort, stage);
     // Every tensor store has read its box before the CTA can exit.
     if (p.y_tma && lane == 0) bulk_wait_all();
   } else if (MODE == kGroupedQ) {
@@ -1425,29 +1385,12 @@ int max_pair_clusters() {
   }
 }
 
-// Ring stages for a launch: all of them, except that a TMA-store epilogue
-// (kDense / kSkinny) gives up whole stages until the box buffers of its
-// storing warps (4 KB each) fit in the freed stages plus the epilogue slices.
-template <int MODE, bool PAIR>
-void choose_stages(TcParams& p) {
-  using G = Geo<MODE, PAIR>;
-  p.stages = G::kStages;
-  if (MODE != kDense && MODE != kSkinny) p.y_tma = 0;
-  if (p.y_tma != 1) return;   // narrow boxes use the staging slices
-  const int need = (G::kTileN / Cfg<MODE, PAIR>::kCols) * 4 * kYBoxBytes;
-  while (p.stages > 2 && (G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) --p.stages;
-  if ((G::kStages - p.stages) * G::kStageBytes + Cfg<MODE, PAIR>::kEpiBytes < need) {
-    p.y_tma = 0;
-    p.stages = G::kStages;
-  }
-}
-
 template <int MODE, bool PAIR>
 mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtensorMap& ms, const CUtensorMap& mz,
                         const TcParams& p_in, int64_t work, cudaStream_t stream) {
   constexpr int kSmem = Cfg<MODE, PAIR>::kSmem, kThreadsM = Cfg<MODE, PAIR>::kThreads;
   TcParams p = p_in;
-  choose_stages<MODE, PAIR>(p);
+  if (MODE != kDense && MODE != kSkinny) p.y_tma = 0;
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MM_ERR_CUDA;
@@ -1560,13 +1503,12 @@ int sm_count_public() { return sm_count(); }
 namespace {
 
 // The 16-bit output Y [batch.., M, N] (row stride y.rs, unit column stride) as
-// a tensor map of 32-row x 64-column boxes, 128-byte swizzled, for the
-// TMA-store epilogue: sets p->y_tma and p->y_bc when Y's layout fits TMA.
+// a tensor map of 32 x 32 boxes, 64-byte swizzled, for the TMA-store
+// epilogue: sets p->y_tma and p->y_bc when Y's layout fits TMA.
 void plan_output(const GemmArgs& g, TcParams* p, OperandPlan* y) {
   p->y_tma = 0;
   if (g.dtype != MM_BF16 && g.dtype != MM_F16) return;
   if (g.y.cs != 1 || g.y.rs < g.N || g.M < 1 || g.N < 1) return;
-  const bool wide = (g.K + BK - 1) / BK <= kYTmaMaxKb;   // wide boxes cost a ring stage
   auto encode = encode_fn();
   if (!encode || (reinterpret_cast<uintptr_t>(g.y.ptr) & 15)) return;
   const int64_t pitch = g.M == 1 ? (g.N + 7) / 8 * 8 : g.y.rs;   // one row: any valid pitch
@@ -1591,15 +1533,15 @@ void plan_output(const GemmArgs& g, TcParams* p, OperandPlan* y) {
   const cuuint64_t strides[2] = {(cuuint64_t)pitch * 2,
                                  unit != 0 ? (cuuint64_t)unit * 2 : (cuuint64_t)((pitch * 2 * g.M + 15) & ~15ll)};
   if (strides[0] >= (1ull << 40) || strides[1] >= (1ull << 40)) return;
-  const cuuint32_t box[3] = {wide ? 64u : 32u, 32u, 1u};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = g.dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (encode(&y->map, dt, 3, const_cast<void*>(g.y.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return;
   y->mn_major = 0;
-  p->y_tma = wide ? 1 : 2;
+  p->y_tma = 1;
   for (int d = 0; d < kMaxBatchDims; ++d) p->y_bc[d] = y->bc[d];
 }
 

@@ -47,13 +47,10 @@ struct TcParams {
   int64_t y_rs;
   int y_vec, out_f16, out_f32;
   // 16-bit dense outputs: y_tma set when the epilogue writes each warp's
-  // 32 x 64 output box with a TMA tensor store (the map is the kernel's fourth
-  // tensor map); y_bc maps a batch index to the map's batch coordinate.
+  // output as 32 x 32 boxes with TMA tensor stores (the map is the kernel's
+  // fourth tensor map); y_bc maps a batch index to the map's batch coordinate.
   int y_tma;
   int64_t y_bc[kMaxBatchDims];
-  // Ring stages in use (at most the mode's compiled count); a TMA-store
-  // epilogue takes the shared memory of the unused stages for its boxes.
-  int stages;
   // float epilogue: v = alpha*acc + beta*C
   float alpha, beta;
   const void* c;

@@ -34,8 +34,9 @@ def test_stream_probe_write_and_copy():
 def test_alu_probe_int32_chains():
     iters = 7
     macs = qg.mm_alu_probe(0, iters)
-    threads = macs // (8 * iters)
-    assert threads > 0 and macs == threads * 8 * iters
+    chains = qg.MM_ALU_CHAINS
+    threads = macs // (chains * iters)
+    assert threads > 0 and macs == threads * chains * iters
     out = torch.zeros(threads, dtype=torch.int64, device=DEV)
     qg.mm_alu_probe(0, iters, out=out)
     torch.cuda.synchronize()
@@ -45,7 +46,7 @@ def test_alu_probe_int32_chains():
     a, c = seed | 1, seed ^ 0x9E3779B9
     tid = np.arange(threads, dtype=np.uint64)
     s = np.zeros(threads, dtype=np.uint64)
-    for j in range(8):
+    for j in range(chains):
         x = (tid + j) & 0xFFFFFFFF
         for _ in range(iters):
             x = (x * a + c) & 0xFFFFFFFF
@@ -57,10 +58,10 @@ def test_alu_probe_int32_chains():
 def test_alu_probe_float_chains_run(op):
     iters = 50
     macs = qg.mm_alu_probe(op, iters)
-    out = torch.zeros(macs // (8 * iters), dtype=torch.float64, device=DEV)
+    out = torch.zeros(macs // (qg.MM_ALU_CHAINS * iters), dtype=torch.float64, device=DEV)
     qg.mm_alu_probe(op, iters, out=out)
     torch.cuda.synchronize()
-    threads = macs // (8 * iters)
+    threads = macs // (qg.MM_ALU_CHAINS * iters)
     vals = out if op == 1 else out.view(torch.float32)[:threads]   # fp32 sums are packed
     assert torch.isfinite(vals).all() and (vals != 0).any()
     with pytest.raises(qg.MMError):
