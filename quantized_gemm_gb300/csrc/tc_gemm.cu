@@ -46,9 +46,12 @@
 //   kGroupedQ GroupedMatMul with int8/uint8 weights: converter warps form
 //             T((q - zp) * scale) in shared memory (CTA pairs).
 //   kTF32     fp32 MatMul / Gemm as three tf32 products of split operands.
-//   kSkinny   kDense for at most 64 rows against a wide B': 64-column tiles,
-//             64-row A boxes and a 12-stage ring of 16 KB, so that many CTAs
-//             stream B' with many bytes in flight.
+//   kSkinny   kDense for at most 64 rows of A': 256-column tiles whose
+//             k-blocks are split over the CTAs of a cluster (non-persistent,
+//             one tile per cluster), so that B' streams through every SM with
+//             few, wide MMAs; each CTA leaves its partial sums in its shared
+//             memory and the cluster's first CTA adds them in a fixed order
+//             through distributed shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -75,9 +78,9 @@ constexpr int kEpiWarp0 = 2;                     // warps 2.. run the epilogue
 // 6 stages.
 template <int MODE, bool PAIR>
 struct Geo {
-  // kSkinny: 64-column tiles with 64-row A boxes; the M = 128 MMA's rows
-  // 64..127 read the stage's B bytes and are never stored.
-  static constexpr int kTileN = MODE == kSkinny ? 64 : BN;
+  // kSkinny: 64-row A boxes; the M = 128 MMA's rows 64..127 read the
+  // stage's B bytes and are never stored.
+  static constexpr int kTileN = BN;
   static constexpr int kBRows = PAIR ? BN / 2 : kTileN;  // B columns (rows of B') held by one CTA
   static constexpr int kABytes = (MODE == kSkinny ? BM / 2 : BM) * BK * 2;   // rows x 128 bytes
   static constexpr int kBBytes = kBRows * BK * 2;
@@ -87,7 +90,7 @@ struct Geo {
   static constexpr int kStageBytes = (kABytes + kBBytes) * (MODE == kTF32 ? 2 : 1);
   // kGroupedQ gives one stage's worth of shared memory to its int8 staging ring.
   static constexpr int kStages =
-      MODE == kTF32 ? (PAIR ? 3 : 2) : PAIR ? (MODE == kGroupedQ ? 5 : 6) : MODE == kSkinny ? 12 : 4;
+      MODE == kTF32 ? (PAIR ? 3 : 2) : PAIR ? (MODE == kGroupedQ ? 5 : 6) : MODE == kSkinny ? 5 : 4;
   static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // output rows per (pair) tile
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
@@ -126,7 +129,7 @@ struct Cfg {
   static constexpr int kConvWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps + kConv) * 32;
   static constexpr int kCols = kTileN / (kEpiWarps / 4);      // columns per epilogue warp
-  static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : MODE == kTF32 ? 0 : kStageWords;
+  static constexpr int kWarpWords = MODE == kQLinear ? 3 * kCols : (MODE == kTF32 || MODE == kSkinny) ? 0 : kStageWords;
   static constexpr int kEpiBytes = kEpiWarps * kWarpWords * 4;
   // kGroupedQ staging ring, after the epilogue's slices (1024-byte aligned)
   static constexpr int kQOff = (Geo<MODE, PAIR>::kRingBytes + kCtrlBytes + kEpiBytes + 1023) / 1024 * 1024;
@@ -217,10 +220,28 @@ __device__ __forceinline__ int64_t total_tiles(const TcParams& p) {
 }
 
 // The persistent schedule: a CTA (or CTA pair) takes tiles first, first + step, ...
-template <bool PAIR>
-__device__ __forceinline__ int64_t first_tile() { return PAIR ? (blockIdx.x >> 1) : blockIdx.x; }
-template <bool PAIR>
-__device__ __forceinline__ int64_t tile_step() { return PAIR ? (gridDim.x >> 1) : gridDim.x; }
+// kSkinny is not persistent: cluster c of p.split CTAs computes tile c.
+template <int MODE, bool PAIR>
+__device__ __forceinline__ int64_t first_tile(const TcParams& p) {
+  return MODE == kSkinny ? (int64_t)(blockIdx.x / (unsigned)p.split) : PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+}
+template <int MODE, bool PAIR>
+__device__ __forceinline__ int64_t tile_step(const TcParams& p) {
+  return MODE == kSkinny ? (int64_t)(gridDim.x / (unsigned)p.split) : PAIR ? (gridDim.x >> 1) : gridDim.x;
+}
+// The k-blocks this CTA multiplies: all of them, or (kSkinny) its share of
+// the tile's, k-blocks [r*num_kb/split, (r+1)*num_kb/split) for cluster rank r.
+template <int MODE>
+__device__ __forceinline__ void kb_range(const TcParams& p, int& b, int& e) {
+  if (MODE == kSkinny) {
+    const int r = (int)(blockIdx.x % (unsigned)p.split);
+    b = (int)((int64_t)r * p.num_kb / p.split);
+    e = (int)((int64_t)(r + 1) * p.num_kb / p.split);
+  } else {
+    b = 0;
+    e = p.num_kb;
+  }
+}
 
 // ------------------------------------------------------------------ producer
 
@@ -247,8 +268,10 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
   uint32_t qstage = 0, qphase = 0, qpending = 0, qpend_parity = 0;   // the same for the staging ring
   Tile ti;
   int gh = 0;
-  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
-    for (int kb = 0; kb < p.num_kb; ++kb) {
+  int kb_b, kb_e;
+  kb_range<MODE>(p, kb_b, kb_e);
+  for (int64_t t = first_tile<MODE, PAIR>(p); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<MODE, PAIR>(p)) {
+    for (int kb = kb_b; kb < kb_e; ++kb) {
       if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.status, p.timeout_ns)) goto done;
       const uint32_t full = full0 + 8 * stage;
       const uint32_t sa = sbase + stage * G::kStageBytes, sb = sa + G::kABytes;
@@ -365,15 +388,17 @@ __device__ void run_mma(const TcParams& p, uint32_t sbase, uint32_t tmem, uint32
   uint32_t stage = 0, phase = 0, seg = 0;
   Tile ti;
   int gh = 0;
-  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
-    for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_seg) {
+  int kb_b, kb_e;
+  kb_range<MODE>(p, kb_b, kb_e);
+  for (int64_t t = first_tile<MODE, PAIR>(p); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<MODE, PAIR>(p)) {
+    for (int kb0 = kb_b; kb0 < kb_e; kb0 += p.kb_per_seg) {
       const uint32_t buf = seg & 1, aph = (seg >> 1) & 1;
       const bool ok = PAIR ? mbar_wait_cluster(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns)
                            : mbar_wait(acce0 + 8 * buf, aph ^ 1, abort, p.status, p.timeout_ns);
       if (!ok) goto done;
       tc_fence_after();
       const uint32_t d = tmem + buf * BN;
-      const int kb1 = min(kb0 + p.kb_per_seg, p.num_kb);
+      const int kb1 = min(kb0 + p.kb_per_seg, kb_e);
       const uint32_t idesc = (PAIR && p.pair_tail && ti.rows <= BM) ? p.idesc_tail : p.idesc;
       for (int kb = kb0; kb < kb1; ++kb) {
         const bool got = PAIR ? mbar_wait_cluster(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns)
@@ -540,7 +565,7 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
   uint32_t stage = 0, qstage = 0, qphase = 0;
   Tile ti;
   int gh = 0;
-  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+  for (int64_t t = first_tile<MODE, PAIR>(p); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<MODE, PAIR>(p)) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (!__all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qstage, qphase, abort, p.status, p.timeout_ns))) return;
       const uint8_t* qs = smem + (qbase - sm0) + qstage * kQStageBytes;
@@ -749,7 +774,7 @@ __device__ void run_split(const TcParams& p, uint8_t* smem, uint32_t sbase, uint
   uint32_t stage = 0, phase = 0;
   Tile ti;
   int gh = 0;
-  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+  for (int64_t t = first_tile<MODE, PAIR>(p); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<MODE, PAIR>(p)) {
     for (int kb = 0; kb < p.num_kb; ++kb) {
       // One decision for all converter warps (they meet at named barriers).
       const bool ok = __all_sync(0xffffffffu, mbar_wait(ld0 + 8 * stage, phase, abort, p.status, p.timeout_ns));
@@ -816,7 +841,7 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
     qmax = p.y_signed ? 127.f : 255.f;
   }
   int gh = 0;
-  for (int64_t t = first_tile<PAIR>(); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<PAIR>()) {
+  for (int64_t t = first_tile<MODE, PAIR>(p); get_tile<MODE, PAIR>(p, t, total, ti, gh); t += tile_step<MODE, PAIR>(p)) {
     const int rows_cta = PAIR ? max(0, min(BM, ti.rows - (int)row_off)) : ti.rows;
     const bool row_ok = rloc < rows_cta;
     const int64_t ncol0 = ti.n0 + slice * kCols;
@@ -1081,6 +1106,84 @@ __device__ void run_epilogue(const TcParams& p, const CUtensorMap* tmY, uint32_t
   }
 }
 
+// ------------------------------------------------------------------ few-row epilogue (kSkinny)
+
+// Each CTA of a cluster has accumulated its share of the tile's k-blocks in
+// TMEM columns 0..255; rows 0..63 (lanes of quadrants 0 and 1) hold the A'
+// rows.  The epilogue warps of those quadrants copy them, fp32, into the
+// CTA's own shared memory (the drained ring) as [64 rows][kSkinnyPitch]
+// (a padded pitch, so the row-wise 16-byte writes of a warp are conflict-free).
+constexpr int kSkinnyPitch = BN + 4;   // floats per partial-sum row
+
+template <int MODE, bool PAIR>
+__device__ void run_skinny_partial(const TcParams& p, uint32_t tmem, uint32_t accf0, volatile int* abort,
+                                   uint32_t part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3, slice = (warp - kEpiWarp0) >> 2;
+  if (quad >= 2) return;
+  if (!__all_sync(0xffffffffu, mbar_wait(accf0, 0, abort, p.status, p.timeout_ns))) return;
+  tc_fence_after();
+  const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slice * 64);
+  uint32_t r[2][32];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) tmem_ld32(taddr + c * 32, r[c]);
+  tmem_ld_wait();
+  const uint32_t row = part + (uint32_t)((quad * 32 + lane) * kSkinnyPitch * 4) + (uint32_t)(slice * 64 * 4);
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    sts128(row + q * 16, make_uint4(r[q >> 3][4 * (q & 7)], r[q >> 3][4 * (q & 7) + 1], r[q >> 3][4 * (q & 7) + 2],
+                                    r[q >> 3][4 * (q & 7) + 3]));
+}
+
+// The cluster's first CTA, once every CTA's partial sums are in its shared
+// memory: epilogue thread t takes row t / 8 and columns 32 * (t % 8) .. +31
+// of the tile, adds the p.split partials in rank order (reading the other
+// CTAs' through distributed shared memory), applies alpha, beta * C and the
+// rounding to 16 bits, and stores the row piece.
+template <int MODE, bool PAIR>
+__device__ void run_skinny_reduce(const TcParams& p, uint32_t part) {
+  const int et = (int)threadIdx.x - kEpiWarp0 * 32;
+  const int row = et >> 3, cc = et & 7;
+  const int64_t total = total_tiles<MODE>(p);
+  Tile ti;
+  int gh = 0;
+  if (!get_tile<MODE, PAIR>(p, first_tile<MODE, PAIR>(p), total, ti, gh)) return;
+  if (row >= ti.rows) return;
+  const uint32_t src = part + (uint32_t)(row * kSkinnyPitch * 4) + (uint32_t)(cc * 32 * 4);
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  for (int rk = 0; rk < p.split; ++rk) {
+    const uint32_t a = mapa_shared(src, (uint32_t)rk);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = lds128_cluster(a + q * 16);
+      v[4 * q] += f.x;
+      v[4 * q + 1] += f.y;
+      v[4 * q + 2] += f.z;
+      v[4 * q + 3] += f.w;
+    }
+  }
+  const int64_t m = ti.m0 + row, n = ti.n0 + cc * 32;
+  if (n >= p.N) return;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
+  if (p.c) add_c32(p, static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs, n, v);
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1], p.out_f16);
+  uint16_t* yrow = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
+  if (p.y_vec && n + 32 <= p.N) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(yrow + n + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int MODE, bool PAIR>
@@ -1156,7 +1259,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   } else if (warp < Cfg<MODE, PAIR>::kConvWarp0) {
     uint32_t* stage = reinterpret_cast<uint32_t*>(smem_raw + (sbase - raw) + G::kRingBytes) +
                       (warp - kEpiWarp0) * Cfg<MODE, PAIR>::kWarpWords;
-    run_epilogue<MODE, PAIR>(p, &tmZ, tmem, accf0, acce0, abort, stage);
+    if constexpr (MODE == kSkinny) run_skinny_partial<MODE, PAIR>(p, tmem, accf0, abort, sbase);
+    else run_epilogue<MODE, PAIR>(p, &tmZ, tmem, accf0, acce0, abort, stage);
     // Every tensor store has read its box before the CTA can exit.
     if (p.y_tma && lane == 0) bulk_wait_all();
   } else if (MODE == kGroupedQ) {
@@ -1166,6 +1270,14 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (MODE == kSkinny) {
+    // Every CTA's partial sums are in its shared memory; the first CTA of the
+    // cluster adds them, and the others keep their shared memory until it
+    // has read them.
+    cluster_sync();
+    if (cluster_ctarank() == 0 && warp >= kEpiWarp0) run_skinny_reduce<MODE, PAIR>(p, sbase);
+    cluster_sync();
+  }
   // Neither CTA of a pair may leave (or free tensor memory) while the other
   // can still signal its barriers or its MMAs can still touch its memory.
   if (PAIR) cluster_sync();
@@ -1390,11 +1502,35 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtens
                         const TcParams& p_in, int64_t work, cudaStream_t stream) {
   constexpr int kSmem = Cfg<MODE, PAIR>::kSmem, kThreadsM = Cfg<MODE, PAIR>::kThreads;
   TcParams p = p_in;
-  if (MODE != kDense && MODE != kSkinny) p.y_tma = 0;
+  if (MODE != kDense) p.y_tma = 0;
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MM_ERR_CUDA;
-  if constexpr (!PAIR) {
+  if constexpr (MODE == kSkinny) {
+    // One cluster per 256-column tile; its CTAs split the tile's k-blocks:
+    // the largest power of two up to 8 that keeps tiles x split within the
+    // SMs and gives every CTA at least one k-block.
+    const int sms = sm_count();
+    int split = 8;
+    while (split > 1 && (work * split > sms || split > p.num_kb)) split >>= 1;
+    p.split = split;
+    if (work * split > 0x7fffffffLL) return MM_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(work * split));
+    cfg.blockDim = dim3(kThreadsM);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, ms, mz, p) == cudaSuccess
+               ? MM_OK
+               : MM_ERR_CUDA;
+  } else if constexpr (!PAIR) {
     const int sms = sm_count();
     const int grid = (int)(work < sms ? (work > 0 ? work : 1) : sms);
     tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, ms, mz, p);
@@ -1435,7 +1571,7 @@ mm_status launch_tc(int mode, bool pair, const OperandPlan& a, const OperandPlan
   int64_t work = 0;
   if (!is_grouped(mode)) {
     const int64_t rows = pair ? 2 * BM : BM;
-    const int64_t cols = mode == kSkinny ? 64 : BN;
+    const int64_t cols = BN;
     p.mt = (p.M + rows - 1) / rows;
     p.nt = (p.N + cols - 1) / cols;
     p.tiles = p.mt * p.nt * p.bm.count;
@@ -1592,21 +1728,18 @@ mm_status launch_tc_gemm(const GemmArgs& g, unsigned* status, cudaStream_t strea
     for (int d = 0; d < g.bm.nb; ++d) p.c_vec = p.c_vec && (g.c.bstride[d] % vec == 0);
   }
   p.status = status;
-  // A few rows (at most 64, K-major A) against a wide B' with fewer whole
-  // tiles than half the SMs: the skinny configuration streams B' with 64-
-  // column tiles and a deep ring.
-  if (!p.out_f32 && g.M <= BM / 2 &&
-      ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * g.bm.count * 2 <= sm_count()) {
+  // A few rows (at most 64, K-major A) against fewer 256-column tiles than
+  // SMs: the few-row configuration splits each tile's k-blocks over a cluster
+  // so that every SM streams B'.
+  if (!p.out_f32 && g.M <= BM / 2 && ((g.N + BN - 1) / BN) * g.bm.count < sm_count()) {
     OperandPlan a, b;
     const int64_t vec = 8;
     const int64_t a_rs = (g.M == 1 && g.a.cs == 1) ? (g.K + vec - 1) / vec * vec : g.a.rs;
     if (g.N >= 2 && g.y.cs == 1 &&
         plan_operand(g.a.ptr, g.dtype, g.M, g.K, a_rs, g.a.cs, g.bm, g.a.bstride, BM / 2, &a) && !a.mn_major &&
-        plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, 64, &b)) {
-      p.idesc = make_idesc_mn(p.out_f16, 0, b.mn_major, BM, 64);
-      OperandPlan ymap;
-      plan_output(g, &p, &ymap);
-      return launch_tc(kSkinny, false, a, b, p, stream, nullptr, p.y_tma ? &ymap : nullptr);
+        plan_operand(g.b.ptr, g.dtype, g.N, g.K, g.b.cs, g.b.rs, g.bm, g.b.bstride, BN, &b)) {
+      p.idesc = make_idesc_mn(p.out_f16, 0, b.mn_major, BM, BN);
+      return launch_tc(kSkinny, false, a, b, p, stream);
     }
   }
   // CTA pairs (256-row tiles) for long-K products with more than one row tile;

@@ -35,6 +35,7 @@ struct TcParams {
   int64_t a_bc[kMaxBatchDims], b_bc[kMaxBatchDims];   // batch index -> TMA batch coordinate
   int a_mn, b_mn;                              // operand is MN-major in shared memory
   int num_kb, kb_per_seg;                      // k-blocks; k-blocks per accumulation segment
+  int split;                                   // kSkinny: CTAs of a cluster that split one tile's k-blocks
   uint32_t idesc;                              // tcgen05 instruction descriptor
   // CTA pairs: a pair tile with at most 128 valid rows (the last row tile of
   // a group, or of a dense product) runs as one M = 128 cta_group::2 MMA

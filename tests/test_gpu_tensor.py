@@ -499,3 +499,36 @@ def test_grouped_tensor_invalid_indices():
     assert _grouped(x, w, gi, None)
     assert qg.mm_get_device_status() == "MM_ERR_INDEX_RANGE"
     assert qg.mm_get_device_status() == "MM_OK"
+
+
+# The few-row tensor-core configuration (at most 64 rows of A', fewer
+# 256-column tiles than SMs): each tile's k-blocks are split over a cluster of
+# up to 8 CTAs and the partial sums added through distributed shared memory.
+# Splits of 1, 2, 4 and 8 (K of 64, 128, 1000 and 8192; N from one ragged tile
+# to 32 tiles), both layouts of B', C absent, a row vector or full, and a
+# batched MatMul whose B is broadcast.
+@pytest.mark.parametrize("M,N,K", [(5, 200, 64), (16, 1000, 128), (33, 8192, 1000), (64, 520, 8192),
+                                   (17, 8200, 4104)])
+@pytest.mark.parametrize("tB", [0, 1])
+@pytest.mark.parametrize("c_kind", [None, "row", "full"])
+def test_gemm_tensor_few_rows_split_k(M, N, K, tB, c_kind):
+    A = rand_tensor((M, K), torch.bfloat16, 131, DEV)
+    B = rand_tensor((N, K) if tB else (K, N), torch.bfloat16, 132, DEV)
+    C = None if c_kind is None else rand_tensor((1, N) if c_kind == "row" else (M, N), torch.bfloat16, 133, DEV)
+    with tensor_path():
+        Y = qg.mm_gemm(A, B, C, 0.75, 1.5, 0, tB)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    c = None if C is None else to_np(C)
+    kw = dict(alpha=0.75, beta=1.5, transB=tB)
+    assert max_rel_err(to_np(Y), oracle.gemm(a, b, c, **kw), oracle.gemm_abs_scale(a, b, c, **kw)) <= TOL[torch.bfloat16]
+
+
+def test_matmul_tensor_few_rows_batched_f16():
+    A = rand_tensor((2, 3, 24, 640), torch.float16, 134, DEV)
+    B = rand_tensor((640, 1304), torch.float16, 135, DEV)   # row pitch a multiple of 16 bytes
+    with tensor_path():
+        Y = qg.mm_matmul(A, B)
+    ran_on_tensor_cores()
+    a, b = to_np(A), to_np(B)
+    assert max_rel_err(to_np(Y), oracle.matmul(a, b), oracle.matmul_abs_scale(a, b)) <= TOL[torch.float16]
