@@ -50,8 +50,9 @@
 //             k-blocks are split over the CTAs of a cluster (non-persistent,
 //             one tile per cluster), so that B' streams through every SM with
 //             few, wide MMAs; each CTA leaves its partial sums in its shared
-//             memory and the cluster's first CTA adds them in a fixed order
-//             through distributed shared memory.
+//             memory and each CTA adds the cluster's partials for its share
+//             of the columns, in a fixed order, through distributed shared
+//             memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -1135,52 +1136,55 @@ __device__ void run_skinny_partial(const TcParams& p, uint32_t tmem, uint32_t ac
                                     r[q >> 3][4 * (q & 7) + 3]));
 }
 
-// The cluster's first CTA, once every CTA's partial sums are in its shared
-// memory: epilogue thread t takes row t / 8 and columns 32 * (t % 8) .. +31
-// of the tile, adds the p.split partials in rank order (reading the other
-// CTAs' through distributed shared memory), applies alpha, beta * C and the
-// rounding to 16 bits, and stores the row piece.
+// Once every CTA's partial sums are in its shared memory, CTA r of the cluster
+// finishes columns [r * 256 / split, (r + 1) * 256 / split) of the tile: each
+// item is one row and 8 columns; its epilogue threads add the split partials
+// in rank order (the other CTAs' through distributed shared memory), apply
+// alpha, beta * C and the rounding to 16 bits, and store 16 bytes.
 template <int MODE, bool PAIR>
 __device__ void run_skinny_reduce(const TcParams& p, uint32_t part) {
+  constexpr int kThr = Cfg<MODE, PAIR>::kEpiWarps * 32;
   const int et = (int)threadIdx.x - kEpiWarp0 * 32;
-  const int row = et >> 3, cc = et & 7;
   const int64_t total = total_tiles<MODE>(p);
   Tile ti;
   int gh = 0;
   if (!get_tile<MODE, PAIR>(p, first_tile<MODE, PAIR>(p), total, ti, gh)) return;
-  if (row >= ti.rows) return;
-  const uint32_t src = part + (uint32_t)(row * kSkinnyPitch * 4) + (uint32_t)(cc * 32 * 4);
-  float v[32];
+  const int rank = (int)(cluster_ctarank());
+  const int width = BN / p.split, groups = width / 8;
+  const uint16_t* cbase =
+      p.c ? static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) : nullptr;
+  uint16_t* ybase = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch);
+  for (int item = et; item < ti.rows * groups; item += kThr) {
+    const int row = item / groups;
+    const int col = rank * width + (item - row * groups) * 8;   // within the tile
+    const int64_t m = ti.m0 + row, n = ti.n0 + col;
+    if (n >= p.N) continue;
+    const uint32_t src = part + (uint32_t)(row * kSkinnyPitch * 4) + (uint32_t)(col * 4);
+    float v[8];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = 0.f;
-  for (int rk = 0; rk < p.split; ++rk) {
-    const uint32_t a = mapa_shared(src, (uint32_t)rk);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 f = lds128_cluster(a + q * 16);
-      v[4 * q] += f.x;
-      v[4 * q + 1] += f.y;
-      v[4 * q + 2] += f.z;
-      v[4 * q + 3] += f.w;
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    for (int rk = 0; rk < p.split; ++rk) {
+      const uint32_t a = mapa_shared(src, (uint32_t)rk);
+      const float4 f0 = lds128_cluster(a), f1 = lds128_cluster(a + 16);
+      v[0] += f0.x; v[1] += f0.y; v[2] += f0.z; v[3] += f0.w;
+      v[4] += f1.x; v[5] += f1.y; v[6] += f1.z; v[7] += f1.w;
     }
-  }
-  const int64_t m = ti.m0 + row, n = ti.n0 + cc * 32;
-  if (n >= p.N) return;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
-  if (p.c) add_c32(p, static_cast<const uint16_t*>(p.c) + batch_off(p, p.c_bstride, ti.batch) + m * p.c_rs, n, v);
-  uint32_t w[16];
+    for (int j = 0; j < 8; ++j) {
+      v[j] = p.alpha * v[j];
+      if (cbase && n + j < p.N) v[j] = __fmaf_rn(p.beta, unpack16(cbase[m * p.c_rs + (n + j) * p.c_cs], p.out_f16), v[j]);
+    }
+    uint16_t* yrow = ybase + m * p.y_rs;
+    const uint4 w = make_uint4(pack2(v[0], v[1], p.out_f16), pack2(v[2], v[3], p.out_f16),
+                               pack2(v[4], v[5], p.out_f16), pack2(v[6], v[7], p.out_f16));
+    if (p.y_vec && n + 8 <= p.N) {
+      *reinterpret_cast<uint4*>(yrow + n) = w;
+    } else {
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int j = 0; j < 16; ++j) w[j] = pack2(v[2 * j], v[2 * j + 1], p.out_f16);
-  uint16_t* yrow = static_cast<uint16_t*>(p.y) + batch_off(p, p.y_bstride, ti.batch) + m * p.y_rs;
-  if (p.y_vec && n + 32 <= p.N) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<uint4*>(yrow + n + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+      for (int j = 0; j < 8; ++j)
+        if (n + j < p.N) yrow[n + j] = (uint16_t)((j & 1) ? (ws[j >> 1] >> 16) : (ws[j >> 1] & 0xFFFFu));
+    }
   }
 }
 
@@ -1271,11 +1275,11 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if constexpr (MODE == kSkinny) {
-    // Every CTA's partial sums are in its shared memory; the first CTA of the
-    // cluster adds them, and the others keep their shared memory until it
-    // has read them.
+    // Every CTA's partial sums are in its shared memory; each CTA adds the
+    // cluster's partials for its share of the columns, and no CTA leaves
+    // (taking its shared memory with it) until all have read them.
     cluster_sync();
-    if (cluster_ctarank() == 0 && warp >= kEpiWarp0) run_skinny_reduce<MODE, PAIR>(p, sbase);
+    if (warp >= kEpiWarp0) run_skinny_reduce<MODE, PAIR>(p, sbase);
     cluster_sync();
   }
   // Neither CTA of a pair may leave (or free tensor memory) while the other
