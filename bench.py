@@ -736,17 +736,17 @@ PER_CONFIG = (
                                                  "frac_of_write_peak", "cpu_baseline")),
     ("4_qlinear_s8", "qlinear_s8", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
     ("5_grouped_bf16", "grouped_bf16", ("value", "unit", "ms_per_call", "frac", "cpu_baseline")),
-    ("f1_qlinear_u8", "qlinear_u8", ("value", "ms_per_call", "frac")),
-    ("f1_qlinear_u8s8_f16scales", "qlinear_u8s8_f16scales", ("value", "ms_per_call", "frac")),
-    ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "ms_per_call", "frac")),
-    ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "ms_per_call", "frac")),
-    ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "ms_per_call", "frac")),
-    ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "ms_per_call", "frac")),
+    ("f1_qlinear_u8", "qlinear_u8", ("value", "frac")),
+    ("f1_qlinear_u8s8_f16scales", "qlinear_u8s8_f16scales", ("value", "frac")),
+    ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "frac")),
+    ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "frac")),
+    ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "frac")),
+    ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "frac")),
     ("f4_gemm_f32", "gemm_f32", ("value", "ms_per_call", "frac")),
     ("a3_skinny_m16", "gemm_bf16_skinny_m16", ("value", "unit", "us_per_call_in_graph", "frac")),
     ("a3_skinny_m64", "gemm_bf16_skinny_m64", ("value", "us_per_call_in_graph", "frac")),
-    ("a13_gemm_f64_simt", "gemm_f64_simt", ("value", "ms_per_call", "frac", "peak")),
-    ("a13_gemm_i32_simt", "gemm_i32_simt", ("value", "ms_per_call", "frac", "peak")),
+    ("a13_gemm_f64_simt", "gemm_f64_simt", ("value", "frac", "peak")),
+    ("a13_gemm_i32_simt", "gemm_i32_simt", ("value", "frac", "peak")),
 )
 
 
@@ -819,7 +819,7 @@ def run_ours(args, rank, world, local):
         "per_config": per_config,
         "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic, seeded (workloads.py)",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic, seeded",
         "config": {"workload": "gemm_bf16", "M": M, "N": N, "K": K, "transB": 1, "alpha": 0.5,
                    "beta": 2.0, "C": [1, N], "parallelism": "replicas x%d" % world, "l2": "A+B 256 MiB > L2"},
         "roofline": {"bound": "tensor", "achieved": _r(tflops_rank), "peak": peak, "unit": "TFLOP/s",
