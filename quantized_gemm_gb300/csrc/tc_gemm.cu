@@ -180,7 +180,13 @@ __device__ __forceinline__ bool get_tile(const TcParams& p, int64_t t, int64_t t
     const uint32_t local = (uint32_t)(t - __ldg(p.g_tile_start + g));
     const int cnt = __ldg(p.g_count + g);
     const uint32_t mtg = (uint32_t)((cnt + TR - 1) / TR);
-    const uint32_t ntile = local / mtg, mtile = local - ntile * mtg;
+    // Within a group, bands of up to kGroupM row tiles, each band's column
+    // tiles in turn: the band's rows of A stay in L2 while its column tiles
+    // stream the group's weights (8 groups: 2.32 -> 2.22 ms; 64: unchanged).
+    const uint32_t ntot = (uint32_t)p.nt;
+    const uint32_t band = local / (kGroupM * ntot), w = local - band * (kGroupM * ntot);
+    const uint32_t h = min((uint32_t)kGroupM, mtg - band * kGroupM);
+    const uint32_t ntile = w / h, mtile = band * kGroupM + (w - ntile * h);
     ti.batch = 0;
     ti.g = g;
     ti.m0 = (int64_t)mtile * TR;
