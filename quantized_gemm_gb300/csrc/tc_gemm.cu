@@ -1256,6 +1256,10 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched with programmatic stream serialization, this grid may start while
+  // the previous kernel on the stream is finishing: the set-up above overlaps
+  // its tail, and nothing below touches global memory before it completes.
+  griddep_wait();
   const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
 
   if (warp == 0) {
@@ -1516,6 +1520,21 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtens
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MM_ERR_CUDA;
+  // Every launch allows programmatic stream serialization: the kernel's
+  // set-up (barriers, tensor memory, descriptor prefetch) may overlap the
+  // previous kernel's last blocks; it waits for that kernel before any
+  // global-memory access.  Clustered launches add the cluster size.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreadsM);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
   if constexpr (MODE == kSkinny) {
     // One cluster per 256-column tile; its CTAs split the tile's k-blocks:
     // the largest power of two up to 8 that keeps tiles x split within the
@@ -1525,48 +1544,25 @@ mm_status launch_kernel(const OperandPlan& a, const OperandPlan& b, const CUtens
     while (split > 1 && (work * split > sms || split > p.num_kb)) split >>= 1;
     p.split = split;
     if (work * split > 0x7fffffffLL) return MM_ERR_UNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[1].val.clusterDim.x = (unsigned)split;
     cfg.gridDim = dim3((unsigned)(work * split));
-    cfg.blockDim = dim3(kThreadsM);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, ms, mz, p) == cudaSuccess
-               ? MM_OK
-               : MM_ERR_CUDA;
+    cfg.numAttrs = 2;
   } else if constexpr (!PAIR) {
     const int sms = sm_count();
-    const int grid = (int)(work < sms ? (work > 0 ? work : 1) : sms);
-    tc_gemm_kernel<MODE, PAIR><<<grid, kThreadsM, kSmem, stream>>>(a.map, b.map, ms, mz, p);
-    return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+    cfg.gridDim = dim3((unsigned)(work < sms ? (work > 0 ? work : 1) : sms));
+    cfg.numAttrs = 1;
   } else {
     // One persistent pair per resident cluster slot: a pair that could not be
     // resident would only start after the others finish.
     const int slots = max_pair_clusters<MODE>();
     if (slots <= 0) return MM_ERR_UNSUPPORTED;
     const int clusters = (int)(work < slots ? (work > 0 ? work : 1) : slots);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[1].val.clusterDim.x = 2;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
-    cfg.blockDim = dim3(kThreadsM);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, ms, mz, p) == cudaSuccess
-               ? MM_OK
-               : MM_ERR_CUDA;
+    cfg.numAttrs = 2;
   }
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE, PAIR>, a.map, b.map, ms, mz, p) == cudaSuccess ? MM_OK
+                                                                                                      : MM_ERR_CUDA;
 }
 
 }  // namespace
