@@ -89,4 +89,38 @@ __device__ __forceinline__ float requant_f32(int32_t acc, float sa, float sb, fl
   return fminf(fmaxf(t, qmin), qmax);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization (launch_pdl) and calls pdl_wait()
+// before its first access to global memory: it waits there until the kernels
+// it depends on on its stream have completed and their memory is visible, so
+// that its launch and set-up overlap the end of the previous kernel.
+// pdl_trigger() lets the next kernel on the stream be launched before this
+// one ends (otherwise that happens as this grid completes).  Short SIMT
+// kernels and the large dense tensor-core products trigger right after their
+// wait; the operand preparation kernels and the few-row, QLinear and grouped
+// products do not, since the next kernel's blocks, resident early, measured
+// slower there.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_wait();
+  pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace qg

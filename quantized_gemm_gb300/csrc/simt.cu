@@ -262,6 +262,7 @@ __device__ __forceinline__ void lds_vec(const Acc* src, Acc (&dst)[RM]) {
 template <typename T, int TM, int TN>
 __global__ void __launch_bounds__(kThreads, TM == 8 ? 1 : 2)
     simt_gemm_kernel(const GemmArgs p, SimtOperand opa, SimtOperand opb) {
+  pdl_begin();
   using Acc = typename Arith<T>::acc;
   constexpr int RM = (16 / (int)sizeof(Acc)) < TM ? 16 / (int)sizeof(Acc) : TM;   // rows per band
   constexpr int RN = (16 / (int)sizeof(Acc)) < TN ? 16 / (int)sizeof(Acc) : TN;
@@ -444,6 +445,7 @@ template <> __device__ __forceinline__ float dot16<float>(float acc, uint4 a, ui
 template <typename T, int MT>
 __global__ void __launch_bounds__(kVecWarps * 32) vec_gemm_kernel(const GemmArgs p, int64_t groups, int64_t tasks,
                                                                   int64_t warps) {
+  pdl_begin();
   constexpr int kVecCols = VecShape<MT>::cols;
   constexpr int U = VecShape<MT>::steps;
   constexpr int kPiece = 16 / (int)sizeof(T);   // values of k in a 16-byte piece
@@ -558,6 +560,7 @@ constexpr int kMnRounds = 8;   // rows of B' per warp in flight
 template <typename T, int MT>
 __global__ void __cluster_dims__(kMnSplit, 1, 1) __launch_bounds__(kMnWarps * 32)
     vec_mn_kernel(const GemmArgs p) {
+  pdl_begin();
   constexpr int kPiece = 16 / (int)sizeof(T);
   constexpr int kSpan = 32 * kPiece;   // columns of a cluster
   __shared__ __align__(16) float part[kMnWarps][MT][kSpan];
@@ -669,7 +672,7 @@ mm_status launch_vec(const GemmArgs& p, cudaStream_t stream) {
   const int64_t rounds = (tasks + wmax - 1) / wmax;
   const int64_t warps = (tasks + rounds - 1) / rounds;   // every warp runs rounds or rounds - 1 groups
   const int64_t blocks = (warps + kVecWarps - 1) / kVecWarps;
-  vec_gemm_kernel<T, MT><<<(unsigned)blocks, kVecWarps * 32, 0, stream>>>(p, groups, tasks, warps);
+  launch_pdl(vec_gemm_kernel<T, MT>, dim3((unsigned)blocks), dim3(kVecWarps * 32), 0, stream, p, groups, tasks, warps);
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
@@ -678,7 +681,7 @@ mm_status launch_vec_mn(const GemmArgs& p, cudaStream_t stream) {
   constexpr int kSpan = 32 * (16 / (int)sizeof(T));
   const int64_t spans = (p.N + kSpan - 1) / kSpan;
   const unsigned gz = (unsigned)(p.bm.count < 65535 ? p.bm.count : 65535);
-  vec_mn_kernel<T, MT><<<dim3(kMnSplit, (unsigned)spans, gz), kMnWarps * 32, 0, stream>>>(p);
+  launch_pdl(vec_mn_kernel<T, MT>, dim3(kMnSplit, (unsigned)spans, gz), dim3(kMnWarps * 32), 0, stream, p);
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
@@ -728,6 +731,7 @@ __device__ __forceinline__ float load_scale(const void* base, int64_t off, int i
 }
 
 __global__ void __launch_bounds__(kThreads) simt_qlinear_kernel(const QLinearArgs p) {
+  pdl_begin();
   __shared__ int As[kTk][kTile + 1];
   __shared__ int Bs[kTk][kTile + 1];
   const int tid = threadIdx.x;
@@ -827,6 +831,7 @@ __device__ __forceinline__ typename Arith<T>::acc dequant_weight(const GroupedAr
 
 template <typename T, bool QW>
 __global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArgs p, unsigned* status) {
+  pdl_begin();
   using Acc = typename Arith<T>::acc;
   constexpr int kChunk = 1024;
   __shared__ Acc xs[kChunk];
@@ -870,8 +875,8 @@ __global__ void __launch_bounds__(kThreads) simt_grouped_kernel(const GroupedArg
 
 template <typename T>
 void launch_grouped(const GroupedArgs& p, unsigned* status, dim3 grid, cudaStream_t stream) {
-  if (p.wq) simt_grouped_kernel<T, true><<<grid, kThreads, 0, stream>>>(p, status);
-  else simt_grouped_kernel<T, false><<<grid, kThreads, 0, stream>>>(p, status);
+  if (p.wq) launch_pdl(simt_grouped_kernel<T, true>, grid, dim3(kThreads), 0, stream, p, status);
+  else launch_pdl(simt_grouped_kernel<T, false>, grid, dim3(kThreads), 0, stream, p, status);
 }
 
 dim3 tile_grid(int64_t M, int64_t N, int64_t batch) {
@@ -905,7 +910,7 @@ mm_status launch_tile_cfg(const GemmArgs& p, cudaStream_t stream) {
                   (unsigned)(p.bm.count < 65535 ? p.bm.count : 65535));
   const SimtOperand oa = simt_operand(p.a.ptr, (int)sizeof(T), p.a.rs, p.a.cs, p.bm, p.a.bstride);
   const SimtOperand ob = simt_operand(p.b.ptr, (int)sizeof(T), p.b.cs, p.b.rs, p.bm, p.b.bstride);
-  simt_gemm_kernel<T, TM, TM><<<grid, kThreads, 0, stream>>>(p, oa, ob);
+  launch_pdl(simt_gemm_kernel<T, TM, TM>, grid, dim3(kThreads), 0, stream, p, oa, ob);
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 
@@ -969,7 +974,7 @@ mm_status launch_vec_gemm(const GemmArgs& p, cudaStream_t stream) {
 mm_status launch_simt_qlinear(const QLinearArgs& p, cudaStream_t stream) {
   if (p.M == 0 || p.N == 0 || p.bm.count == 0) return MM_OK;
   if ((p.N + kTile - 1) / kTile > 0x7fffffff) return MM_ERR_UNSUPPORTED;
-  simt_qlinear_kernel<<<tile_grid(p.M, p.N, p.bm.count), kThreads, 0, stream>>>(p);
+  launch_pdl(simt_qlinear_kernel, tile_grid(p.M, p.N, p.bm.count), dim3(kThreads), 0, stream, p);
   return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }
 

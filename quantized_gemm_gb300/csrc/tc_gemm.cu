@@ -1259,7 +1259,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
   // Launched with programmatic stream serialization, this grid may start while
   // the previous kernel on the stream is finishing: the set-up above overlaps
   // its tail, and nothing below touches global memory before it completes.
-  griddep_wait();
+  pdl_wait();
+  if constexpr (MODE == kDense || MODE == kTF32) pdl_trigger();
   const uint32_t rank = PAIR ? (cluster_ctarank() & 1) : 0;
 
   if (warp == 0) {

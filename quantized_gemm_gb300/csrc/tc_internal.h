@@ -18,8 +18,10 @@ constexpr int kTileK = 64;    // one 128-byte swizzle row of 16-bit elements
 // kTF32: fp32 MatMul / Gemm as three tf32 products (hi*hi + hi*lo + lo*hi of
 // each operand's split x = hi + lo, split in shared memory by converter warps).
 // kSkinny: dense bf16/f16 products with at most 64 rows and few tiles (a
-// vector or a few rows against a wide B'): 64-column tiles, 64-row A boxes
-// and a 12-stage ring of 16 KB, so that many more bytes of B' are in flight.
+// vector or a few rows against a wide B'): 256-column tiles whose k-blocks
+// are split across the `split` CTAs of a cluster; each CTA keeps its fp32
+// partial sums in shared memory and reduces a slice of the columns over
+// distributed shared memory, so that every SM streams its own share of B'.
 enum TcMode { kDense = 0, kGrouped = 1, kQLinear = 2, kGroupedQ = 3, kTF32 = 4, kSkinny = 5 };
 
 struct TcParams {

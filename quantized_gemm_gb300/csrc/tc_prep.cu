@@ -112,6 +112,7 @@ __device__ __forceinline__ void store16_f16(__half* dst, const int (&x)[16], int
 
 // a: one warp per (matrix, row): converts the row and writes its exact sum.
 __global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t total = p.count * p.rows;
@@ -159,6 +160,7 @@ constexpr int kColGroups = 16;                   // 16-column groups per block
 constexpr int kRowLanes = 16;
 
 __global__ void __launch_bounds__(kColGroups * kRowLanes, 2) shift_cols_kernel(const ShiftArgs p) {
+  pdl_wait();
   __shared__ uint32_t part_s[kRowLanes][kColGroups * 16 + 1];
   const int cgl = threadIdx.x % kColGroups, lane_r = threadIdx.x / kColGroups;
   const int64_t cgroups = (p.cols + 15) / 16;
@@ -308,11 +310,12 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
   if (cudaMemsetAsync(cs, 0, (size_t)(l.b_count * q.N * 4), stream) != cudaSuccess) return MM_ERR_CUDA;
   const int64_t awarps = l.a_count * q.M;
   const int64_t ablocks = (awarps + 7) / 8;
-  shift_rows_kernel<<<(unsigned)(ablocks < 8 * 152 * 8 ? ablocks : 8 * 152 * 8), 256, 0, stream>>>(sa);
+  launch_pdl(shift_rows_kernel, dim3((unsigned)(ablocks < 8 * 152 * 8 ? ablocks : 8 * 152 * 8)), dim3(256), 0, stream,
+             sa);
   const int64_t bblocks =
       l.b_count * ((q.K + kColRows - 1) / kColRows) * ((((q.N + 15) / 16) + kColGroups - 1) / kColGroups);
-  shift_cols_kernel<<<(unsigned)(bblocks < 16 * 152 * 8 ? bblocks : 16 * 152 * 8), kColGroups * kRowLanes, 0,
-                      stream>>>(sb);
+  launch_pdl(shift_cols_kernel, dim3((unsigned)(bblocks < 16 * 152 * 8 ? bblocks : 16 * 152 * 8)),
+             dim3(kColGroups * kRowLanes), 0, stream, sb);
   if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
 
   // 2. The f16 GEMM with 1024-deep exact segments and the zero-point-correcting,
@@ -374,6 +377,7 @@ constexpr int kHistGroups = 4096;
 __global__ void __launch_bounds__(256) route_count_kernel(const void* gi, int ind64, int64_t gi_ms, int64_t gi_ss,
                                                           int64_t M, int64_t S, int64_t G, int32_t* count,
                                                           unsigned* status) {
+  pdl_wait();
   __shared__ int32_t hist[kHistGroups];
   const int64_t total = M * S;
   const bool shared_hist = G <= kHistGroups;
@@ -438,6 +442,7 @@ __device__ __forceinline__ int64_t block_inclusive_sum(int64_t v, int64_t* part)
 // One block: offset[g] = sum_{h<g} count[h]; tile_start[g] = sum_{h<g} ceil(count[h]/tile_rows) * nt.
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* count, int64_t G, int64_t nt,
                                                           int tile_rows, int32_t* offset, int32_t* tile_start) {
+  pdl_wait();
   __shared__ int64_t part[32];
   const int t = threadIdx.x, T = blockDim.x;
   const int64_t per = (G + T - 1) / T;
@@ -473,6 +478,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) route_scatter_kernel(const GroupedArgs g, const int32_t* offset,
                                                             int32_t* cursor, int32_t* rowlist, T* xperm,
                                                             int64_t kp) {
+  pdl_wait();
   __shared__ int64_t s_pos;
   const int64_t total = g.M * g.S;
   const T* X = static_cast<const T*>(g.x);
@@ -589,16 +595,17 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
 
   if (cudaMemsetAsync(count, 0, l.off_offset - l.off_count, stream) != cudaSuccess) return MM_ERR_CUDA;
   const int64_t cb = (rows + 255) / 256;
-  route_count_kernel<<<(unsigned)(cb < 4096 ? cb : 4096), 256, 0, stream>>>(g.gi, g.ind64, g.gi_ms, g.gi_ss, g.M,
-                                                                          g.S, g.G, count, status);
-  route_scan_kernel<<<1, 1024, 0, stream>>>(count, g.G, nt, pair ? 2 * kTileM : kTileM, offset, tile_start);
+  launch_pdl(route_count_kernel, dim3((unsigned)(cb < 4096 ? cb : 4096)), dim3(256), 0, stream, g.gi, g.ind64, g.gi_ms,
+             g.gi_ss, g.M, g.S, g.G, count, status);
+  launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)count, g.G, nt,
+             pair ? 2 * kTileM : kTileM, offset, tile_start);
   const unsigned sgrid = (unsigned)(rows < 65536 ? rows : 65536);
   if (g.dtype == MM_BF16)
-    route_scatter_kernel<__nv_bfloat16><<<sgrid, 128, 0, stream>>>(g, offset, cursor, rowlist,
-                                                                   static_cast<__nv_bfloat16*>(xperm), l.kp);
+    launch_pdl(route_scatter_kernel<__nv_bfloat16>, dim3(sgrid), dim3(128), 0, stream, g, (const int32_t*)offset,
+               cursor, rowlist, static_cast<__nv_bfloat16*>(xperm), l.kp);
   else
-    route_scatter_kernel<__half><<<sgrid, 128, 0, stream>>>(g, offset, cursor, rowlist, static_cast<__half*>(xperm),
-                                                            l.kp);
+    launch_pdl(route_scatter_kernel<__half>, dim3(sgrid), dim3(128), 0, stream, g, (const int32_t*)offset, cursor,
+               rowlist, static_cast<__half*>(xperm), l.kp);
   if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
 
   TcParams p;

@@ -169,11 +169,6 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // Until this thread's committed bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Programmatic dependent launch: wait until the grids this one depends on
-// have completed and their memory is visible (a no-op for a launch without
-// the programmatic-serialization attribute).
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Shared-memory vector accesses by 32-bit shared address.
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
