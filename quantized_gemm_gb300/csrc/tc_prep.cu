@@ -110,111 +110,131 @@ __device__ __forceinline__ void store16_f16(__half* dst, const int (&x)[16], int
   if (c0 + 8 < ld) d[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// a: one warp per (matrix, row): converts the row and writes its exact sum.
-__global__ void __launch_bounds__(256) shift_rows_kernel(const ShiftArgs p) {
+// a: one warp converts one row (matrix `mat`, row r) and writes its exact sum.
+__device__ __forceinline__ void shift_row(const ShiftArgs& p, int64_t wr, int lane) {
+  const int64_t mat = wr / p.rows, r = wr - mat * p.rows;
+  const uint8_t* srow = p.src + own_offset(p, mat) + r * p.src_rs;
+  __half* drow = p.dst + wr * p.ld;
+  uint32_t sum = 0;   // modulo 2^32, like every term of the int32 accumulator
+  for (int64_t cb = (int64_t)lane * 16; cb < p.cols; cb += 512 * kBatch) {
+    uint4 raw[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t c0 = cb + 512 * u;
+      raw[u] = vec16_ok(p, srow, c0) ? __ldg(reinterpret_cast<const uint4*>(srow + c0)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t c0 = cb + 512 * u;
+      if (c0 >= p.cols) break;
+      int x[16];
+      if (vec16_ok(p, srow, c0)) decode16(raw[u], p.is_signed, x);
+      else load16_scalar(p, srow, c0, x);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sum += (uint32_t)x[e];
+      store16_f16(drow + c0, x, c0, p.ld);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) p.sums[wr] = (int32_t)sum;
+}
+
+// b: one warp converts a strip of 256 columns (8 per lane) over a band of
+// kStripRows rows, reading kBatch consecutive rows at a time (each load of the
+// warp is 256 contiguous bytes of a row), and adds its partial column sums to
+// the column sums (which start at zero) with one atomic add per column.
+constexpr int kStripRows = 64;
+
+// x = 8 bytes moved into [-128, 127]; zeros beyond `cols`.  Vector loads need
+// a unit column stride and an 8-byte aligned, complete piece.
+__device__ __forceinline__ bool vec8_ok(const ShiftArgs& p, const uint8_t* srow, int64_t c0) {
+  return p.src_cs == 1 && c0 + 8 <= p.cols && ((reinterpret_cast<uintptr_t>(srow + c0) & 7) == 0);
+}
+
+__device__ __forceinline__ void decode8(const uint2& u, int is_signed, int (&x)[8]) {
+  const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t b = (w[q] >> (8 * e)) & 0xFFu;
+      x[4 * q + e] = is_signed ? (int)(int8_t)b : (int)b - 128;
+    }
+}
+
+__device__ __forceinline__ void shift_strip(const ShiftArgs& p, int64_t unit, int lane) {
+  const int64_t strips = (p.cols + 255) / 256;
+  const int64_t bands = (p.rows + kStripRows - 1) / kStripRows;
+  const int64_t mat = unit / (strips * bands);
+  const int64_t rest = unit - mat * strips * bands;
+  const int64_t band = rest / strips, strip = rest - band * strips;
+  const int64_t c0 = strip * 256 + (int64_t)lane * 8;
+  if (c0 >= p.cols) return;
+  const uint8_t* base = p.src + own_offset(p, mat);
+  __half* dbase = p.dst + mat * p.rows * p.ld + c0;
+  const int64_t r0 = band * kStripRows, r1 = min(p.rows, r0 + kStripRows);
+  uint32_t part[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[e] = 0;
+  for (int64_t rb = r0; rb < r1; rb += kBatch) {
+    uint2 raw[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const uint8_t* srow = base + (rb + u) * p.src_rs;
+      raw[u] = (rb + u < r1 && vec8_ok(p, srow, c0)) ? __ldg(reinterpret_cast<const uint2*>(srow + c0))
+                                                     : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t r = rb + u;
+      if (r >= r1) break;
+      const uint8_t* srow = base + r * p.src_rs;
+      int x[8];
+      if (vec8_ok(p, srow, c0)) {
+        decode8(raw[u], p.is_signed, x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          int v = 0;
+          if (c0 + e < p.cols) {
+            const uint8_t b = __ldg(srow + (c0 + e) * p.src_cs);
+            v = p.is_signed ? (int)(int8_t)b : (int)b - 128;
+          }
+          x[e] = v;
+        }
+      }
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        part[2 * e] += (uint32_t)x[2 * e];
+        part[2 * e + 1] += (uint32_t)x[2 * e + 1];
+        __half2 h = __floats2half2_rn((float)x[2 * e], (float)x[2 * e + 1]);   // exact: |x| <= 128
+        w[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      // 8 columns from c0 < cols end within the row padded to ld = round8(cols)
+      *reinterpret_cast<uint4*>(dbase + r * p.ld) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  unsigned* sums = reinterpret_cast<unsigned*>(p.sums) + mat * p.cols;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (c0 + e < p.cols) atomicAdd(sums + c0 + e, part[e]);
+}
+
+// Both operands in one launch, one warp per unit: units [0, b_units) are b's
+// column strips (the larger units, taken first), the rest a's rows.  One
+// launch lets b's work fill the gaps of a's and leaves no second, partly
+// filled last wave.  Four blocks per SM cap a thread at 64 registers (no
+// spills); unbounded, the strip path took 153.
+__global__ void __launch_bounds__(256, 4) shift_kernel(const ShiftArgs pa, const ShiftArgs pb, const int64_t b_units) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t total = p.count * p.rows;
-  for (int64_t wr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wr < total; wr += warps) {
-    const int64_t mat = wr / p.rows, r = wr - mat * p.rows;
-    const uint8_t* srow = p.src + own_offset(p, mat) + r * p.src_rs;
-    __half* drow = p.dst + wr * p.ld;
-    uint32_t sum = 0;   // modulo 2^32, like every term of the int32 accumulator
-    for (int64_t cb = (int64_t)lane * 16; cb < p.cols; cb += 512 * kBatch) {
-      uint4 raw[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int64_t c0 = cb + 512 * u;
-        raw[u] = vec16_ok(p, srow, c0) ? __ldg(reinterpret_cast<const uint4*>(srow + c0)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int64_t c0 = cb + 512 * u;
-        if (c0 >= p.cols) break;
-        int x[16];
-        if (vec16_ok(p, srow, c0)) decode16(raw[u], p.is_signed, x);
-        else load16_scalar(p, srow, c0, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sum += (uint32_t)x[e];
-        store16_f16(drow + c0, x, c0, p.ld);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) p.sums[wr] = (int32_t)sum;
-  }
-}
-
-// b: a block converts a strip of 256 columns (16 column groups of 16) over a
-// band of kColRows rows; its 16 row lanes stride through the band, their
-// partial column sums are combined in shared memory, and one atomic add per
-// column and block accumulates the band into the column sums (which start at
-// zero).  Consecutive threads read consecutive 16-byte pieces of a row.
-// Two blocks per SM: unbounded, the batched loads and decoded values took 246
-// registers a thread and one block per SM; capped at 122 (no spills) the
-// int8 workload's call is 0.4145 -> 0.4087 ms, its 4-batch variant (four b
-// matrices) 0.481 -> 0.457 ms.
-constexpr int kColRows = 128;
-constexpr int kColGroups = 16;                   // 16-column groups per block
-constexpr int kRowLanes = 16;
-
-__global__ void __launch_bounds__(kColGroups * kRowLanes, 2) shift_cols_kernel(const ShiftArgs p) {
-  pdl_wait();
-  __shared__ uint32_t part_s[kRowLanes][kColGroups * 16 + 1];
-  const int cgl = threadIdx.x % kColGroups, lane_r = threadIdx.x / kColGroups;
-  const int64_t cgroups = (p.cols + 15) / 16;
-  const int64_t cblocks = (cgroups + kColGroups - 1) / kColGroups;
-  const int64_t rblocks = (p.rows + kColRows - 1) / kColRows;
-  const int64_t total = p.count * rblocks * cblocks;
-  for (int64_t bidx = blockIdx.x; bidx < total; bidx += gridDim.x) {
-    const int64_t cb = bidx % cblocks;
-    const int64_t rest = bidx / cblocks;
-    const int64_t rb = rest % rblocks, mat = rest / rblocks;
-    const int64_t cg = cb * kColGroups + cgl;
-    const int64_t c0 = cg * 16;
-    uint32_t part[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) part[e] = 0;
-    if (cg < cgroups) {
-      const uint8_t* base = p.src + own_offset(p, mat);
-      const int64_t r1 = min(p.rows, (rb + 1) * kColRows);
-      for (int64_t rbase = rb * kColRows + lane_r; rbase < r1; rbase += kRowLanes * kBatch) {
-        uint4 raw[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t r = rbase + kRowLanes * u;
-          const uint8_t* srow = base + r * p.src_rs;
-          raw[u] = (r < r1 && vec16_ok(p, srow, c0)) ? __ldg(reinterpret_cast<const uint4*>(srow + c0))
-                                                     : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t r = rbase + kRowLanes * u;
-          if (r >= r1) break;
-          const uint8_t* srow = base + r * p.src_rs;
-          int x[16];
-          if (vec16_ok(p, srow, c0)) decode16(raw[u], p.is_signed, x);
-          else load16_scalar(p, srow, c0, x);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) part[e] += (uint32_t)x[e];
-          store16_f16(p.dst + (mat * p.rows + r) * p.ld + c0, x, c0, p.ld);
-        }
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < 16; ++e) part_s[lane_r][cgl * 16 + e] = part[e];
-    __syncthreads();
-    // thread t sums column t of the strip over the 16 row lanes
-    const int col = threadIdx.x;
-    const int64_t c = cb * kColGroups * 16 + col;
-    if (c < p.cols) {
-      uint32_t sum = 0;
-#pragma unroll
-      for (int l = 0; l < kRowLanes; ++l) sum += part_s[l][col];
-      atomicAdd(reinterpret_cast<unsigned*>(p.sums) + mat * p.cols + c, sum);
-    }
+  const int64_t total = b_units + pa.count * pa.rows;
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < total; u += warps) {
+    if (u < b_units) shift_strip(pb, u, lane);
+    else shift_row(pa, u - b_units, lane);
   }
 }
 
@@ -308,14 +328,10 @@ mm_status launch_tc_qlinear(const QLinearArgs& q, void* ws, unsigned* status, cu
     sb.src_bstride[d] = q.b.bstride[d];
   }
   if (cudaMemsetAsync(cs, 0, (size_t)(l.b_count * q.N * 4), stream) != cudaSuccess) return MM_ERR_CUDA;
-  const int64_t awarps = l.a_count * q.M;
-  const int64_t ablocks = (awarps + 7) / 8;
-  launch_pdl(shift_rows_kernel, dim3((unsigned)(ablocks < 8 * 152 * 8 ? ablocks : 8 * 152 * 8)), dim3(256), 0, stream,
-             sa);
-  const int64_t bblocks =
-      l.b_count * ((q.K + kColRows - 1) / kColRows) * ((((q.N + 15) / 16) + kColGroups - 1) / kColGroups);
-  launch_pdl(shift_cols_kernel, dim3((unsigned)(bblocks < 16 * 152 * 8 ? bblocks : 16 * 152 * 8)),
-             dim3(kColGroups * kRowLanes), 0, stream, sb);
+  const int64_t b_units = l.b_count * ((q.N + 255) / 256) * ((q.K + kStripRows - 1) / kStripRows);
+  const int64_t blocks = (b_units + l.a_count * q.M + 7) / 8;
+  launch_pdl(shift_kernel, dim3((unsigned)(blocks < 8 * 152 * 8 ? blocks : 8 * 152 * 8)), dim3(256), 0, stream, sa, sb,
+             b_units);
   if (cudaGetLastError() != cudaSuccess) return MM_ERR_CUDA;
 
   // 2. The f16 GEMM with 1024-deep exact segments and the zero-point-correcting,
