@@ -243,11 +243,11 @@ def test_qlinear_tensor(ta, tb, ty, gran, M, K, N):
 @pytest.mark.parametrize("M,K,N,gran,batch", [(600, 1096, 264, "vector", ()), (1000, 2048, 520, "matrix", ()),
                                                (385, 1024, 136, "vector", ()), (300, 1024, 264, "matrix", (2,))])
 def test_qlinear_tensor_long_k_ragged(M, K, N, gran, batch):
-    # K >= 1024 (several exact 1024-deep segments; CTA pairs of 256-row tiles)
-    # with ragged edges: 600, 1000 and 385 rows end in partial pair tiles
-    # whose second CTA holds 0, 104 and 1 valid rows, K = 1096 in a partial
-    # k-block and a 72-deep last segment, N = 264 and 136 in partial column
-    # tiles; the last case has batch-indexed per-row and per-column parameters.
+    # K >= 1024 (several exact 1024-deep segments) with ragged edges: 600,
+    # 1000 and 385 rows end in partial 128-row tiles of 88, 104 and 1 valid
+    # rows, K = 1096 in a partial k-block and a 72-deep last segment, N = 264
+    # and 136 in partial column tiles; the last case has batch-indexed per-row
+    # and per-column parameters.
     _q(_qcase(M, K, N, torch.int8, torch.uint8, torch.int8, gran, batch_a=batch, batch_b=batch, seed=M))
 
 
