@@ -18,8 +18,8 @@ Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize(), timed with CUDA events on the stream the library
 launches on; the max over ranks is reported.  The Gemm inputs (A and B,
 256 MiB) are larger than L2 (129 MB); the small f32 workload flushes L2
-(writes 256 MiB) between timed iterations.  nvidia-smi samples the SM clock
-and throttle reasons while the timed loop runs.
+(reads a 258 MB buffer) between timed iterations.  nvidia-smi samples the SM
+clock and throttle reasons every 20 ms while the timed loop runs.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent problems, no data-path collective: weak scaling); the
@@ -111,7 +111,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples, 100 ms apart, for one GPU."""
+    """nvidia-smi SM clock / throttle-reason samples, 20 ms apart, for one GPU."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -127,7 +127,7 @@ class ClockSampler:
             sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:

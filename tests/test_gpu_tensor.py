@@ -251,6 +251,25 @@ def test_qlinear_tensor_long_k_ragged(M, K, N, gran, batch):
     _q(_qcase(M, K, N, torch.int8, torch.uint8, torch.int8, gran, batch_a=batch, batch_b=batch, seed=M))
 
 
+@pytest.mark.parametrize("layout", ["transposed", "odd_offset"])
+def test_qlinear_tensor_strided_operands(layout):
+    # The preparation kernel reads a and b through their strides: column-major
+    # operands (no unit stride along a row) and rows that start one byte past
+    # an aligned address (no vector load is aligned) take its byte-wise loads,
+    # in both the row path (a) and the column-strip path (b).
+    d = _qcase(300, 1100, 264, torch.int8, torch.uint8, torch.int8, "vector", seed=11)
+    for key in ("a", "b"):
+        x = d[key]
+        if layout == "transposed":
+            d[key] = x.t().contiguous().t()
+        else:
+            wide = torch.zeros((x.shape[0], x.shape[1] + 1), dtype=x.dtype, device=DEV)
+            wide[:, 1:] = x
+            d[key] = wide[:, 1:]
+        assert not d[key].is_contiguous()
+    _q(d)
+
+
 def test_qlinear_tensor_f16_scales_and_batch():
     _q(_qcase(150, 300, 200, torch.int8, torch.int8, torch.int8, "matrix", torch.float16,
               batch_a=(2, 3), batch_b=(2, 3)))
