@@ -11,6 +11,7 @@ shared library was not built raises immediately.
 
 import ctypes
 import os
+import struct
 
 import torch
 
@@ -95,30 +96,39 @@ def _lib():
     return _LIB
 
 
+# MMTensor's bytes: pointer, dtype, ndim, shape[8], strides[8] (packed in one
+# call, which is cheaper than filling the ctypes arrays element by element).
+_MM_TENSOR_BYTES = struct.Struct("<Qii%dq%dq" % (MM_MAX_DIMS, MM_MAX_DIMS))
+_ZEROS = (0,) * MM_MAX_DIMS
+
+
 def _desc(t):
     """mm_tensor describing torch tensor ``t`` (None -> NULL)."""
     if t is None:
         return None
-    if t.dtype not in _DTYPES:
+    dt = _DTYPES.get(t.dtype)
+    if dt is None:
         raise TypeError("unsupported dtype %s" % t.dtype)
-    if t.dim() > MM_MAX_DIMS:
+    nd = t.dim()
+    if nd > MM_MAX_DIMS:
         raise ValueError("at most %d dimensions" % MM_MAX_DIMS)
-    d = MMTensor()
-    d.data = t.data_ptr() if t.numel() > 0 else None
-    d.dtype = _DTYPES[t.dtype]
-    d.ndim = t.dim()
-    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
-        d.shape[i] = s
-        d.strides[i] = st
-    return d
+    return MMTensor.from_buffer_copy(_MM_TENSOR_BYTES.pack(
+        t.data_ptr() if t.numel() > 0 else 0, dt, nd, *(tuple(t.shape) + _ZEROS[nd:]), *(t.stride() + _ZEROS[nd:])))
 
 
 def _ref(d):
     return None if d is None else ctypes.byref(d)
 
 
+# The current stream's handle for a device index, without building a
+# torch.cuda.Stream object (the public route below when torch lacks it).
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t, stream):
     if stream is None:
+        if _RAW_STREAM is not None and t.is_cuda:
+            return ctypes.c_void_p(_RAW_STREAM(t.get_device()))
         stream = torch.cuda.current_stream(t.device)
     return ctypes.c_void_p(stream.cuda_stream)
 
@@ -209,8 +219,9 @@ def mm_matmul(A, B, out=None, stream=None):
     """Y = A @ B with numpy.matmul semantics (MatMul, opset 13)."""
     lib = _lib()
     dA, dB = _desc(A), _desc(B)
-    shape = _out_shape(lib.mm_matmul_output_shape, _ref(dA), _ref(dB))
-    Y = torch.empty(shape, dtype=A.dtype, device=A.device) if out is None else out
+    # A given output is checked by the library itself (MM_ERR_SHAPE).
+    Y = out if out is not None else torch.empty(_out_shape(lib.mm_matmul_output_shape, _ref(dA), _ref(dB)),
+                                                dtype=A.dtype, device=A.device)
     _check(lib.mm_matmul(_ref(dA), _ref(dB), _ref(_desc(Y)), _stream(A, stream)), "mm_matmul")
     return Y
 
@@ -219,8 +230,9 @@ def mm_gemm(A, B, C=None, alpha=1.0, beta=1.0, transA=0, transB=0, out=None, str
     """Y = alpha * A' @ B' + beta * C (Gemm, opset 13)."""
     lib = _lib()
     dA, dB = _desc(A), _desc(B)
-    shape = _out_shape(lib.mm_gemm_output_shape, _ref(dA), _ref(dB), int(transA), int(transB))
-    Y = torch.empty(shape, dtype=A.dtype, device=A.device) if out is None else out
+    Y = out if out is not None else torch.empty(
+        _out_shape(lib.mm_gemm_output_shape, _ref(dA), _ref(dB), int(transA), int(transB)), dtype=A.dtype,
+        device=A.device)
     _check(lib.mm_gemm(_ref(dA), _ref(dB), _ref(_desc(C)), float(alpha), float(beta), int(transA), int(transB),
                        _ref(_desc(Y)), _stream(A, stream)), "mm_gemm")
     return Y
@@ -231,8 +243,8 @@ def mm_qlinear_matmul(a, a_scale, a_zero_point, b, b_scale, b_zero_point, y_scal
     """Quantized matmul of int8/uint8 tensors (QLinearMatMul, opset 10); y has y_zero_point's type."""
     lib = _lib()
     da, db = _desc(a), _desc(b)
-    shape = _out_shape(lib.mm_matmul_output_shape, _ref(da), _ref(db))
-    y = torch.empty(shape, dtype=y_zero_point.dtype, device=a.device) if out is None else out
+    y = out if out is not None else torch.empty(_out_shape(lib.mm_matmul_output_shape, _ref(da), _ref(db)),
+                                                dtype=y_zero_point.dtype, device=a.device)
     nbytes = ctypes.c_size_t()
     _check(lib.mm_qlinear_matmul_workspace_size(_ref(da), _ref(db), ctypes.byref(nbytes)),
            "mm_qlinear_matmul_workspace_size")
