@@ -91,6 +91,21 @@ def test_qweights_tensor(dtype, wdtype, block, with_zp, with_bias):
     assert qg.mm_get_device_status() == "MM_OK"
 
 
+@pytest.mark.parametrize("wdtype", [torch.int8, torch.uint8], ids=str)
+@pytest.mark.parametrize("block", [0, 192])
+def test_qweights_tensor_long_k(wdtype, block):
+    # K = 1000: 16 k-blocks per tile, so each of the five staging slots is
+    # reused several times within a tile and across the row tiles of a group;
+    # with one scale row per column (block 0) every k-block of a column tile
+    # takes the same scale and zero-point rows, with blocks of 192 rows of K
+    # they change every 3 k-blocks.
+    d = _case(520, 1000, 400, 3, 2, torch.bfloat16, wdtype, block, True, False, 61, p=[0.6, 0.3, 0.1])
+    with path(qg.MM_PATH_TENSOR):
+        _check(d, TOL[torch.bfloat16])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=str)
 @pytest.mark.parametrize("wdtype", [torch.int8, torch.uint8], ids=str)
 def test_qweights_tensor_dequantized_values_exact(dtype, wdtype):
