@@ -59,7 +59,13 @@ typedef enum mm_status {
 typedef enum mm_dtype {
   MM_BF16 = 0, MM_F16 = 1, MM_F32 = 2, MM_F64 = 3,
   MM_I32 = 4, MM_I64 = 5, MM_U32 = 6, MM_U64 = 7,
-  MM_I8 = 8, MM_U8 = 9
+  MM_I8 = 8, MM_U8 = 9,
+  /* 4-bit integers ([-8, 7] and [0, 15]), packed two per byte: the element
+   * at element offset e = sum_d index[d] * strides[d] is the low nibble of
+   * byte e / 2 of `data` when e is even and its high nibble when e is odd.
+   * Accepted only as the weights and zero points of
+   * mm_grouped_matmul_qweights (quantized experts stored with 4 bits). */
+  MM_I4 = 10, MM_U4 = 11
 } mm_dtype;
 
 typedef struct mm_tensor {
@@ -210,16 +216,20 @@ mm_status mm_grouped_matmul(const mm_tensor* input, const mm_tensor* weights,
  * used: the difference is an exact integer and the product is rounded once to
  * T (nearest, ties to even), so W is exactly what a separate dequantization to
  * T would store; the product with W then accumulates as in mm_grouped_matmul.
- *   input [M,K] (T = bf16, f16, f32 or f64); weights_q [G,K,N] MM_I8 or MM_U8;
- *   w_scale [G, ceil(K/B), N] of type T; w_zero_point NULL (zero) or of the
- *   type of weights_q and the shape of w_scale; group_indices [M,S] MM_I32 or
+ *   input [M,K] (T = bf16, f16, f32 or f64); weights_q [G,K,N] MM_I8, MM_U8,
+ *   MM_I4 or MM_U4; w_scale [G, ceil(K/B), N] of type T; w_zero_point NULL
+ *   (zero) or of the type of weights_q and the shape of w_scale; 4-bit
+ *   weights and zero points need a unit stride along N, N even and even
+ *   strides along G and K (rows start on byte boundaries; otherwise
+ *   MM_ERR_SHAPE); group_indices [M,S] MM_I32 or
  *   MM_I64; bias NULL or [G,N] of type T; output dense [M,S,N] of type T.
  *   block_size < 0 returns MM_ERR_INVALID_ARG.  Invalid group indices as for
  *   mm_grouped_matmul (zero rows, MM_ERR_INDEX_RANGE in the device status).
  * The tensor-core path (bf16/f16; weights, scales and zero points with a
  * unit-stride N dimension and 16-byte aligned rows; B a multiple of 64 or
- * B >= K) keeps the weights int8 in memory: each k-block is loaded as int8
- * and converted in shared memory just before the tensor cores read it.
+ * B >= K) keeps the weights 8- or 4-bit in memory: each k-block is loaded
+ * as stored and converted in shared memory just before the tensor cores
+ * read it.
  * Workspace: mm_grouped_matmul_qweights_workspace_size() bytes. */
 mm_status mm_grouped_matmul_qweights_workspace_size(const mm_tensor* input, const mm_tensor* weights_q,
                                                     const mm_tensor* w_scale, const mm_tensor* w_zero_point,

@@ -44,7 +44,7 @@ from .matmul import matmul, matmul_output_shape, matmul_abs_scale
 from .gemm import gemm, gemm_output_shape, gemm_abs_scale
 from .qlinear_matmul import qlinear_matmul, requantize
 from .grouped_matmul import grouped_matmul, grouped_abs_scale
-from .dequantize_linear import (dequantize_linear, grouped_matmul_qweights, grouped_qweights_abs_scale,
+from .dequantize_linear import (dequantize_linear, unpack_4bit, grouped_matmul_qweights, grouped_qweights_abs_scale,
                                 round_to, round_to_bf16)
 
 __all__ = [
@@ -52,5 +52,5 @@ __all__ = [
     "gemm", "gemm_output_shape", "gemm_abs_scale",
     "qlinear_matmul", "requantize",
     "grouped_matmul", "grouped_abs_scale",
-    "dequantize_linear", "grouped_matmul_qweights", "grouped_qweights_abs_scale", "round_to", "round_to_bf16",
+    "dequantize_linear", "unpack_4bit", "grouped_matmul_qweights", "grouped_qweights_abs_scale", "round_to", "round_to_bf16",
 ]

@@ -7,7 +7,11 @@ GroupedMatMul; a runtime may fuse the two so that the dequantized [G, K, N]
 weights are never formed.  The pages name DequantizeLinear without defining
 it.  The reading used here (the plainest one; listed in the design notes):
 
-* weights_q [G, K, N] of int8 or uint8.  scale and zero_point share one shape
+* weights_q [G, K, N] of int8 or uint8, or of DequantizeLinear's 4-bit
+  types int4 / uint4 (values in [-8, 7] / [0, 15]).  4-bit tensors are stored
+  packed two per byte along their last axis, the even element in the low
+  nibble (``unpack_4bit`` states the layout; the formula below sees the
+  unpacked values).  scale and zero_point share one shape
   [G, Kb, N], Kb = ceil(K / block): element (g, k, n) uses entry
   (g, k // block, n), i.e. blocks of `block` consecutive k for each group and
   output column; block = K (Kb = 1) is one scale per group and column.
@@ -59,6 +63,22 @@ def round_to(x, t):
     if t == "f64":
         return np.asarray(x, dtype=np.float64)
     raise ValueError("t must be one of %s" % (T_NAMES,))
+
+
+def unpack_4bit(packed, signed):
+    """The 4-bit values stored in ``packed`` (uint8 [..., N/2]) as an int8
+    (signed: int4, [-8, 7]) or uint8 (uint4, [0, 15]) array [..., N]: element
+    2j of a row is the low nibble of byte j, element 2j + 1 its high nibble."""
+    b = np.asarray(packed)
+    if b.dtype != np.uint8:
+        raise TypeError("packed 4-bit values arrive as uint8 bytes")
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.int16)
+    out[..., 0::2] = b & 0x0F
+    out[..., 1::2] = b >> 4
+    if signed:
+        out = np.where(out >= 8, out - 16, out)
+        return out.astype(np.int8)
+    return out.astype(np.uint8)
 
 
 def dequantize_linear(weights_q, scale, zero_point=None, block=None, t="bf16"):

@@ -35,6 +35,9 @@ _DTYPES = {
     torch.int32: 4, torch.int64: 5, torch.uint32: 6, torch.uint64: 7,
     torch.int8: 8, torch.uint8: 9,
 }
+# 4-bit types (include/mm.h MM_I4 / MM_U4), which torch has no dtype for:
+# passed as uint8 bytes holding two values each (see _desc4).
+_PACKED4 = {"int4": 10, "uint4": 11}
 
 
 def library_path():
@@ -114,6 +117,23 @@ def _desc(t):
         raise ValueError("at most %d dimensions" % MM_MAX_DIMS)
     return MMTensor.from_buffer_copy(_MM_TENSOR_BYTES.pack(
         t.data_ptr() if t.numel() > 0 else 0, dt, nd, *(tuple(t.shape) + _ZEROS[nd:]), *(t.stride() + _ZEROS[nd:])))
+
+
+def _desc4(t, kind):
+    """mm_tensor of 4-bit values stored packed in uint8 tensor ``t`` [..., N/2]:
+    logical shape [..., N], element strides twice the byte strides (the last
+    one 1); the even element of a byte is its low nibble."""
+    if t is None:
+        return None
+    if kind not in _PACKED4:
+        raise ValueError("packed4 must be 'int4' or 'uint4'")
+    if t.dtype != torch.uint8 or t.dim() < 1 or t.stride(-1) != 1:
+        raise ValueError("packed 4-bit values arrive as a uint8 tensor with a unit stride in its last dimension")
+    nd = t.dim()
+    shape = tuple(t.shape[:-1]) + (2 * t.shape[-1],)
+    strides = tuple(2 * st for st in t.stride()[:-1]) + (1,)
+    return MMTensor.from_buffer_copy(_MM_TENSOR_BYTES.pack(
+        t.data_ptr() if t.numel() > 0 else 0, _PACKED4[kind], nd, *(shape + _ZEROS[nd:]), *(strides + _ZEROS[nd:])))
 
 
 def _ref(d):
@@ -273,27 +293,38 @@ def mm_grouped_matmul(input, weights, group_indices, bias=None, out=None, stream
     return y
 
 
-def mm_grouped_matmul_qweights_workspace_size(input, weights_q, w_scale, w_zero_point, block_size, group_indices):
+def _qdesc(t, packed4):
+    return _desc(t) if packed4 is None else _desc4(t, packed4)
+
+
+def mm_grouped_matmul_qweights_workspace_size(input, weights_q, w_scale, w_zero_point, block_size, group_indices,
+                                              packed4=None):
     nbytes = ctypes.c_size_t()
     _check(_lib().mm_grouped_matmul_qweights_workspace_size(
-        _ref(_desc(input)), _ref(_desc(weights_q)), _ref(_desc(w_scale)), _ref(_desc(w_zero_point)),
-        int(block_size), _ref(_desc(group_indices)), ctypes.byref(nbytes)), "mm_grouped_matmul_qweights_workspace_size")
+        _ref(_desc(input)), _ref(_qdesc(weights_q, packed4)), _ref(_desc(w_scale)),
+        _ref(_qdesc(w_zero_point, packed4)), int(block_size), _ref(_desc(group_indices)), ctypes.byref(nbytes)),
+        "mm_grouped_matmul_qweights_workspace_size")
     return nbytes.value
 
 
 def mm_grouped_matmul_qweights(input, weights_q, w_scale, w_zero_point, block_size, group_indices, bias=None,
-                               out=None, stream=None, workspace=None):
-    """GroupedMatMul of int8/uint8 experts: input[m] @ W[g] (+ bias[g]) with
+                               out=None, stream=None, workspace=None, packed4=None):
+    """GroupedMatMul of quantized experts: input[m] @ W[g] (+ bias[g]) with
     W = DequantizeLinear(weights_q, w_scale, w_zero_point) in blocks of
-    ``block_size`` rows of K (0: one scale per group and column), fused."""
+    ``block_size`` rows of K (0: one scale per group and column), fused.
+    weights_q and w_zero_point are int8/uint8 tensors, or with ``packed4``
+    ('int4' or 'uint4') uint8 tensors [G, K, N/2] / [G, Kb, N/2] holding two
+    4-bit values per byte (the even column in the low nibble)."""
     lib = _lib()
-    M, S, N = input.shape[0], group_indices.shape[1], weights_q.shape[2]
+    M, S = input.shape[0], group_indices.shape[1]
+    N = weights_q.shape[2] * (2 if packed4 is not None else 1)
     y = torch.empty((M, S, N), dtype=input.dtype, device=input.device) if out is None else out
     ws, wsb = _workspace(mm_grouped_matmul_qweights_workspace_size(input, weights_q, w_scale, w_zero_point,
-                                                                   block_size, group_indices),
+                                                                   block_size, group_indices, packed4),
                          input.device, workspace)
-    _check(lib.mm_grouped_matmul_qweights(_ref(_desc(input)), _ref(_desc(weights_q)), _ref(_desc(w_scale)),
-                                          _ref(_desc(w_zero_point)), int(block_size), _ref(_desc(group_indices)),
+    _check(lib.mm_grouped_matmul_qweights(_ref(_desc(input)), _ref(_qdesc(weights_q, packed4)), _ref(_desc(w_scale)),
+                                          _ref(_qdesc(w_zero_point, packed4)), int(block_size),
+                                          _ref(_desc(group_indices)),
                                           _ref(_desc(bias)), _ref(_desc(y)), None if ws is None else ws.data_ptr(),
                                           wsb, _stream(input, stream)),
            "mm_grouped_matmul_qweights")

@@ -47,6 +47,7 @@ int elem_size(int dt) {
 bool is_int_type(int dt) { return dt == MM_I32 || dt == MM_I64 || dt == MM_U32 || dt == MM_U64; }
 bool is_matmul_type(int dt) { return dt >= MM_BF16 && dt <= MM_U64; }   // MatMul-13 / Gemm-13 T
 bool is_q8(int dt) { return dt == MM_I8 || dt == MM_U8; }
+bool is_q4(int dt) { return dt == MM_I4 || dt == MM_U4; }
 
 int64_t numel(const mm_tensor* t) {
   int64_t n = 1;
@@ -57,7 +58,7 @@ int64_t numel(const mm_tensor* t) {
 mm_status check_tensor(const mm_tensor* t) {
   if (!t) return MM_ERR_INVALID_ARG;
   if (t->ndim < 0 || t->ndim > MM_MAX_DIMS) return MM_ERR_INVALID_ARG;
-  if (elem_size(t->dtype) == 0) return MM_ERR_DTYPE;
+  if (elem_size(t->dtype) == 0 && !is_q4(t->dtype)) return MM_ERR_DTYPE;
   for (int d = 0; d < t->ndim; ++d)
     if (t->shape[d] < 0 || t->strides[d] < 0) return MM_ERR_INVALID_ARG;
   if (!t->data && numel(t) != 0) return MM_ERR_INVALID_ARG;
@@ -534,7 +535,7 @@ mm_status plan_grouped_q(const mm_tensor* input, const mm_tensor* weights_q, con
   if (block_size < 0) return MM_ERR_INVALID_ARG;
   const int dt = input->dtype;
   if (dt != MM_BF16 && dt != MM_F16 && dt != MM_F32 && dt != MM_F64) return MM_ERR_DTYPE;
-  if (weights_q->dtype != MM_I8 && weights_q->dtype != MM_U8) return MM_ERR_DTYPE;
+  if (!is_q8(weights_q->dtype) && !is_q4(weights_q->dtype)) return MM_ERR_DTYPE;
   if (w_scale->dtype != dt || (bias && bias->dtype != dt)) return MM_ERR_DTYPE;
   if (w_zero_point && w_zero_point->dtype != weights_q->dtype) return MM_ERR_DTYPE;
   if (gi->dtype != MM_I32 && gi->dtype != MM_I64) return MM_ERR_DTYPE;
@@ -550,6 +551,14 @@ mm_status plan_grouped_q(const mm_tensor* input, const mm_tensor* weights_q, con
       if (w_zero_point->shape[d] != w_scale->shape[d]) return MM_ERR_SHAPE;
   }
   if (bias && (bias->ndim != 2 || bias->shape[0] != G || bias->shape[1] != N)) return MM_ERR_SHAPE;
+  if (is_q4(weights_q->dtype)) {
+    // packed 4-bit rows start on byte boundaries: unit stride along N, N even
+    // and even strides along G and K (for the zero points likewise)
+    auto rows_on_bytes = [&](const mm_tensor* t) {
+      return t->strides[2] == 1 && t->shape[2] % 2 == 0 && t->strides[1] % 2 == 0 && t->strides[0] % 2 == 0;
+    };
+    if (!rows_on_bytes(weights_q) || (w_zero_point && !rows_on_bytes(w_zero_point))) return MM_ERR_SHAPE;
+  }
   memset(g, 0, sizeof(*g));
   g->dtype = dt;
   g->ind64 = gi->dtype == MM_I64;
@@ -559,7 +568,12 @@ mm_status plan_grouped_q(const mm_tensor* input, const mm_tensor* weights_q, con
   g->w_gs = weights_q->strides[0]; g->w_ks = weights_q->strides[1]; g->w_ns = weights_q->strides[2];
   g->gi = gi->data; g->gi_ms = gi->strides[0]; g->gi_ss = gi->strides[1];
   if (bias) { g->bias = bias->data; g->bias_gs = bias->strides[0]; g->bias_ns = bias->strides[1]; }
-  g->wq = weights_q->dtype == MM_I8 ? 1 : 2;
+  switch (weights_q->dtype) {
+    case MM_I8: g->wq = 1; break;
+    case MM_U8: g->wq = 2; break;
+    case MM_I4: g->wq = 3; break;
+    default: g->wq = 4; break;
+  }
   g->wsc = w_scale->data;
   g->wsc_gs = w_scale->strides[0]; g->wsc_bs = w_scale->strides[1]; g->wsc_ns = w_scale->strides[2];
   if (w_zero_point) {

@@ -48,9 +48,12 @@ struct GroupedArgs {
   const void* gi;  int64_t gi_ms, gi_ss;
   const void* bias; int64_t bias_gs, bias_ns;   // bias null = absent
   void* out;                 // dense [M, S, N]
-  // Weight-only quantized experts: w holds int8 (wq == 1) or uint8 (wq == 2)
-  // values and the weights are W = T((w - zero_point) * scale), scale and
-  // zero point [G, Kb, N] indexed by (g, k / qblock, n).  wq == 0: w is T.
+  // Weight-only quantized experts: w holds int8 (wq == 1), uint8 (2), int4
+  // (3) or uint4 (4) values and the weights are W = T((w - zero_point) *
+  // scale), scale and zero point [G, Kb, N] indexed by (g, k / qblock, n).
+  // 4-bit values are packed two per byte (element offset e: the low nibble
+  // of byte e / 2 when e is even, else its high nibble; strides in elements).
+  // wq == 0: w is T.
   int wq;
   const void* wsc; int64_t wsc_gs, wsc_bs, wsc_ns;   // scale, type T
   const void* wzp; int64_t wzp_gs, wzp_bs, wzp_ns;   // zero point (null = 0), type of w

@@ -808,6 +808,16 @@ __global__ void __launch_bounds__(kThreads) simt_qlinear_kernel(const QLinearArg
 
 // ------------------------------------------------------------------ GroupedMatMul
 
+// Quantized value at element offset e: int8 (wq 1), uint8 (2), or a 4-bit
+// int4 (3) / uint4 (4) packed two per byte, element e in the low nibble of
+// byte e / 2 when e is even and in its high nibble when e is odd.
+__device__ __forceinline__ int load_qweight(const void* base, int64_t e, int wq) {
+  const uint8_t* b = static_cast<const uint8_t*>(base);
+  if (wq <= 2) return wq == 1 ? (int)(int8_t)b[e] : (int)b[e];
+  const int nib = (b[e >> 1] >> ((e & 1) * 4)) & 15;
+  return wq == 3 ? nib - ((nib & 8) << 1) : nib;
+}
+
 // Weight (g, k, n) of weight-only quantized experts: T((q - zp) * scale), the
 // difference exact, the product exact in the accumulator type for a bf16 or
 // f16 scale (at most 9 + 11 significant bits) and rounded once for f32/f64;
@@ -818,12 +828,8 @@ __device__ __forceinline__ typename Arith<T>::acc dequant_weight(const GroupedAr
                                                                  int64_t n) {
   using Acc = typename Arith<T>::acc;
   const int64_t kq = k / p.qblock;
-  const uint8_t qb = static_cast<const uint8_t*>(p.w)[g * p.w_gs + k * p.w_ks + n * p.w_ns];
-  int d = p.wq == 1 ? (int)(int8_t)qb : (int)qb;
-  if (p.wzp) {
-    const uint8_t zb = static_cast<const uint8_t*>(p.wzp)[g * p.wzp_gs + kq * p.wzp_bs + n * p.wzp_ns];
-    d -= p.wq == 1 ? (int)(int8_t)zb : (int)zb;
-  }
+  int d = load_qweight(p.w, g * p.w_gs + k * p.w_ks + n * p.w_ns, p.wq);
+  if (p.wzp) d -= load_qweight(p.wzp, g * p.wzp_gs + kq * p.wzp_bs + n * p.wzp_ns, p.wq);
   const Acc sc = Arith<T>::load(static_cast<const T*>(p.wsc) + g * p.wsc_gs + kq * p.wsc_bs + n * p.wsc_ns);
   const T w = Arith<T>::store((Acc)d * sc);
   return Arith<T>::load(&w);

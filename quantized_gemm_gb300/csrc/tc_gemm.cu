@@ -273,6 +273,10 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
   uint32_t stage = 0, phase = 0;
   uint32_t pending = 0, pend_parity = 0;   // bit s: a load into stage s was issued (and its parity)
   uint32_t qstage = 0, qphase = 0, qpending = 0, qpend_parity = 0;   // the same for the staging ring
+  // kGroupedQ: bytes one staging slot receives per k-block (weight tile,
+  // scale row, zero-point row)
+  const uint32_t qbytes = p.w4 ? kQTileBytes / 2 + 256 + (p.wzp_present ? 64 : 0)
+                               : kQTileBytes + 256 + (p.wzp_present ? 128 : 0);
   Tile ti;
   int gh = 0;
   int kb_b, kb_e;
@@ -315,10 +319,12 @@ __device__ void run_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, con
         if (rank == 0) mbar_arrive_expect_tx(full, 2 * G::kABytes + 2 * kConvWarps * kSignalBytes);
         tma_load_3d_pair(sa, tmA, k0, ar, ti.a_b, mapa_shared(full, 0));
         const int32_t kq = kb / p.kb_per_q;
-        mbar_arrive_expect_tx(qfull, kQTileBytes + 256 + (p.wzp_present ? 128 : 0));
-        tma_load_3d(qs, tmB, bc, k0, ti.b_b, qfull);
+        // 4-bit weights and zero points: maps over bytes (two columns each)
+        const int32_t bq = p.w4 ? bc >> 1 : bc;
+        mbar_arrive_expect_tx(qfull, qbytes);
+        tma_load_3d(qs, tmB, bq, k0, ti.b_b, qfull);
         tma_load_3d(qs + kQScaleOff, tmS, bc, kq, ti.b_b, qfull);
-        if (p.wzp_present) tma_load_3d(qs + kQZeroOff, tmZ, bc, kq, ti.b_b, qfull);
+        if (p.wzp_present) tma_load_3d(qs + kQZeroOff, tmZ, bq, kq, ti.b_b, qfull);
         qpending |= 1u << qstage;
         qpend_parity = (qpend_parity & ~(1u << qstage)) | (qphase << qstage);
         if (++qstage == kQStages) { qstage = 0; qphase ^= 1; }
@@ -554,7 +560,7 @@ __device__ __forceinline__ uint32_t requant_byte_fast(int32_t acc, float sa, flo
 // final conversion is the only rounding.  Each warp then makes its writes
 // visible to the tensor cores, frees the staging slot and arrives on the
 // leader CTA's stage barrier, which the MMA waits on.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool W4>
 __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, uint32_t full0, uint32_t qbase,
                             uint32_t qfull0, uint32_t qempty0, uint32_t ctrl_u32, volatile int* abort) {
   using G = Geo<MODE, PAIR>;
@@ -562,9 +568,13 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
   const int lane = threadIdx.x & 31;
   const int cc = ct & 15, k_first = ct >> 4;
   const int sub = cc >> 3, c = cc & 7;
-  const uint32_t flip = p.w_signed ? 0x80808080u : 0u;
-  const float zbias = 8388608.f + (p.w_signed ? 128.f : 0.f);
-  const float hbias = 1024.f + (p.w_signed ? 128.f : 0.f);
+  // Signed values are moved to [0, 2^bits) by flipping their top bit: + 128
+  // for int8, + 8 for int4 (W4: 4-bit weights, two per byte, the even column
+  // in the low nibble; a staged row is 64 bytes instead of 128).
+  const float wshift = p.w_signed ? (W4 ? 8.f : 128.f) : 0.f;
+  const uint32_t flip = p.w_signed ? (W4 ? 0x08080808u : 0x80808080u) : 0u;
+  const float zbias = 8388608.f + wshift;
+  const float hbias = 1024.f + wshift;
   const bool f16 = p.out_f16 != 0;
   // smem is the kernel's shared memory; sbase and qbase are shared addresses in it.
   const uint32_t sm0 = smem_u32(smem);
@@ -582,10 +592,18 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
       constexpr int kRowStep = 2 * kConvWarps, kRows = 64 / kRowStep;
       uint2 raw[kRows];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i)
-        raw[i] = *reinterpret_cast<const uint2*>(qs + (k_first + kRowStep * i) * 128 + cc * 8);
+      for (int i = 0; i < kRows; ++i) {
+        if constexpr (W4)
+          raw[i] = make_uint2(*reinterpret_cast<const uint32_t*>(qs + (k_first + kRowStep * i) * 64 + cc * 4), 0u);
+        else
+          raw[i] = *reinterpret_cast<const uint2*>(qs + (k_first + kRowStep * i) * 128 + cc * 8);
+      }
       const uint4 sraw = *reinterpret_cast<const uint4*>(qs + kQScaleOff + cc * 16);
-      const uint2 zraw = p.wzp_present ? *reinterpret_cast<const uint2*>(qs + kQZeroOff + cc * 8) : make_uint2(0u, 0u);
+      uint2 zraw = make_uint2(0u, 0u);
+      if (p.wzp_present) {
+        if constexpr (W4) zraw.x = *reinterpret_cast<const uint32_t*>(qs + kQZeroOff + cc * 4);
+        else zraw = *reinterpret_cast<const uint2*>(qs + kQZeroOff + cc * 8);
+      }
       // Per column pair e2: the scales as staged (a bf16/f16 pair) and the
       // zero-point bias cz = bias + zp, in fp32 (bf16) or as an f16 pair.
       const uint32_t sw[4] = {sraw.x, sraw.y, sraw.z, sraw.w};
@@ -593,14 +611,32 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
       int zp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-        zp[e] = p.w_signed ? (int)(int8_t)zb : (int)zb;
+        if constexpr (W4) {
+          const int nib = (int)((zraw.x >> (4 * e)) & 15u);
+          zp[e] = p.w_signed ? nib - ((nib & 8) << 1) : nib;
+        } else {
+          const uint32_t zb = (zw[e >> 2] >> (8 * (e & 3))) & 0xFFu;
+          zp[e] = p.w_signed ? (int)(int8_t)zb : (int)zb;
+        }
       }
+      // A row's 8 values as bytes in [0, 2^bits), in column order: 4-bit
+      // values are spread over the bytes of two words (even columns from the
+      // low nibbles, odd ones from the high) and interleaved back.
+      auto row_bytes = [&](const uint2& r, uint32_t& qx, uint32_t& qy) {
+        if constexpr (W4) {
+          const uint32_t lo = (r.x & 0x0F0F0F0Fu) ^ flip, hi = ((r.x >> 4) & 0x0F0F0F0Fu) ^ flip;
+          qx = __byte_perm(lo, hi, 0x5140u);
+          qy = __byte_perm(lo, hi, 0x7362u);
+        } else {
+          qx = r.x ^ flip;
+          qy = r.y ^ flip;
+        }
+      };
       uint8_t* bsm = smem + (sbase - sm0) + stage * G::kStageBytes + G::kABytes + sub * 8192;
       if (f16) {
         // 1024 + u as f16 (byte u in the low mantissa of 0x6400) minus
-        // 1024 + 128*signed + zp is q - zp exactly (all below 2048); the f16
-        // pair product is rounded once.
+        // 1024 + shift + zp is q - zp exactly (all below 2048); the f16 pair
+        // product is rounded once.
         __half2 czh[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2)
@@ -608,7 +644,8 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
           const int k = k_first + kRowStep * i;
-          const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+          uint32_t qx, qy;
+          row_bytes(raw[i], qx, qy);
           uint32_t w[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
@@ -621,9 +658,9 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
           *reinterpret_cast<uint4*>(bsm + k * 128 + ((c ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       } else {
-        // The byte u (q moved to [0, 255]) in byte 1 of the pattern 0x47000000
-        // is the fp32 value 32768 + u.  With the column's bf16 scale s (8
-        // significant bits) and kc = -(32768 + c) * s, c = 128*signed + zp
+        // The byte u (q moved to [0, 2^bits)) in byte 1 of the pattern
+        // 0x47000000 is the fp32 value 32768 + u.  With the column's bf16 scale
+        // s (8 significant bits) and kc = -(32768 + c) * s, c = shift + zp
         // (a 16-bit integer times s: at most 24 significant bits, exact),
         // fma(32768 + u, s, kc) is (u - c) * s = (q - zp) * s before its one
         // rounding, and that value has at most 9 + 8 significant bits: the
@@ -635,14 +672,15 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           sf[e] = __uint_as_float((e & 1) ? (sw[e >> 1] & 0xFFFF0000u) : (sw[e >> 1] << 16));
-          kc[e] = __fmul_rn(-(32768.f + (p.w_signed ? 128.f : 0.f) + (float)zp[e]), sf[e]);
+          kc[e] = __fmul_rn(-(32768.f + wshift + (float)zp[e]), sf[e]);
           smax = fmaxf(smax, fabsf(sf[e]));
         }
         if (smax < 0x1p100f) {
 #pragma unroll
           for (int i = 0; i < kRows; ++i) {
             const int k = k_first + kRowStep * i;
-            const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+            uint32_t qx, qy;
+          row_bytes(raw[i], qx, qy);
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
@@ -666,7 +704,8 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
 #pragma unroll
           for (int i = 0; i < kRows; ++i) {
             const int k = k_first + kRowStep * i;
-            const uint32_t qx = raw[i].x ^ flip, qy = raw[i].y ^ flip;
+            uint32_t qx, qy;
+          row_bytes(raw[i], qx, qy);
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
@@ -1279,7 +1318,8 @@ __global__ void __launch_bounds__(Cfg<MODE, PAIR>::kThreads, 1)
     // Every tensor store has read its box before the CTA can exit.
     if (p.y_tma && lane == 0) bulk_wait_all();
   } else if (MODE == kGroupedQ) {
-    run_convert<MODE, PAIR>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
+    if (p.w4) run_convert<MODE, PAIR, true>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
+    else run_convert<MODE, PAIR, false>(p, smem_raw, sbase, full0, qbase, qfull0, qempty0, cbase, abort);
   } else if (MODE == kTF32) {
     run_split<MODE, PAIR>(p, smem_raw, sbase, full0, qfull0, cbase, abort);
   }

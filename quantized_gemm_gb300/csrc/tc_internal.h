@@ -74,9 +74,11 @@ struct TcParams {
   const int32_t* g_tile_start;
   const int32_t* g_rowlist;
   int G;
-  // kGroupedQ: weights are int8 (w_signed) or uint8; a scale row (and, when
-  // wzp_present, a zero-point row) applies to kb_per_q consecutive k-blocks.
-  int w_signed, wzp_present, kb_per_q;
+  // kGroupedQ: weights are int8 (w_signed) or uint8, or with w4 int4
+  // (w_signed) or uint4 packed two per byte (the even column in the low
+  // nibble); a scale row (and, when wzp_present, a zero-point row of the
+  // weights' type) applies to kb_per_q consecutive k-blocks.
+  int w_signed, w4, wzp_present, kb_per_q;
   unsigned* status;
   unsigned long long timeout_ns;    // limit of each pipeline wait
   unsigned long long teardown_ns;   // limit of the waits that let in-flight copies and MMAs land

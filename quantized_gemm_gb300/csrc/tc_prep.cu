@@ -542,21 +542,25 @@ int64_t map_stride(int64_t stride_bytes, int64_t count, int64_t fallback) {
   return count == 1 ? (fallback + 15) / 16 * 16 : stride_bytes;
 }
 
-// Weight-only quantized experts: the int8/uint8 weights (boxes of 128 columns
-// x 64 k) and the scale and zero-point rows (boxes of 128 columns x 1 row) as
-// plain tensor maps indexed (n, k or k-block, g).
+// Weight-only quantized experts: the weights (boxes of 128 columns x 64 k)
+// and the scale and zero-point rows (boxes of 128 columns x 1 row) as plain
+// tensor maps indexed (n, k or k-block, g).  The maps of 4-bit weights and
+// zero points address bytes (two columns each): boxes of 64 bytes.
 bool plan_grouped_q(const GroupedArgs& g, OperandPlan* b, OperandPlan* sm, OperandPlan* zm) {
   if (g.wq == 0 || g.w_ns != 1 || g.wsc_ns != 1 || (g.wzp && g.wzp_ns != 1)) return false;
   if (!(g.qblock >= g.K || g.qblock % kTileK == 0)) return false;
   const int64_t kb = (g.K + g.qblock - 1) / g.qblock;
-  if (!plan_plain_3d(g.w, 1, g.N, g.K, g.G, map_stride(g.w_ks, g.K, g.N), map_stride(g.w_gs, g.G, g.w_ks * g.K),
-                     128, 64, b))
+  const int64_t per = g.wq >= 3 ? 2 : 1;   // elements per byte
+  const int64_t nb = g.N / per;             // bytes per row (N is even for 4-bit)
+  const int box = 128 / (int)per;
+  if (!plan_plain_3d(g.w, 1, nb, g.K, g.G, map_stride(g.w_ks / per, g.K, nb),
+                     map_stride(g.w_gs / per, g.G, g.w_ks / per * g.K), box, 64, b))
     return false;
   const int64_t sbs = map_stride(g.wsc_bs * 2, kb, g.N * 2);
   if (!plan_plain_3d(g.wsc, 2, g.N, kb, g.G, sbs, map_stride(g.wsc_gs * 2, g.G, sbs * kb), 128, 1, sm)) return false;
   if (g.wzp) {
-    const int64_t zbs = map_stride(g.wzp_bs, kb, g.N);
-    if (!plan_plain_3d(g.wzp, 1, g.N, kb, g.G, zbs, map_stride(g.wzp_gs, g.G, zbs * kb), 128, 1, zm)) return false;
+    const int64_t zbs = map_stride(g.wzp_bs / per, kb, nb);
+    if (!plan_plain_3d(g.wzp, 1, nb, kb, g.G, zbs, map_stride(g.wzp_gs / per, g.G, zbs * kb), box, 1, zm)) return false;
   }
   return true;
 }
@@ -634,7 +638,8 @@ mm_status launch_tc_grouped(const GroupedArgs& g, void* ws, unsigned* status, cu
     p.idesc_tail = make_idesc_rows(g.dtype == MM_F16, a.mn_major, b.mn_major, kTileM);
   }
   if (g.wq) {
-    p.w_signed = g.wq == 1;
+    p.w_signed = g.wq == 1 || g.wq == 3;
+    p.w4 = g.wq >= 3;
     p.wzp_present = g.wzp != nullptr;
     p.kb_per_q = g.qblock >= g.K ? (1 << 30) : (int)(g.qblock / kTileK);
   }

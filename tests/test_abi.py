@@ -161,6 +161,29 @@ def test_policy_and_status_strings(lib):
     assert qg.mm_version() == "0.1.0"
 
 
+def test_grouped_qweights_4bit_validation(lib):
+    # 4-bit weights and zero points (MM_I4 = 10, MM_U4 = 11, packed two per
+    # byte): unit stride along N, N even and even outer strides, so that every
+    # row starts on a byte boundary
+    ref = ctypes.byref
+    x, gi = T((6, 8), 0), T((6, 2), 4)
+    call = lib.mm_grouped_matmul_qweights
+    s16, out16 = T((3, 1, 16), 0), T((6, 2, 16), 0)
+
+    def run(wq, s=s16, zp=None, out=out16):
+        return call(ref(x), ref(wq), ref(s), None if zp is None else ref(zp), 0, ref(gi), None, ref(out), None, 0,
+                    None)
+    assert run(T((3, 8, 15), 10), T((3, 1, 15), 0), out=T((6, 2, 15), 0)) == 2            # odd N
+    assert run(T((3, 8, 16), 10, strides=(256, 32, 2))) == 2                                 # N not unit-stride
+    assert run(T((3, 8, 16), 10, strides=(136, 17, 1))) == 2                                 # odd row stride
+    assert run(T((3, 8, 16), 11), zp=T((3, 1, 16), 11, strides=(17, 16, 1))) == 2           # zero point, odd stride
+    assert run(T((3, 8, 16), 10), zp=T((3, 1, 16), 11)) == 3                                 # zero point of the other type
+    assert run(T((3, 8, 16), 10), zp=T((3, 1, 16), 8)) == 3                                  # an 8-bit zero point
+    # no other operator takes 4-bit values
+    assert lib.mm_matmul(ref(T((4, 8), 10)), ref(T((8, 6), 10)), ref(T((4, 6), 10)), None) == 3
+    assert lib.mm_grouped_matmul(ref(x), ref(T((3, 8, 16), 11)), ref(gi), None, ref(out16), None, 0, None) == 3
+
+
 def test_grouped_qweights_validation(lib):
     # input bf16 [6,8]; int8 weights [3,8,16]; scales bf16 [3, ceil(8/B), 16]
     ref = ctypes.byref

@@ -186,3 +186,97 @@ def test_qweights_matches_dequantize_then_grouped():
     ref, scale = _oracle(d)
     assert max_rel_err(to_np(y), ref, scale) <= 1e-2
     assert max_rel_err(to_np(y2), ref, scale) <= 1e-2
+
+
+# ------------------------------------------------------------------ 4-bit experts (int4 / uint4, two per byte)
+
+def _pack4(v):
+    """Values in [-8, 15] as packed bytes [..., N/2], the even column in the low nibble."""
+    u = (np.asarray(v) & 15).astype(np.uint8)
+    return u[..., 0::2] | (u[..., 1::2] << 4)
+
+
+def _case4(M, K, N, G, S, dtype, kind, block, with_zp, with_bias, seed, p=None):
+    g = np.random.default_rng(seed)
+    kb = -(-K // (block or K))
+    signed = kind == "int4"
+    q = g.integers(-8, 8, (G, K, N)) if signed else g.integers(0, 16, (G, K, N))
+    zp = (g.integers(-3, 4, (G, kb, N)) if signed else g.integers(6, 10, (G, kb, N))) if with_zp else None
+    x = torch.from_numpy(g.standard_normal((M, K))).to(dtype)
+    scale = torch.from_numpy(g.uniform(0.5, 1.5, (G, kb, N)) / 8.0).to(dtype)
+    bias = torch.from_numpy(g.standard_normal((G, N))).to(dtype) if with_bias else None
+    probs = p if p is not None else np.full(G, 1.0 / G)
+    gi = torch.from_numpy(g.choice(G, size=(M, S), p=probs).astype(np.int32))
+    wq = _pack4(q)
+    assert np.array_equal(oracle.unpack_4bit(wq, signed), q)    # the layout the oracle reads
+    d = {"input": x, "weights_q": torch.from_numpy(wq), "w_scale": scale,
+         "w_zero_point": None if zp is None else torch.from_numpy(_pack4(zp)), "block_size": block,
+         "group_indices": gi, "bias": bias}
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    d["packed4"] = kind
+    return d
+
+
+def _run4(d):
+    return qg.mm_grouped_matmul_qweights(d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"],
+                                         d["block_size"], d["group_indices"], d["bias"], packed4=d["packed4"])
+
+
+def _unpacked4(d):
+    signed = d["packed4"] == "int4"
+    wq = oracle.unpack_4bit(d["weights_q"].cpu().numpy(), signed)
+    zp = None if d["w_zero_point"] is None else oracle.unpack_4bit(d["w_zero_point"].cpu().numpy(), signed)
+    return wq, zp
+
+
+def _check4(d, tol):
+    y = _run4(d)
+    t = T_NAME[d["input"].dtype]
+    wq, zp = _unpacked4(d)
+    args = (to_np(d["input"]), wq, to_np(d["w_scale"]), zp, d["block_size"], d["group_indices"].cpu().numpy(),
+            None if d["bias"] is None else to_np(d["bias"]), t)
+    ref, scale = oracle.grouped_matmul_qweights(*args), oracle.grouped_qweights_abs_scale(*args)
+    assert max_rel_err(to_np(y), ref, scale) <= tol
+    return y
+
+
+@pytest.mark.parametrize("policy", [qg.MM_PATH_SIMT, qg.MM_PATH_TENSOR], ids=["simt", "tensor"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("kind", ["int4", "uint4"])
+@pytest.mark.parametrize("block,with_zp,with_bias", [(0, True, True), (0, False, False), (64, True, False)])
+def test_qweights_4bit(policy, dtype, kind, block, with_zp, with_bias):
+    # K = 330: a partial last k-block; N = 384 (192 bytes a row): a partial
+    # column tile on the tensor cores.
+    d = _case4(300, 330, 384, 4, 2, dtype, kind, block, with_zp, with_bias, 71, p=[0.5, 0.3, 0.15, 0.05])
+    with path(policy):
+        _check4(d, TOL[dtype])
+    assert qg.mm_last_path() == policy
+    assert qg.mm_get_device_status() == "MM_OK"
+
+
+@pytest.mark.parametrize("kind", ["int4", "uint4"])
+def test_qweights_4bit_f32_simt(kind):
+    d = _case4(100, 70, 48, 3, 2, torch.float32, kind, 16, True, True, 72)
+    _check4(d, TOL[torch.float32])
+    assert qg.mm_last_path() == qg.MM_PATH_SIMT
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("kind", ["int4", "uint4"])
+def test_qweights_4bit_tensor_dequantized_values_exact(dtype, kind):
+    # One-hot input rows: output[m, i, :] = W[g, k(m), :], so the converters'
+    # nibble unpacking and arithmetic must give the oracle's dequantized
+    # weights bit for bit, over 16 k-blocks (K = 1024) and two column tiles.
+    M, K, N, G = 1024, 1024, 512, 2
+    d = _case4(M, K, N, G, 1, dtype, kind, 128, True, False, 73)
+    x = torch.zeros((M, K), dtype=dtype)
+    ks = np.arange(M) % K
+    x[np.arange(M), ks] = 1
+    d["input"] = x.to(DEV)
+    with path(qg.MM_PATH_TENSOR):
+        y = _run4(d)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    wq, zp = _unpacked4(d)
+    w = oracle.dequantize_linear(wq, to_np(d["w_scale"]), zp, 128, T_NAME[dtype])
+    gi = d["group_indices"].cpu().numpy()
+    assert np.array_equal(to_np(y)[:, 0, :], w[gi[:, 0], ks, :])

@@ -559,6 +559,27 @@ def test_dequantize_worked_values():
     assert ORC.dequantize_linear(qu, np.array([[[2.0, 0.25]]]), None, 1, "f16").tolist() == [[[0.0, 63.75]]]
 
 
+def test_unpack_4bit_layout():
+    # Two values per byte, the even element in the low nibble: 0x7F holds
+    # (15, 7), 0x80 holds (0, 8), 0x0F holds (15, 0); as int4, nibbles of 8
+    # and above are negative (15 -> -1, 8 -> -8).
+    b = np.array([[0x7F, 0x80, 0x0F]], dtype=np.uint8)
+    assert oracle.unpack_4bit(b, False).tolist() == [[15, 7, 0, 8, 15, 0]]
+    assert oracle.unpack_4bit(b, True).tolist() == [[-1, 7, 0, -8, -1, 0]]
+    assert oracle.unpack_4bit(b, True).dtype == np.int8 and oracle.unpack_4bit(b, False).dtype == np.uint8
+
+
+def test_dequantize_4bit_worked_values():
+    # int4 [-8, 7] and uint4 [0, 15] by hand: (-8 - 3) * 0.5 = -5.5,
+    # (7 + 1) * 1.25 = 10, (15 - 9) * 0.75 = 4.5, (0 - 9) * 0.75 = -6.75.
+    q = oracle.unpack_4bit(np.array([[[0x78]]], dtype=np.uint8), True)      # [[[-8, 7]]]
+    zp = oracle.unpack_4bit(np.array([[[0xF3]]], dtype=np.uint8), True)     # [[[3, -1]]]
+    assert ORC.dequantize_linear(q, np.array([[[0.5, 1.25]]]), zp, None, "bf16").tolist() == [[[-5.5, 10.0]]]
+    qu = oracle.unpack_4bit(np.array([[[0x0F]]], dtype=np.uint8), False)    # [[[15, 0]]]
+    zu = oracle.unpack_4bit(np.array([[[0x99]]], dtype=np.uint8), False)    # [[[9, 9]]]
+    assert ORC.dequantize_linear(qu, np.array([[[0.75, 0.75]]]), zu, None, "f16").tolist() == [[[4.5, -6.75]]]
+
+
 def test_dequantize_rounds_once_to_the_scale_type():
     # 255 * 1.5 = 382.5: bfloat16 spacing is 2 in [256, 512), so 382; exact in float16.
     q = np.array([[[127]]], dtype=np.int8)
