@@ -490,6 +490,10 @@ def bench_extra_workloads(dev, world, stream, peaks, peak_kind, cpu=True):
     for block in (0, 128):
         out["grouped_qweights_b%d" % block] = bench_grouped_q(workloads.grouped_qweights(device=dev, block=block),
                                                               world, stream, bf16_peak)
+    # The same with int4 experts (two weights per byte, 1.9 GB), one scale per
+    # group and column.
+    out["grouped_qweights4_b0"] = bench_grouped_q(workloads.grouped_qweights(device=dev, bits=4), world, stream,
+                                                  bf16_peak)
     return out
 
 
@@ -558,18 +562,22 @@ def bench_grouped(d, world, stream, peak, cpu=False):
 def bench_grouped_q(d, world, stream, peak):
     import quantized_gemm_gb300 as qg
     x, wq, gi = d["input"], d["weights_q"], d["group_indices"]
+    p4 = d.get("packed4")
     M, K = x.shape
-    S, N = gi.shape[1], wq.shape[2]
+    S, N = gi.shape[1], wq.shape[2] * (2 if p4 else 1)
     yo = torch.empty((M, S, N), dtype=x.dtype, device=x.device)
     args = (x, wq, d["w_scale"], d["w_zero_point"], d["block_size"], gi)
-    ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*args), dtype=torch.uint8, device=x.device)
-    ms, _ = time_loop(lambda: qg.mm_grouped_matmul_qweights(*args, d["bias"], out=yo, workspace=ws), 10, 3, world,
-                      stream, idle_s=EXTRA_IDLE_S)
+    ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*args, packed4=p4), dtype=torch.uint8,
+                     device=x.device)
+    ms, _ = time_loop(lambda: qg.mm_grouped_matmul_qweights(*args, d["bias"], out=yo, workspace=ws, packed4=p4), 10,
+                      3, world, stream, idle_s=EXTRA_IDLE_S)
     assert qg.mm_last_path() == qg.MM_PATH_TENSOR
     tf = 2 * M * S * K * N / ms / 1e9
+    wdesc = p4 or "int8"
     res = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "bound": "tensor", "peak_tflops": peak,
-           "frac": tf / peak, "kernels_per_call": 4, "l2": "weights (3.8 GB int8) larger than L2",
-           "types": "input %s, weights int8, block %s" % (x.dtype, d["block_size"] or "K")}
+           "frac": tf / peak, "kernels_per_call": 4,
+           "l2": "weights (%.1f GB %s) larger than L2" % (wq.numel() / 1e9, wdesc),
+           "types": "input %s, weights %s, block %s" % (x.dtype, wdesc, d["block_size"] or "K")}
     del d, x, wq, gi, yo, ws
     torch.cuda.empty_cache()
     return res
@@ -741,6 +749,7 @@ PER_CONFIG = (
     ("f1_qlinear_s8_batched4", "qlinear_s8_batched4", ("value", "frac")),
     ("f2_grouped_qweights_b0", "grouped_qweights_b0", ("value", "frac")),
     ("f2_grouped_qweights_b128", "grouped_qweights_b128", ("value", "frac")),
+    ("f2_grouped_qweights_int4", "grouped_qweights4_b0", ("value", "frac")),
     ("f3_grouped_f16_i64", "grouped_f16_i64", ("value", "frac")),
     ("f4_gemm_f32", "gemm_f32", ("value", "ms_per_call", "frac")),
     ("a3_skinny_m16", "gemm_bf16_skinny_m16", ("value", "unit", "us_per_call_in_graph", "frac")),
@@ -887,13 +896,17 @@ def run_profile_workload(args):
         ws = torch.empty(qg.mm_qlinear_matmul_workspace_size(d["a"], d["b"]), dtype=torch.uint8, device=dev)
         step = lambda: qg.mm_qlinear_matmul(*[d[k] for k in keys], out=yq, workspace=ws)
     elif name.startswith("grouped_qweights"):
-        # grouped_qweights_b128: blocks of 128 rows; a _gN suffix: N groups (same M, K, N)
-        parts = dict((t[0], int(t[1:])) for t in name[len("grouped_qweights"):].split("_") if t)
-        d = workloads.grouped_qweights(device=dev, block=parts.get("b", 0), G=parts.get("g", 64))
+        # grouped_qweights_b128: blocks of 128 rows; a _gN suffix: N groups (same M, K, N);
+        # grouped_qweights4_...: int4 experts
+        bits = 4 if name.startswith("grouped_qweights4") else 8
+        parts = dict((t[0], int(t[1:])) for t in name[len("grouped_qweights") + (bits == 4):].split("_") if t)
+        d = workloads.grouped_qweights(device=dev, block=parts.get("b", 0), G=parts.get("g", 64), bits=bits)
+        p4 = d.get("packed4")
         yo = torch.empty((16384, 2, 14336), dtype=torch.bfloat16, device=dev)
         qargs = (d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"], d["block_size"], d["group_indices"])
-        ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*qargs), dtype=torch.uint8, device=dev)
-        step = lambda: qg.mm_grouped_matmul_qweights(*qargs, d["bias"], out=yo, workspace=ws)
+        ws = torch.empty(qg.mm_grouped_matmul_qweights_workspace_size(*qargs, packed4=p4), dtype=torch.uint8,
+                         device=dev)
+        step = lambda: qg.mm_grouped_matmul_qweights(*qargs, d["bias"], out=yo, workspace=ws, packed4=p4)
     elif name.startswith("grouped_bf16"):
         # grouped_bf16_g8: 8 groups (same M, K, N); a _nN suffix: N output
         # columns (a smaller case of the same routing, for full ncu captures)

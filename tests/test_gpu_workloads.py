@@ -266,3 +266,27 @@ def test_grouped_qweights_sampled_tokens_and_columns(block):
     scale = oracle.native.grouped_qweights_abs_scale(*args)
     assert max_rel_err(to_np(out[:, :, ct]), ref, scale) <= 1e-2
 
+
+
+def test_grouped_qweights_int4_all_rows_on_column_subset():
+    """int4 weight-only experts (two per byte) at the GroupedMatMul workload's
+    size: every routed row of every group on a column subset, against the C++
+    oracle given the unpacked values."""
+    d = workloads.grouped_qweights(device=DEV, bits=4)
+    out = qg.mm_grouped_matmul_qweights(d["input"], d["weights_q"], d["w_scale"], d["w_zero_point"],
+                                        d["block_size"], d["group_indices"], d["bias"], packed4=d["packed4"])
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    assert qg.mm_get_device_status() == "MM_OK"
+    cols = _cols(14336, 27)
+    ct = torch.from_numpy(cols).to(DEV)
+    # the bytes holding the subset's columns, unpacked: column c is element
+    # 2j + c % 2 of the unpacked subset when byte j is byte c // 2
+    bt = torch.from_numpy(cols // 2).to(DEV)
+    pick = 2 * np.arange(len(cols)) + cols % 2
+    wq = oracle.unpack_4bit(d["weights_q"][:, :, bt].cpu().numpy(), True)[:, :, pick]
+    zp = oracle.unpack_4bit(d["w_zero_point"][:, :, bt].cpu().numpy(), True)[:, :, pick]
+    args = (to_np(d["input"]), wq, to_np(d["w_scale"][:, :, ct]), zp, 0, d["group_indices"].cpu().numpy(),
+            to_np(d["bias"][:, ct]), "bf16")
+    ref = oracle.native.grouped_matmul_qweights(*args)
+    scale = oracle.native.grouped_qweights_abs_scale(*args)
+    assert max_rel_err(to_np(out[:, :, ct]), ref, scale) <= 1e-2

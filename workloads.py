@@ -177,7 +177,8 @@ def grouped_bf16(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, dty
     }
 
 
-def grouped_qweights(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, block=0, dtype=torch.bfloat16):
+def grouped_qweights(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2, block=0, dtype=torch.bfloat16,
+                     bits=8):
     """The GroupedMatMul workload with weight-only int8 experts.
 
     Same input, routing and bias as ``grouped_bf16``; weights_q int8 [G,K,N]
@@ -185,8 +186,25 @@ def grouped_qweights(device="cuda", seed=0, M=16384, K=4096, N=14336, G=64, S=2,
     uniform on (1.5e-4, 2.7e-4) rounded to ``dtype``, one per group and output
     column (block 0) or per ``block`` rows of K, so that the dequantized
     weights have about the standard deviation 1/64 of the bf16 workload.
+
+    bits=4: int4 experts stored two per byte along N (uint8 [G, K, N/2] and
+    zero points [G, Kb, N/2], the even column in the low nibble; pass
+    ``packed4="int4"``): values uniform on {-8..7} (uniform random bytes),
+    zero points on {-1..1}, scales 16 times larger (2.4e-3, 4.3e-3).
     """
     kb = 1 if block == 0 else -(-K // block)
+    if bits == 4:
+        z = uniform_int((G, kb, N), -1, 1, torch.int8, device, seed + 5).to(torch.int16) & 15
+        return {
+            "input": normal((M, K), device, seed, 1.0, dtype),
+            "weights_q": uniform_int((G, K, N // 2), 0, 255, torch.uint8, device, seed + 1),
+            "w_scale": uniform((G, kb, N), 2.4e-3, 4.3e-3, device, seed + 4, dtype),
+            "w_zero_point": (z[..., 0::2] | (z[..., 1::2] << 4)).to(torch.uint8),
+            "block_size": block,
+            "bias": normal((G, N), device, seed + 2, 0.1, dtype),
+            "group_indices": zipf_two_distinct(M, G, S, 1.1, device, seed + 3),
+            "packed4": "int4",
+        }
     return {
         "input": normal((M, K), device, seed, 1.0, dtype),
         "weights_q": uniform_int((G, K, N), -128, 127, torch.int8, device, seed + 1),
