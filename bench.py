@@ -736,7 +736,8 @@ def compact(entry, keys):
 
 
 # Workload name in the detail -> key in per_config: the five configurations,
-# then the type variants at the same sizes.
+# then the type variants (other operand, scale and index types, int8 and int4
+# experts, fp32) at the same sizes.
 PER_CONFIG = (
     ("1_matmul_f32", "matmul_f32", ("value", "unit", "us_per_call", "us_per_graph_replay", "paths",
                                     "cpu_baseline")),

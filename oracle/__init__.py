@@ -6,8 +6,7 @@ code with the CUDA path: nothing under ``quantized_gemm_gb300/`` may import it,
 and it imports nothing from there.  Only ``tests/``, ``__graft_entry__.smoke()``
 and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.
 
-Arithmetic conventions (readings of the pages, listed with reasons in the
-design notes):
+Arithmetic conventions (readings of points the pages leave open):
 
 * Floating point: every input is widened exactly to float64 and the
   contraction is done in float64; results are returned unrounded (float64).

@@ -5,7 +5,7 @@ experts are expressed by applying DequantizeLinear, with the weights' scales
 and zero points, to the quantized weights and passing the result to
 GroupedMatMul; a runtime may fuse the two so that the dequantized [G, K, N]
 weights are never formed.  The pages name DequantizeLinear without defining
-it.  The reading used here (the plainest one; listed in the design notes):
+it.  The reading used here (the plainest one):
 
 * weights_q [G, K, N] of int8 or uint8, or of DequantizeLinear's 4-bit
   types int4 / uint4 (values in [-8, 7] / [0, 15]).  4-bit tensors are stored

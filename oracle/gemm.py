@@ -10,7 +10,7 @@ its definition paragraph and its Inputs / Outputs sections:
 * C is optional; when it is absent the computation is done as if C were the
   scalar 0.  When present, C is unidirectionally broadcastable to (M, N).
 
-Readings of points the page leaves open (each is listed in the design notes):
+Readings of points the page leaves open:
 
 * Defaults are alpha = 1.0, beta = 1.0, transA = transB = 0; they are not
   printed, but the examples test_cc_gemm_default, test_cc_gemm_alpha,

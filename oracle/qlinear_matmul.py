@@ -18,7 +18,7 @@ What is computed, in the order the page gives it:
    round-to-nearest with ties to even and saturate clamps to the range of the
    output type T3 (int8: [-128, 127], uint8: [0, 255]).
 
-Readings (listed in the design notes):
+Readings of points the page leaves open:
 
 * x is evaluated in IEEE float32 as  s = a_scale * b_scale;  v = float(acc) * s;
   q = v / y_scale;  r = rint(q);  t = r + float(y_zero_point);
