@@ -280,3 +280,29 @@ def test_qweights_4bit_tensor_dequantized_values_exact(dtype, kind):
     w = oracle.dequantize_linear(wq, to_np(d["w_scale"]), zp, 128, T_NAME[dtype])
     gi = d["group_indices"].cpu().numpy()
     assert np.array_equal(to_np(y)[:, 0, :], w[gi[:, 0], ks, :])
+
+
+@pytest.mark.parametrize("kind", ["int4", "uint4"])
+def test_qweights_4bit_tensor_extreme_scales_exact(kind):
+    # As for 8-bit weights: bf16 scales by blocks of 8 columns, ordinary ones
+    # (fused multiply-add form) and ones of 2^100 and more (subtract-then-
+    # multiply form) alternating, must give the oracle's dequantized weights
+    # bit for bit with one-hot input rows.
+    M, K, N, G = 256, 192, 256, 2
+    d = _case4(M, K, N, G, 1, torch.bfloat16, kind, 0, True, False, 74)
+    ordinary = [1 + 2.0 ** -7, 2.0 ** -120, 0.75, 3 * 2.0 ** 90]
+    huge = [2.0 ** 110, 3 * 2.0 ** 105, 1 + 2.0 ** -7, 2.0 ** -120]
+    cols = [(huge if (n // 8) % 2 else ordinary)[n % 4] for n in range(N)]
+    d["w_scale"] = torch.tensor(cols, dtype=torch.float64).reshape(1, 1, N).expand(G, 1, N).to(
+        torch.bfloat16).contiguous().to(DEV)
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    ks = np.arange(M) % K
+    x[np.arange(M), ks] = 1
+    d["input"] = x.to(DEV)
+    with path(qg.MM_PATH_TENSOR):
+        y = _run4(d)
+    assert qg.mm_last_path() == qg.MM_PATH_TENSOR
+    wq, zp = _unpacked4(d)
+    w = oracle.dequantize_linear(wq, to_np(d["w_scale"]), zp, 0, "bf16")
+    gi = d["group_indices"].cpu().numpy()
+    assert np.array_equal(to_np(y)[:, 0, :], w[gi[:, 0], ks, :])
