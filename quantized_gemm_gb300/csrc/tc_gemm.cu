@@ -680,7 +680,7 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
           for (int i = 0; i < kRows; ++i) {
             const int k = k_first + kRowStep * i;
             uint32_t qx, qy;
-          row_bytes(raw[i], qx, qy);
+            row_bytes(raw[i], qx, qy);
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
@@ -705,7 +705,7 @@ __device__ void run_convert(const TcParams& p, uint8_t* smem, uint32_t sbase, ui
           for (int i = 0; i < kRows; ++i) {
             const int k = k_first + kRowStep * i;
             uint32_t qx, qy;
-          row_bytes(raw[i], qx, qy);
+            row_bytes(raw[i], qx, qy);
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
