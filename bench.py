@@ -760,6 +760,19 @@ PER_CONFIG = (
 )
 
 
+def per_config_entries(headline, extras):
+    """The line's per_config object: the headline Gemm's entry and the compact
+    entry (PER_CONFIG) of every other workload measured, sorted by key; an
+    error of the other workloads is kept, cut to 200 characters."""
+    per_config = {"2_gemm_bf16": headline}
+    for key, name, keys in PER_CONFIG:
+        if name in extras:
+            per_config[key] = compact(extras[name], keys)
+    if "error" in extras:
+        per_config["error"] = extras["error"][:200]
+    return dict(sorted(per_config.items()))
+
+
 def run_ours(args, rank, world, local):
     import quantized_gemm_gb300 as qg
     from quantized_gemm_gb300 import build as qbuild
@@ -814,14 +827,8 @@ def run_ours(args, rank, world, local):
             extras = {"error": "%s: %s" % (type(exc).__name__, exc)}
 
     # (the headline's roofline and CPU baseline are in the line itself)
-    per_config = {"2_gemm_bf16": {"value": _r(tflops_rank), "unit": "TFLOP/s", "ms_per_call": _r(ms),
-                                  "frac": _r(tflops_rank / peak)}}
-    for key, name, keys in PER_CONFIG:
-        if name in extras:
-            per_config[key] = compact(extras[name], keys)
-    if "error" in extras:
-        per_config["error"] = extras["error"][:200]
-    per_config = dict(sorted(per_config.items()))
+    per_config = per_config_entries({"value": _r(tflops_rank), "unit": "TFLOP/s", "ms_per_call": _r(ms),
+                                     "frac": _r(tflops_rank / peak)}, extras)
 
     traffic = stored_traffic("tc_gemm_kernel_gemm_bf16_8192")
     line = {
