@@ -24,7 +24,11 @@
  *   once one call has run on the device (it caches per-device properties)
  *   they can be captured in a CUDA graph and replayed.  Device-side conditions (an out-of-range
  *   group index, a pipeline wait that timed out) are recorded in a per-device
- *   status word read with mm_get_device_status().
+ *   status word read with mm_get_device_status().  Every kernel is launched
+ *   with programmatic stream serialization: it may be scheduled while the
+ *   previous kernel on the stream is finishing, and waits for that kernel to
+ *   complete (and its memory to be visible) before its first global-memory
+ *   access, so stream order is kept for any work before or after a call.
  * Memory.  The library never allocates device memory.  Operators whose fast
  *   path needs scratch space (QLinearMatMul, GroupedMatMul) take a
  *   caller-provided workspace whose size is given by the matching
